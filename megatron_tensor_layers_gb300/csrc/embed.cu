@@ -1,0 +1,114 @@
+// Vocab-parallel input embedding (page "Tensor parallelism from scratch",
+// tp.py VocabParallelEmbedding; page "vLLM source analysis 13: tensor
+// parallelism in detail", §2.4.1).
+//
+// Rank r owns ids [r*per, min((r+1)*per, V)), per = ceil(V/t).  Its output
+// for an id outside its range is exactly 0 (masked_fill, so a NaN row of
+// another rank never leaks), and the t outputs are all-reduced (summed in
+// rank order).  Ranges are disjoint, so for every token at most one rank
+// holds a real row: the kernel reads that one row (one warp per token,
+// 16-byte loads) and forms the rank-order sum of it and t-1 exact zeros in
+// float32.  That sum is bit-exact to the lookup, except that -0.0 becomes
+// +0.0 when t > 1, which is what summing the ranks' outputs gives.
+// Bytes moved per token: h*b read (owner row) + h*b written (+ t*h*b for the
+// optional per-rank outputs) + 4 for the id.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tpk {
+
+struct EmbedArgs {
+    const void* table[TP_MAX_SHARDS];
+    void* partials[TP_MAX_SHARDS];
+    const int32_t* ids;
+    void* out;
+    int64_t vocab, h, n, per;
+    int t;
+    int with_partials;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) vocab_embed_kernel(const __grid_constant__ EmbedArgs a) {
+    constexpr int VEC = BF16 ? 8 : 4;             // elements per 16-byte vector
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t nvec = a.h / VEC;
+    for (int64_t tok = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; tok < a.n; tok += warps) {
+        const int64_t id = a.ids[tok];
+        int owner = -1;
+        int64_t local = 0;
+        if (id >= 0 && id < a.vocab) {
+            owner = static_cast<int>(id / a.per);
+            local = id - static_cast<int64_t>(owner) * a.per;
+        }
+        const uint4* src = owner >= 0 ? reinterpret_cast<const uint4*>(a.table[owner]) + local * nvec : nullptr;
+        uint4* dst = reinterpret_cast<uint4*>(a.out) + tok * nvec;
+        for (int64_t v = lane; v < nvec; v += 32) {
+            const uint4 row = owner >= 0 ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+            const uint32_t w[4] = {row.x, row.y, row.z, row.w};
+            float x[VEC];
+            if constexpr (BF16) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    x[2 * i] = __uint_as_float(w[i] << 16);
+                    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) x[i] = __uint_as_float(w[i]);
+            }
+            // The all-reduce: rank 0's masked output, then ranks 1..t-1 added in order.
+            float acc[VEC];
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc[i] = owner == 0 ? x[i] : 0.0f;
+            for (int r = 1; r < a.t; ++r) {
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) acc[i] = acc[i] + (owner == r ? x[i] : 0.0f);
+            }
+            uint4 o;
+            if constexpr (BF16) {
+                o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                               pack_bf16x2(acc[6], acc[7]));
+            } else {
+                o = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                               __float_as_uint(acc[3]));
+            }
+            dst[v] = o;
+            if (a.with_partials) {
+                for (int r = 0; r < a.t; ++r)
+                    reinterpret_cast<uint4*>(a.partials[r])[tok * nvec + v] = owner == r ? row : make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+}
+
+tp_status launch_vocab_embed(const EmbedDesc& d, cudaStream_t stream) {
+    if (d.n == 0) return TP_OK;
+    EmbedArgs a;
+    for (int r = 0; r < TP_MAX_SHARDS; ++r) {
+        a.table[r] = r < d.t ? d.table[r] : nullptr;
+        a.partials[r] = (d.with_partials && r < d.t) ? d.partials[r] : nullptr;
+    }
+    a.ids = d.ids;
+    a.out = d.out;
+    a.vocab = d.vocab;
+    a.h = d.h;
+    a.n = d.n;
+    a.per = d.per;
+    a.t = d.t;
+    a.with_partials = d.with_partials;
+    const int64_t threads = d.n * 32;
+    const int grid = static_cast<int>(std::min<int64_t>((threads + 255) / 256, 65535));
+    if (d.bf16)
+        vocab_embed_kernel<true><<<grid, 256, 0, stream>>>(a);
+    else
+        vocab_embed_kernel<false><<<grid, 256, 0, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+}  // namespace tpk

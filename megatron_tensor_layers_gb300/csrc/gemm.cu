@@ -1,0 +1,462 @@
+// Tensor-parallel GEMMs on the 5th-generation tensor core (sm_103a).
+//
+// One persistent, warp-specialised kernel family computes, for every shard
+// ("group") g of a tensor-parallel layer,
+//
+//     D_g = sum over K-segments s of  A_{g,s} · B_{g,s}^T        (fp32 accumulate)
+//
+// with A [M, K] and B [N, K] both K-major bf16 (weights are stored [out, in],
+// so x @ w^T is exactly this form).  It serves
+//   - ColumnParallelLinear: group = shard, A = the replicated input x,
+//     B = the shard's weight block (page "Nano-vLLM walkthrough 22", §3);
+//   - the gated MLP up-projection: B's tile is the shard's gate rows stacked
+//     on the SAME rows of its up block (the merged "double cut", §5 of the
+//     same page) and the epilogue writes act(gate) * up (page "Tensor
+//     parallelism from scratch", tp.py TPMLP);
+//   - RowParallelLinear: group = shard writing its own partial sum, or one
+//     group with t K-segments whose partial products are accumulated in rank
+//     order in the same TMEM accumulator ("fused" all-reduce, no partial is
+//     ever written) (page "6.2 Tensor-parallel inference", §1: Y = sum_i
+//     act(X A_i) B_i);
+//   - the vocab-sharded LM head: group = shard, the epilogue writes straight
+//     into the shard's column slice of the full logits (zero-copy gather).
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0  lane 0: TMA producer, fills a STAGES-deep ring of A/B tiles;
+//   warp 1  lane 0: MMA issuer (tcgen05.mma, 128 x BN x 16 per instruction)
+//           into one of two TMEM accumulators; the whole warp allocates TMEM;
+//   warps 2-5: epilogue, 128 threads = the 128 TMEM lanes = the tile's rows;
+//           they drain one accumulator while the MMA fills the other.
+// Every barrier wait is bounded (1 s); a wait that expires records
+// TP_ERR_TIMEOUT and the CTA unwinds and exits normally.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tpk {
+
+constexpr int BM = 128;          // tile rows (tokens) = TMEM lanes
+constexpr int BK = 64;           // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kThreads = 192;
+constexpr int kGroupM = 16;      // tile raster: bands of 16 row-tiles share B tiles in L2
+
+enum { EPI_STORE = 0, EPI_GLU = 1 };
+
+struct GemmArgs {
+    CUtensorMap mapA[TP_MAX_SHARDS];
+    CUtensorMap mapB[TP_MAX_SHARDS];
+    void* out[TP_MAX_SHARDS];         // per-group output base (already offset for a gather)
+    const void* bias[TP_MAX_SHARDS];  // per-group bf16 bias over output columns, or null
+    int64_t ldo;                      // output row stride (elements)
+    int out_f32;                      // 1: float32 output, 0: bf16
+    int M;                            // rows of A / D
+    int N;                            // output columns per group (widest group)
+    int n_valid[TP_MAX_SHARDS];       // valid output columns of each group
+    int m_tiles, n_tiles, groups, total_tiles;
+    int k_blocks;                     // K blocks per segment
+    int segs;                         // K segments accumulated into one tile
+    int a_per_group;                  // A map index = group (else 0); with segs > 1 it is the segment
+    int glu_up_row;                   // row offset of the up block inside B (gated epilogue)
+    int act;                          // tp_act for the gated epilogue
+    int* status;                      // library status word
+};
+
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g, int& m, int& n) {
+    const int per_group = a.m_tiles * a.n_tiles;
+    g = tile / per_group;
+    const int l = tile - g * per_group;
+    const int width = kGroupM * a.n_tiles;
+    const int band = l / width;
+    const int first_m = band * kGroupM;
+    const int gm = min(a.m_tiles - first_m, kGroupM);
+    const int r = l - band * width;
+    m = first_m + r % gm;
+    n = r / gm;
+}
+
+__device__ __forceinline__ float act_fn(float g, int act) {
+    if (act == TP_ACT_GELU_TANH_MUL) {
+        const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+        return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
+    }
+    return g / (1.0f + __expf(-g));  // SiLU
+}
+
+// Store 32 consecutive fp32 values of one output row, columns [col0, col0 + nvalid).
+__device__ __forceinline__ void store_chunk(void* base, int64_t ldo, int out_f32, int64_t row, int col0, int nvalid,
+                                            const float (&v)[32]) {
+    if (nvalid <= 0) return;
+    if (out_f32) {
+        float* p = static_cast<float*>(base) + row * ldo + col0;
+        if (nvalid == 32 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                reinterpret_cast<float4*>(p)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < nvalid) p[j] = v[j];
+        }
+    } else {
+        uint16_t* p = static_cast<uint16_t*>(base) + row * ldo + col0;
+        if (nvalid == 32 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint4 q;
+                q.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+                q.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+                q.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+                q.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+                reinterpret_cast<uint4*>(p)[j] = q;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < nvalid) p[j] = f32_to_bf16(v[j]);
+        }
+    }
+}
+
+template <int BN, int STAGES, int EPI>
+struct GemmCfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;                 // two accumulators
+    static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int OUT_COLS = (EPI == EPI_GLU) ? BN / 2 : BN;   // output columns per tile
+    static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+    static_assert(BN % 16 == 0 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
+    static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+};
+
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_constant__ GemmArgs args) {
+    using Cfg = GemmCfg<BN, STAGES, EPI>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned base for the swizzled tiles.
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const uint32_t bar_base = base + STAGES * Cfg::STAGE_BYTES;
+    uint8_t* bar_ptr = base_ptr + STAGES * Cfg::STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * (2 * STAGES + 4) + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 128);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < args.groups && i < TP_MAX_SHARDS; ++i) prefetch_tmap(&args.mapB[i]);
+        prefetch_tmap(&args.mapA[0]);
+    }
+    if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(smem_u32(tmem_slot));
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int kb_per_tile = args.k_blocks * args.segs;
+    bool aborted = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < args.total_tiles && !aborted; tile += gridDim.x) {
+                int g, m, n;
+                tile_coords(args, tile, g, m, n);
+                for (int kk = 0; kk < kb_per_tile; ++kk) {
+                    const int seg = kk / args.k_blocks;
+                    const int kb = kk - seg * args.k_blocks;
+                    const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                    const int bi = args.segs > 1 ? seg : g;
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
+                        aborted = true;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
+                    const uint32_t sb = sa + Cfg::A_BYTES;
+                    mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                    tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);
+                    if (EPI == EPI_GLU) {
+                        tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * (BN / 2));
+                        tma_load_2d(sb + (BN / 2) * 128, &args.mapB[bi], full_bar(stage), kb * BK,
+                                    args.glu_up_row + n * (BN / 2));
+                    } else {
+                        tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * BN);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = mma_idesc_bf16(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int tile = blockIdx.x; tile < args.total_tiles && !aborted; tile += gridDim.x) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kk = 0; kk < kb_per_tile; ++kk) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.status)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        // advance 16 bf16 = 32 bytes along K inside the swizzle row
+                        tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (aborted) break;
+                tc_commit(tfull_bar(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x) {
+            int g, m, n;
+            tile_coords(args, tile, g, m, n);
+            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            const int64_t grow = static_cast<int64_t>(m) * BM + row_in_tile;
+            const bool row_ok = grow < args.M;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            void* out = args.out[g];
+            const uint16_t* bias = static_cast<const uint16_t*>(args.bias[g]);
+            const int ncols = args.n_valid[g];
+            if (EPI == EPI_GLU) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t rg[32], ru[32];
+                    tmem_ld32(taddr + c * 32, rg);
+                    tmem_ld32(taddr + BN / 2 + c * 32, ru);
+                    tmem_ld_wait();
+                    const int col0 = n * (BN / 2) + c * 32;
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = act_fn(__uint_as_float(rg[j]), args.act) * __uint_as_float(ru[j]);
+                    if (row_ok) store_chunk(out, args.ldo, args.out_f32, grow, col0, min(32, ncols - col0), v);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + c * 32, r);
+                    tmem_ld_wait();
+                    const int col0 = n * BN + c * 32;
+                    const int nvalid = min(32, ncols - col0);
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if (bias != nullptr) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nvalid) v[j] += bf16_to_f32(bias[col0 + j]);
+                    }
+                    if (row_ok) store_chunk(out, args.ldo, args.out_f32, grow, col0, nvalid, v);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    if (aborted) spin_ns(50000);    // let issued TMA copies and MMAs land before teardown
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) spin_ns(50000);
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc<Cfg::TMEM_COLS>(tmem_base);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// bf16 K-major operand [rows, cols] with row stride ld (elements), tiles of
+// box_rows x 64 with 128-byte swizzle; out-of-range elements read as zero.
+static bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static int cache[64] = {0};
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+template <int BN, int STAGES, int EPI>
+static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream) {
+    using Cfg = GemmCfg<BN, STAGES, EPI>;
+    a.n_tiles = (d.N + Cfg::OUT_COLS - 1) / Cfg::OUT_COLS;
+    a.total_tiles = a.groups * a.m_tiles * a.n_tiles;
+    if (a.total_tiles == 0) return TP_OK;
+    const int b_box = (EPI == EPI_GLU) ? BN / 2 : BN;
+    const int nA = d.segs > 1 ? d.segs : (d.a_per_group ? d.groups : 1);
+    const int nB = d.segs > 1 ? d.segs : d.groups;
+    for (int i = 0; i < nA; ++i)
+        if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, BM)) return TP_ERR_CUDA;
+    for (int i = 0; i < nB; ++i) {
+        const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
+        if (!make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box)) return TP_ERR_CUDA;
+    }
+    auto kern = tp_gemm_kernel<BN, STAGES, EPI>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+        return TP_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return TP_ERR_CUDA;
+    const int grid = std::min(a.total_tiles, sms);
+    kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// Estimated time units of a launch with output tile width w: whole waves of
+// tiles times the per-tile cost (proportional to the MMA N plus a fixed
+// share for the A tile).
+static long long plan_cost(int tiles, int bn, int sms) {
+    const long long waves = (tiles + sms - 1) / sms;
+    return waves * (bn + 32);
+}
+
+tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int g = 0; g < d.groups; ++g) {
+        a.out[g] = d.out[g];
+        a.bias[g] = d.bias[g];
+        a.n_valid[g] = static_cast<int>(d.n_valid[g] > 0 ? d.n_valid[g] : d.N);
+    }
+    a.ldo = d.ldo;
+    a.out_f32 = d.out_f32;
+    a.M = static_cast<int>(d.M);
+    a.N = static_cast<int>(d.N);
+    a.m_tiles = static_cast<int>((d.M + BM - 1) / BM);
+    a.groups = d.groups;
+    a.k_blocks = static_cast<int>((d.K + BK - 1) / BK);
+    a.segs = d.segs;
+    a.a_per_group = d.a_per_group;
+    a.glu_up_row = static_cast<int>(d.glu_up_row);
+    a.act = d.act;
+    a.status = d.status;
+    if (d.M == 0 || d.N == 0) return TP_OK;
+
+    const int sms = std::max(1, sm_count());
+    const bool glu = d.glu != 0;
+    // Candidate MMA widths, largest first; pick the one with the lowest cost.
+    const int cands[3] = {256, 128, 64};
+    int best = 256;
+    long long best_cost = -1;
+    for (int bn : cands) {
+        const int out_cols = glu ? bn / 2 : bn;
+        const int tiles = d.groups * a.m_tiles * static_cast<int>((d.N + out_cols - 1) / out_cols);
+        const long long c = plan_cost(tiles, bn, sms);
+        if (best_cost < 0 || c < best_cost) {
+            best_cost = c;
+            best = bn;
+        }
+    }
+    if (d.force_bn) best = d.force_bn;
+    if (glu) {
+        if (best == 256) return launch_cfg<256, 4, EPI_GLU>(a, d, stream);
+        if (best == 128) return launch_cfg<128, 6, EPI_GLU>(a, d, stream);
+        return launch_cfg<64, 8, EPI_GLU>(a, d, stream);
+    }
+    if (best == 256) return launch_cfg<256, 4, EPI_STORE>(a, d, stream);
+    if (best == 128) return launch_cfg<128, 6, EPI_STORE>(a, d, stream);
+    return launch_cfg<64, 8, EPI_STORE>(a, d, stream);
+}
+
+}  // namespace tpk

@@ -1,0 +1,78 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tp.h"
+
+namespace tpk {
+
+// One tensor-parallel GEMM launch: for each group g,
+//   D_g = sum_s A_{g,s} B_{g,s}^T, A [M, K] (lda), B [b_rows, K] (ldb), bf16.
+struct GemmDesc {
+    int64_t M = 0, N = 0, K = 0;        // K = per-segment depth
+    int groups = 1;                      // independent outputs (shards)
+    int segs = 1;                        // K segments summed into one output (fused reduce)
+    int a_per_group = 0;                 // A operand differs per group
+    const void* a[TP_MAX_SHARDS] = {};   // per group (a_per_group), per segment (segs > 1), or a[0]
+    int64_t lda = 0;
+    const void* b[TP_MAX_SHARDS] = {};   // per group, or per segment
+    int64_t ldb = 0;
+    int64_t b_rows = 0;                  // rows of each B matrix
+    int64_t n_valid[TP_MAX_SHARDS] = {}; // per-group output width when groups differ (0: use N)
+    int glu = 0;                         // gated epilogue: B = [gate rows; up rows]
+    int64_t glu_up_row = 0;              // first up row inside B
+    int act = TP_ACT_NONE;
+    void* out[TP_MAX_SHARDS] = {};       // per-group output base
+    const void* bias[TP_MAX_SHARDS] = {};
+    int64_t ldo = 0;
+    int out_f32 = 0;
+    int* status = nullptr;
+    int force_bn = 0;                    // 0: chosen by cost; else 64/128/256
+};
+
+tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream);
+
+// Shard reduce.
+struct ReduceDesc {
+    int t = 0;
+    int64_t count = 0;
+    int in_bf16 = 1;
+    const void* p[TP_MAX_SHARDS] = {};
+    void* out = nullptr;
+    int out_bf16 = 1;
+    int ring = 0;
+    int hop_bf16 = 0;
+    int replicate = 0;
+};
+tp_status launch_shard_reduce(const ReduceDesc& d, cudaStream_t stream);
+
+// Vocab-parallel embedding.
+struct EmbedDesc {
+    int t = 0;
+    int64_t vocab = 0, h = 0, n = 0, per = 0;
+    const int32_t* ids = nullptr;
+    const void* table[TP_MAX_SHARDS] = {};
+    int bf16 = 1;
+    void* out = nullptr;
+    void* partials[TP_MAX_SHARDS] = {};
+    int with_partials = 0;
+};
+tp_status launch_vocab_embed(const EmbedDesc& d, cudaStream_t stream);
+
+// Concatenation of t [rows, cols_r] shards along columns.
+struct GatherDesc {
+    int t = 0;
+    int64_t rows = 0;
+    int64_t cols[TP_MAX_SHARDS] = {};
+    int elem_bytes = 2;
+    const void* shards[TP_MAX_SHARDS] = {};
+    void* out = nullptr;
+};
+tp_status launch_shard_gather(const GatherDesc& d, cudaStream_t stream);
+
+tp_status launch_expire_wait(uint64_t limit_ns, int* status, cudaStream_t stream);
+
+}  // namespace tpk

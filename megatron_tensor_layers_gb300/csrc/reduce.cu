@@ -1,0 +1,279 @@
+// The "all-reduce sum" of t in-memory partial buffers, the all-gather of
+// vocab-sharded outputs, and the bounded-wait probe used by failure tests.
+//
+// Shard reduce (page "vLLM source analysis 13: tensor parallelism in
+// detail", §1.1.1 Reduce-Scatter, §1.1.2 All-Gather, and the one-shot
+// low-latency sum after §1.2).  On one GPU every "rank" buffer is directly
+// addressable, so both orders are a single streaming pass: each thread owns
+// 16 bytes of every buffer, loads all t of them (t x 128-bit loads in
+// flight), folds them in registers and writes the result.
+//   DIRECT: fold ranks 0, 1, ..., t-1 with a float32 carry.
+//   RING:   the buffer is cut into t chunks of ceil(K/t) elements; chunk c
+//           starts at rank c and folds c, c+1, ..., c+t-1 (mod t), exactly
+//           the order in which the ring's reduce-scatter steps add the
+//           ranks' copies into it; each addition rounds to the hop dtype
+//           (a bf16 wire rounds at every hop).  The all-gather phase moves
+//           the finished chunks unchanged, so it is the final write (to
+//           `out`, and to every rank buffer when replicating).
+// The pass is HBM-bound: t*K*b bytes read, K*b (or t*K*b) written.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tpk {
+
+struct ReduceArgs {
+    const void* p[TP_MAX_SHARDS];
+    void* out;
+    int64_t count;
+    int64_t chunk;
+    int t;
+    int ring;
+    int hop_bf16;
+    int out_bf16;
+    int replicate;
+};
+
+__device__ __forceinline__ float round_bf16(float x) { return bf16_to_f32(f32_to_bf16(x)); }
+
+template <bool IN_BF16>
+__device__ __forceinline__ float load_elem(const void* p, int64_t e) {
+    if (IN_BF16) return bf16_to_f32(static_cast<const uint16_t*>(p)[e]);
+    return static_cast<const float*>(p)[e];
+}
+
+template <bool IN_BF16>
+__device__ __forceinline__ void store_elem(void* p, int64_t e, float v, bool as_bf16) {
+    if (as_bf16)
+        static_cast<uint16_t*>(p)[e] = f32_to_bf16(v);
+    else
+        static_cast<float*>(p)[e] = v;
+}
+
+template <bool IN_BF16>
+__device__ void reduce_scalar(const ReduceArgs& a, int64_t e) {
+    const int start = a.ring ? static_cast<int>(e / a.chunk) : 0;
+    float acc = load_elem<IN_BF16>(a.p[start], e);
+    for (int j = 1; j < a.t; ++j) {
+        int r = start + j;
+        if (r >= a.t) r -= a.t;
+        const float x = load_elem<IN_BF16>(a.p[r], e);
+        acc = a.hop_bf16 ? round_bf16(acc + x) : acc + x;
+    }
+    if (a.out) store_elem<IN_BF16>(a.out, e, acc, a.out_bf16 != 0);
+    if (a.replicate)
+        for (int r = 0; r < a.t; ++r) store_elem<IN_BF16>(const_cast<void*>(a.p[r]), e, acc, IN_BF16);
+}
+
+template <bool IN_BF16>
+__device__ __forceinline__ void unpack(const uint4& q, float (&x)[IN_BF16 ? 8 : 4]) {
+    if constexpr (IN_BF16) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+        x[0] = __uint_as_float(q.x);
+        x[1] = __uint_as_float(q.y);
+        x[2] = __uint_as_float(q.z);
+        x[3] = __uint_as_float(q.w);
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void store_vec(void* base, int64_t e0, const float (&acc)[VEC], bool as_bf16) {
+    if (as_bf16) {
+        uint32_t w[VEC / 2];
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i) w[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+        if constexpr (VEC == 8) {
+            reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + e0)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + e0)[0] = make_uint2(w[0], w[1]);
+        }
+    } else {
+        float* o = static_cast<float*>(base) + e0;
+#pragma unroll
+        for (int i = 0; i < VEC; i += 4)
+            reinterpret_cast<float4*>(o + i)[0] = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+    }
+}
+
+template <bool IN_BF16>
+__global__ void __launch_bounds__(256) shard_reduce_kernel(const __grid_constant__ ReduceArgs a) {
+    constexpr int VEC = IN_BF16 ? 8 : 4;
+    const int64_t ngroups = a.count / VEC;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t gi = tid; gi < ngroups; gi += stride) {
+        const int64_t e0 = gi * VEC;
+        int start = 0;
+        if (a.ring) {
+            const int64_t c0 = e0 / a.chunk;
+            if (c0 != (e0 + VEC - 1) / a.chunk) {   // a chunk boundary falls inside this vector
+                for (int i = 0; i < VEC; ++i) reduce_scalar<IN_BF16>(a, e0 + i);
+                continue;
+            }
+            start = static_cast<int>(c0);
+        }
+        uint4 v[TP_MAX_SHARDS];
+#pragma unroll
+        for (int j = 0; j < TP_MAX_SHARDS; ++j) {
+            if (j < a.t) {
+                int r = start + j;
+                if (r >= a.t) r -= a.t;
+                v[j] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const char*>(a.p[r]) + e0 * (IN_BF16 ? 2 : 4)));
+            }
+        }
+        float acc[VEC];
+        unpack<IN_BF16>(v[0], acc);
+#pragma unroll
+        for (int j = 1; j < TP_MAX_SHARDS; ++j) {
+            if (j < a.t) {
+                float x[VEC];
+                unpack<IN_BF16>(v[j], x);
+                if (a.hop_bf16) {
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) acc[i] = round_bf16(acc[i] + x[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) acc[i] = acc[i] + x[i];
+                }
+            }
+        }
+        if (a.out) store_vec<VEC>(a.out, e0, acc, a.out_bf16 != 0);
+        if (a.replicate) {
+#pragma unroll
+            for (int r = 0; r < TP_MAX_SHARDS; ++r)
+                if (r < a.t) store_vec<VEC>(const_cast<void*>(a.p[r]), e0, acc, IN_BF16);
+        }
+    }
+    // ragged tail (count % VEC elements)
+    const int64_t tail0 = ngroups * VEC;
+    if (tid < a.count - tail0) reduce_scalar<IN_BF16>(a, tail0 + tid);
+}
+
+static int sm_count_cached() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static int cache[64] = {0};
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+tp_status launch_shard_reduce(const ReduceDesc& d, cudaStream_t stream) {
+    if (d.count == 0) return TP_OK;
+    ReduceArgs a;
+    for (int r = 0; r < TP_MAX_SHARDS; ++r) a.p[r] = r < d.t ? d.p[r] : nullptr;
+    a.out = d.out;
+    a.count = d.count;
+    a.t = d.t;
+    a.chunk = (d.count + d.t - 1) / d.t;
+    a.ring = d.ring;
+    a.hop_bf16 = d.hop_bf16;
+    a.out_bf16 = d.out_bf16;
+    a.replicate = d.replicate;
+    const int vec = d.in_bf16 ? 8 : 4;
+    const int64_t groups = std::max<int64_t>(d.count / vec, d.count % vec);
+    const int sms = std::max(1, sm_count_cached());
+    const int64_t want = (groups + 255) / 256;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
+    if (d.in_bf16)
+        shard_reduce_kernel<true><<<grid, 256, 0, stream>>>(a);
+    else
+        shard_reduce_kernel<false><<<grid, 256, 0, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ gather
+
+struct GatherArgs {
+    const void* s[TP_MAX_SHARDS];
+    int64_t cols[TP_MAX_SHARDS];
+    int64_t off[TP_MAX_SHARDS];
+    void* out;
+    int64_t rows;
+    int64_t total_cols;
+    int t;
+    int elem;
+};
+
+// One thread block per (row, shard) segment: copy the shard's row into its
+// column slice of the output row, 16 bytes at a time when both ends allow.
+__global__ void __launch_bounds__(256) shard_gather_kernel(const __grid_constant__ GatherArgs a) {
+    const int64_t nseg = a.rows * a.t;
+    for (int64_t seg = blockIdx.x; seg < nseg; seg += gridDim.x) {
+        const int r = static_cast<int>(seg % a.t);
+        const int64_t row = seg / a.t;
+        const int64_t bytes = a.cols[r] * a.elem;
+        if (bytes == 0) continue;
+        const char* src = static_cast<const char*>(a.s[r]) + row * bytes;
+        char* dst = static_cast<char*>(a.out) + (row * a.total_cols + a.off[r]) * a.elem;
+        if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) | bytes) & 15) == 0) {
+            const int64_t nv = bytes / 16;
+            for (int64_t i = threadIdx.x; i < nv; i += blockDim.x)
+                reinterpret_cast<uint4*>(dst)[i] = __ldcs(reinterpret_cast<const uint4*>(src) + i);
+        } else if (a.elem == 4) {
+            for (int64_t i = threadIdx.x; i < a.cols[r]; i += blockDim.x)
+                reinterpret_cast<uint32_t*>(dst)[i] = reinterpret_cast<const uint32_t*>(src)[i];
+        } else {
+            for (int64_t i = threadIdx.x; i < a.cols[r]; i += blockDim.x)
+                reinterpret_cast<uint16_t*>(dst)[i] = reinterpret_cast<const uint16_t*>(src)[i];
+        }
+    }
+}
+
+tp_status launch_shard_gather(const GatherDesc& d, cudaStream_t stream) {
+    GatherArgs a;
+    int64_t off = 0;
+    for (int r = 0; r < TP_MAX_SHARDS; ++r) {
+        a.s[r] = r < d.t ? d.shards[r] : nullptr;
+        a.cols[r] = r < d.t ? d.cols[r] : 0;
+        a.off[r] = off;
+        off += a.cols[r];
+    }
+    a.out = d.out;
+    a.rows = d.rows;
+    a.total_cols = off;
+    a.t = d.t;
+    a.elem = d.elem_bytes;
+    if (d.rows == 0 || off == 0) return TP_OK;
+    const int sms = std::max(1, sm_count_cached());
+    const int64_t nseg = d.rows * d.t;
+    const int grid = static_cast<int>(std::min<int64_t>(nseg, static_cast<int64_t>(sms) * 16));
+    shard_gather_kernel<<<grid, 256, 0, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ probe
+
+// Waits on a barrier that nothing signals; the bounded wait must expire,
+// record TP_ERR_TIMEOUT and return.
+__global__ void expire_wait_kernel(uint64_t limit_ns, int* status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+    __syncthreads();
+}
+
+tp_status launch_expire_wait(uint64_t limit_ns, int* status, cudaStream_t stream) {
+    expire_wait_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+}  // namespace tpk

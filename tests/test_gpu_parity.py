@@ -1,0 +1,452 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Integer-valued inputs make GEMM results exact in fp32, so those cases are
+compared bit for bit; float cases use the gates of tests/gpu_helpers.py.
+Shapes span several tiles with ragged tails in M, N and K, and the edge
+cases of each layer (t = 1, empty ranges, out-of-range ids, specials).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from megatron_tensor_layers_gb300 import _lib as tp
+from megatron_tensor_layers_gb300 import synth
+from megatron_tensor_layers_gb300.build import build
+
+from gpu_helpers import exact, f64, gemm_gate, half_ulp_bf16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+    tp.load()
+    torch.cuda.init()
+    yield
+    assert tp.tp_device_status() == 0
+
+
+def ints(shape, seed, lo=-3, hi=3, dtype=torch.bfloat16):
+    return synth.int_valued(shape, lo, hi, seed, dtype=dtype, device=DEV)
+
+
+def normal(shape, std, seed):
+    return synth.normal_bf16(shape, std, seed, device=DEV)
+
+
+# ------------------------------------------------------------ column parallel
+
+@pytest.mark.parametrize("t,n,k,os_", [(1, 200, 320, 136), (2, 130, 192, 264), (4, 5, 64, 72), (3, 257, 128, 40)])
+@pytest.mark.parametrize("gather", [False, True])
+def test_linear_col_integer_exact(t, n, k, os_, gather):
+    x = ints((n, k), 1)
+    w = [ints((os_, k), 10 + r) for r in range(t)]
+    b = [ints((os_,), 20 + r, -8, 8) for r in range(t)]
+    y = tp.tp_linear_col(x, w, bias=b, gather_output=gather, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    xf = f64(x)
+    refs = [O.linear(xf, f64(w[r]), f64(b[r])) for r in range(t)]
+    if gather:
+        exact(f64(y), O.shard_gather(refs))
+    else:
+        for r in range(t):
+            exact(f64(y[r]), refs[r])
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
+@pytest.mark.parametrize("n", [8, 200])
+def test_linear_col_gated_tiny_config(act, n):
+    # tiny TP-MLP config: t=2, h=1024, f=3072 -> per-shard gate_up [3072, 1024]
+    t, h, f = 2, 1024, 3072
+    fs = f // t
+    x = normal((n, h), 1.0, 0)
+    wg, wu = normal((f, h), 0.02, 1), normal((f, h), 0.02, 2)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    for ydt in (torch.float32, torch.bfloat16):
+        ys = tp.tp_linear_col(x, wgu, act=act, y_dtype=ydt)
+        torch.cuda.synchronize()
+        xf, wgf, wuf = f64(x), f64(wg), f64(wu)
+        for r in range(t):
+            blk = O.merged_column_shard([wgf, wuf], t, r)
+            ref = O.glu(O.linear(xf, blk[:fs]), O.linear(xf, blk[fs:]), act)
+            gemm_gate(f64(ys[r]), ref, bf16_out=ydt == torch.bfloat16)
+
+
+def test_linear_col_gated_ragged_tiles():
+    # f/t not a multiple of the 128-wide output tile, n and h ragged
+    t, n, h, fs = 3, 131, 200, 88
+    x = normal((n, h), 1.0, 5)
+    wgu = [normal((2 * fs, h), 0.05, 6 + r) for r in range(t)]
+    ys = tp.tp_linear_col(x, wgu, act="silu", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for r in range(t):
+        w = f64(wgu[r])
+        ref = O.glu(O.linear(f64(x), w[:fs]), O.linear(f64(x), w[fs:]), "silu")
+        gemm_gate(f64(ys[r]), ref, bf16_out=False)
+
+
+# --------------------------------------------------------------- row parallel
+
+@pytest.mark.parametrize("mode", ["fused", "direct", "ring"])
+@pytest.mark.parametrize("t,n,ks,out", [(2, 200, 192, 264), (4, 7, 64, 72), (1, 129, 128, 256), (3, 64, 96, 40)])
+def test_linear_row_integer_exact(mode, t, n, ks, out):
+    x = [ints((n, ks), 30 + r) for r in range(t)]
+    w = [ints((out, ks), 40 + r) for r in range(t)]
+    bias = ints((out,), 50, -8, 8)
+    y = tp.tp_linear_row(x, w, bias=bias, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    parts = [O.linear(f64(x[r]), f64(w[r]), f64(bias) if r == 0 else None) for r in range(t)]
+    exact(f64(y), O.reduce_direct(parts))
+
+
+def test_linear_row_partials_bias_on_rank0_only():
+    t, n, ks, out = 4, 16, 64, 48
+    x = [ints((n, ks), 60 + r) for r in range(t)]
+    w = [ints((out, ks), 70 + r) for r in range(t)]
+    bias = ints((out,), 80, 1, 9)
+    parts = tp.tp_linear_row(x, w, bias=bias, reduce_results=False, partial_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for r in range(t):
+        exact(f64(parts[r]), O.linear(f64(x[r]), f64(w[r]), f64(bias) if r == 0 else None))
+
+
+def test_row_worked_example_from_page():
+    # Nano-vLLM walkthrough 22, section 4: W=[[1,2,3,4],[5,6,7,8]], b=[10,20], x=[[1,1,1,1]], t=2.
+    # Padded to the 8-element row pitch the ABI needs: the extra columns are zero.
+    W = torch.zeros((2, 16), dtype=torch.bfloat16, device=DEV)
+    W[:, 0:2] = torch.tensor([[1, 2], [5, 6]], dtype=torch.bfloat16)
+    W[:, 8:10] = torch.tensor([[3, 4], [7, 8]], dtype=torch.bfloat16)
+    x = torch.zeros((1, 16), dtype=torch.bfloat16, device=DEV)
+    x[0, 0:2] = 1
+    x[0, 8:10] = 1
+    b = torch.tensor([10, 20], dtype=torch.bfloat16, device=DEV)
+    parts = tp.tp_linear_row([x[:, :8], x[:, 8:]], [W[:, :8], W[:, 8:]], bias=b, reduce_results=False,
+                             partial_dtype=torch.float32, partials=[torch.empty((1, 4), device=DEV) for _ in range(2)])
+    torch.cuda.synchronize()
+    assert parts[0][:, :2].tolist() == [[13.0, 31.0]] and parts[1][:, :2].tolist() == [[7.0, 15.0]]
+
+
+# --------------------------------------------------------------- shard reduce
+
+def _partials(t, count, dtype, seed):
+    if dtype == torch.bfloat16:
+        return [synth.normal_bf16((count,), 1.0, seed + r, device=DEV) for r in range(t)]
+    return [synth.normal_f32((count,), 1.0, seed + r, device=DEV) for r in range(t)]
+
+
+@pytest.mark.parametrize("t", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("count", [1, 7, 8 * 1024 + 5, 3 * 65536])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_shard_reduce_bit_exact_vs_emulation(t, count, dtype):
+    parts = _partials(t, count, dtype, 100)
+    pf = [f64(p) for p in parts]
+    # direct, float32 carry, output in the partial dtype and in fp32
+    y = tp.tp_shard_reduce(parts, mode="direct")
+    y32 = tp.tp_shard_reduce(parts, mode="direct", out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref32 = O.reduce_direct_f32(pf)
+    exact(f64(y32), ref32)
+    exact(f64(y), O.round_to_bf16(ref32) if dtype == torch.bfloat16 else ref32)
+    # ring, float32 carry
+    yr = tp.tp_shard_reduce(parts, mode="ring", out_dtype=torch.float32, hop_dtype=torch.float32)
+    torch.cuda.synchronize()
+    bufs, _ = O.ring_allreduce(pf, hop="f32")
+    exact(f64(yr), bufs[0])
+    if dtype == torch.bfloat16:
+        # ring with a bf16 wire: every hop rounds
+        yb = tp.tp_shard_reduce(parts, mode="ring", hop_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        bufs, _ = O.ring_allreduce(pf, hop="bf16")
+        exact(f64(yb), bufs[0])
+
+
+@pytest.mark.parametrize("mode", ["direct", "ring"])
+def test_shard_reduce_replicate_is_allreduce(mode):
+    t, count = 4, 10000 + 3
+    parts = _partials(t, count, torch.bfloat16, 200)
+    pf = [f64(p) for p in parts]
+    tp.tp_shard_reduce(parts, mode=mode, replicate=True, hop_dtype=torch.float32)
+    torch.cuda.synchronize()
+    if mode == "direct":
+        ref = O.round_to_bf16(O.reduce_direct_f32(pf))
+    else:
+        ref = O.round_to_bf16(O.ring_allreduce(pf, hop="f32")[0][0])
+    for p in parts:
+        exact(f64(p), ref)
+
+
+def test_shard_reduce_fp32_within_1e6_of_fp64():
+    for t in (2, 4, 8):
+        parts = _partials(t, 1 << 20, torch.float32, 300 + t)
+        y = tp.tp_shard_reduce(parts, mode="direct")
+        torch.cuda.synchronize()
+        ref = O.reduce_direct([f64(p) for p in parts])
+        assert np.max(np.abs(f64(y) - ref)) <= 1e-6 * np.max(np.abs(ref))
+
+
+def test_shard_reduce_ring_order_observable():
+    # bf16 wire: element c of chunk c holds 1.0 at the rank that adds it last;
+    # the two small values meet first and survive (see the oracle pin).
+    a, e = 1.0, 2.0 ** -8
+    n = 3
+    vals = [[e, a, e], [e, e, a], [a, e, e]]
+    parts = [torch.tensor(v, dtype=torch.bfloat16, device=DEV) for v in vals]
+    out = tp.tp_shard_reduce(parts, mode="ring", hop_dtype=torch.bfloat16)
+    direct = tp.tp_shard_reduce(parts, mode="direct")
+    torch.cuda.synchronize()
+    assert out.float().tolist() == [1.0 + 2 ** -7] * n
+    assert direct.float().tolist() == [1.0 + 2 ** -7] * n   # fp32 carry keeps every bit here
+
+
+# -------------------------------------------------------------------- MLP
+
+def _mlp_rounding_allowance(xf, wg, wu, wd, t, act, partial_bf16):
+    """Per-element bound of the bf16 roundings inside the sharded MLP
+    (intermediate H, partials), from the oracle's own values."""
+    fs = wg.shape[0] // t
+    extra = 0.0
+    parts = []
+    for r in range(t):
+        blk = O.merged_column_shard([wg, wu], t, r)
+        h = O.glu(O.linear(xf, blk[:fs]), O.linear(xf, blk[fs:]), act)
+        bd = O.row_shard(wd, t, r)
+        extra = extra + half_ulp_bf16(h) @ np.abs(bd).T
+        parts.append(O.linear(h, bd))
+    if partial_bf16:
+        for p in parts:
+            extra = extra + half_ulp_bf16(p)
+    return extra
+
+
+@pytest.mark.parametrize("mode", ["direct", "ring", "fused"])
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
+def test_mlp_forward_tiny_config(mode, act):
+    # t=2, h=1024, f=3072, n=8 tokens, W ~ N(0, 0.02), X ~ N(0, 1), seed 0
+    t, n, h, f = 2, 8, 1024, 3072
+    fs = f // t
+    x = normal((n, h), 1.0, 0)
+    wg, wu, wd = normal((f, h), 0.02, 1), normal((f, h), 0.02, 2), normal((h, f), 0.02, 3)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds = [wd[:, r * fs:(r + 1) * fs] for r in range(t)]          # column views, ld = f
+    xf, wgf, wuf, wdf = f64(x), f64(wg), f64(wu), f64(wd)
+    ref = O.mlp_unsharded(xf, wgf, wuf, wdf, None, act)
+    for pdt in (torch.float32, torch.bfloat16):
+        for ydt in (torch.float32, torch.bfloat16):
+            y = tp.tp_mlp_forward(x, wgu, wds, act=act, mode=mode, partial_dtype=pdt, y_dtype=ydt)
+            torch.cuda.synchronize()
+            extra = _mlp_rounding_allowance(xf, wgf, wuf, wdf, t, act, pdt == torch.bfloat16 and mode != "fused")
+            gemm_gate(f64(y), ref, bf16_out=ydt == torch.bfloat16, extra=extra)
+
+
+def test_mlp_forward_integer_variant_and_bias():
+    # integer-valued (-3..3) variant of the tiny config; bias added once
+    t, n, h, f = 2, 8, 1024, 3072
+    fs = f // t
+    x = ints((n, h), 0)
+    wg, wu, wd = ints((f, h), 1), ints((f, h), 2), ints((h, f), 3)
+    bias = ints((h,), 4, -8, 8)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds = [wd[:, r * fs:(r + 1) * fs].contiguous() for r in range(t)]
+    xf, wgf, wuf, wdf, bf = f64(x), f64(wg), f64(wu), f64(wd), f64(bias)
+    ref = O.mlp_unsharded(xf, wgf, wuf, wdf, bf, "silu")
+    for mode in ("direct", "fused"):
+        y = tp.tp_mlp_forward(x, wgu, wds, bias_down=bias, mode=mode, partial_dtype=torch.float32,
+                              y_dtype=torch.float32)
+        torch.cuda.synchronize()
+        extra = _mlp_rounding_allowance(xf, wgf, wuf, wdf, t, "silu", False)
+        gemm_gate(f64(y), ref, bf16_out=False, extra=extra)
+    # the gate's bf16-rounding emulation of H makes the comparison tight
+    hs = []
+    for r in range(t):
+        blk = O.merged_column_shard([wgf, wuf], t, r)
+        hs.append(O.round_to_bf16(O.glu(O.linear(xf, blk[:fs]), O.linear(xf, blk[fs:]), "silu")))
+    emul = O.reduce_direct([O.linear(hs[r], O.row_shard(wdf, t, r), bf if r == 0 else None) for r in range(t)])
+    y = tp.tp_mlp_forward(x, wgu, wds, bias_down=bias, mode="fused", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    # H can round to a neighbouring bf16 value where fp32 and fp64 straddle a midpoint
+    assert np.max(np.abs(f64(y) - emul)) <= 2e-3 * np.sqrt(np.mean(emul ** 2))
+
+
+def test_mlp_decode_shapes_small():
+    # decode-like: a handful of tokens against wide shards
+    t, h, f = 4, 512, 2048
+    fs = f // t
+    wg, wu, wd = normal((f, h), 0.02, 11), normal((f, h), 0.02, 12), normal((h, f), 0.02, 13)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds = [wd[:, r * fs:(r + 1) * fs] for r in range(t)]
+    for n in (1, 16, 64):
+        x = normal((n, h), 1.0, 20 + n)
+        ref = O.mlp_unsharded(f64(x), f64(wg), f64(wu), f64(wd), None, "silu")
+        extra = _mlp_rounding_allowance(f64(x), f64(wg), f64(wu), f64(wd), t, "silu", False)
+        for mode in ("direct", "fused"):
+            y = tp.tp_mlp_forward(x, wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
+            torch.cuda.synchronize()
+            gemm_gate(f64(y), ref, bf16_out=False, extra=extra)
+
+
+# ---------------------------------------------------------------- embedding
+
+def _table_shards(table, t):
+    v = table.shape[0]
+    out = []
+    for r in range(t):
+        s, e = O.vocab_range(v, t, r)
+        out.append(table[s:e].contiguous() if e > s else None)
+    return out
+
+
+@pytest.mark.parametrize("t", [2, 4])
+def test_vocab_embed_bit_exact_config(t):
+    V, h, n = 151936, 1024, 4096
+    table = normal((V, h), 0.02, 6)
+    ids = synth.uniform_ids(n, V, 5, device=DEV)
+    shards = _table_shards(table, t)
+    partials = [torch.empty((n, h), dtype=torch.bfloat16, device=DEV) for _ in range(t)]
+    out = tp.vocab_parallel_embed(ids, shards, V, partials=partials)
+    torch.cuda.synchronize()
+    ref, refp = O.vocab_parallel_embedding(ids.cpu().numpy(), f64(table), t)
+    exact(f64(out), ref)
+    for r in range(t):
+        exact(f64(partials[r]), refp[r])
+
+
+@pytest.mark.parametrize("t,V", [(1, 50), (3, 50), (4, 3), (8, 101)])
+def test_vocab_embed_edges(t, V):
+    h = 16
+    table = normal((V, h), 1.0, 7)
+    tb = table.clone()
+    tb[0, 0] = float("nan")
+    tb[0, 1] = float("inf")
+    tb[0, 2] = -0.0
+    ids = torch.tensor([-1, V, 10 ** 6, 0, V - 1, -(2 ** 31), 2 ** 31 - 1] + list(range(min(V, 20))),
+                       dtype=torch.int32, device=DEV)
+    out = tp.vocab_parallel_embed(ids, _table_shards(tb, t), V)
+    torch.cuda.synchronize()
+    ref, _ = O.vocab_parallel_embedding(ids.cpu().numpy(), f64(tb), t)
+    exact(f64(out), ref)
+
+
+def test_vocab_embed_worked_example_structure():
+    # vLLM source analysis 13, section 2.4.1: V=10, ids [[1,6],[3,8]], two ranges of 5 rows
+    V, h, t = 10, 8, 2
+    table = normal((V, h), 1.0, 42)
+    ids = torch.tensor([1, 6, 3, 8], dtype=torch.int32, device=DEV)
+    parts = [torch.empty((4, h), dtype=torch.bfloat16, device=DEV) for _ in range(t)]
+    out = tp.vocab_parallel_embed(ids, _table_shards(table, t), V, partials=parts)
+    torch.cuda.synchronize()
+    owners = [0, 1, 0, 1]
+    for i, o in enumerate(owners):
+        assert torch.count_nonzero(parts[1 - o][i]) == 0
+        assert torch.equal(parts[o][i], table[ids[i].item()])
+    assert torch.equal(out, table[ids.long()])
+
+
+# ------------------------------------------------------------------ LM head
+
+@pytest.mark.parametrize("t,V,n,h", [(2, 1000, 130, 64), (3, 1000, 64, 128), (4, 151936, 96, 1024), (8, 77, 5, 32)])
+def test_lm_head_concat_and_per_shard(t, V, n, h):
+    x = normal((n, h), 1.0, 8)
+    table = normal((V, h), 0.02, 6)
+    shards = _table_shards(table, t)
+    logits = tp.lm_head_sharded(x, shards, V, out_dtype=torch.float32)
+    per = tp.lm_head_sharded(x, shards, V, per_shard=True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref, refp = O.lm_head_sharded(f64(x), f64(table), t)
+    gemm_gate(f64(logits), ref, bf16_out=False)
+    for r in range(t):
+        if refp[r].shape[1]:
+            gemm_gate(f64(per[r]), refp[r], bf16_out=False)
+    # the explicit all-gather of the per-shard logits gives the same bits
+    nonempty = [p for p in per if p.shape[1] > 0]
+    cat = tp.tp_shard_gather(nonempty)
+    torch.cuda.synchronize()
+    exact(f64(cat), f64(logits))
+
+
+def test_lm_head_integer_exact_bf16():
+    t, V, n, h = 4, 1024, 136, 256
+    x = ints((n, h), 9)
+    table = ints((V, h), 10)
+    logits = tp.lm_head_sharded(x, _table_shards(table, t), V, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    exact(f64(logits), O.lm_head_unsharded(f64(x), f64(table)))
+
+
+# -------------------------------------------------------------- gather / misc
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_shard_gather_bit_exact(dtype):
+    cols = [8, 3, 0, 16, 5]
+    shards = [synth.normal_f32((37, c), 1.0, 400 + i, device=DEV).to(dtype) for i, c in enumerate(cols)]
+    out = tp.tp_shard_gather(shards)
+    torch.cuda.synchronize()
+    exact(f64(out), O.shard_gather([f64(s) for s in shards]))
+
+
+def test_collective_counter_counts_reduces():
+    t, n, h, f = 2, 8, 256, 512
+    x = normal((n, h), 1.0, 1)
+    wgu = [normal((f, h), 0.02, 2 + r) for r in range(t)]
+    wds = [normal((h, f // t), 0.02, 5 + r) for r in range(t)]
+    tp.tp_reset_collective_count()
+    tp.tp_mlp_forward(x, wgu, wds, mode="direct")
+    tp.tp_mlp_forward(x, wgu, wds, mode="fused")
+    torch.cuda.synchronize()
+    assert tp.tp_collective_count() == 2     # one all-reduce per MLP, as the pages count them
+
+
+def test_bounded_wait_expires_and_reports():
+    tp.tp_debug_expire_wait(2_000_000)       # 2 ms on a barrier nothing signals
+    assert tp.tp_device_status() == 6        # TP_ERR_TIMEOUT, and the context still works
+    assert tp.tp_device_status() == 0        # cleared
+    a = torch.ones(16, device=DEV, dtype=torch.bfloat16)
+    out = tp.tp_shard_reduce([a, a])
+    torch.cuda.synchronize()
+    assert out.float().sum().item() == 32.0
+
+
+# ------------------------------------------------- every tile width, exactly
+
+@pytest.fixture
+def tile_n(request):
+    tp.tp_set_gemm_tile_n(request.param)
+    yield request.param
+    tp.tp_set_gemm_tile_n(0)
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256], indirect=True)
+def test_every_tile_width_integer_exact(tile_n):
+    # plain column GEMM: ragged M (300), N (200 per shard), K (8 blocks + 24)
+    t, n, k, os_ = 2, 300, 536, 200
+    x = ints((n, k), 90)
+    w = [ints((os_, k), 91 + r) for r in range(t)]
+    y = tp.tp_linear_col(x, w, y_dtype=torch.float32)
+    # row GEMM, fused over 3 K-segments and unfused
+    xs = [ints((n, 136), 95 + r) for r in range(3)]
+    ws = [ints((264, 136), 98 + r) for r in range(3)]
+    yf = tp.tp_linear_row(xs, ws, mode="fused", y_dtype=torch.float32)
+    yd = tp.tp_linear_row(xs, ws, mode="direct", partial_dtype=torch.float32, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for r in range(t):
+        exact(f64(y[r]), O.linear(f64(x), f64(w[r])))
+    ref = O.reduce_direct([O.linear(f64(xs[r]), f64(ws[r])) for r in range(3)])
+    exact(f64(yf), ref)
+    exact(f64(yd), ref)
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256], indirect=True)
+def test_every_tile_width_gated(tile_n):
+    t, n, h, fs = 2, 260, 320, 200
+    x = normal((n, h), 1.0, 120)
+    wgu = [normal((2 * fs, h), 0.05, 121 + r) for r in range(t)]
+    ys = tp.tp_linear_col(x, wgu, act="silu", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for r in range(t):
+        w = f64(wgu[r])
+        ref = O.glu(O.linear(f64(x), w[:fs]), O.linear(f64(x), w[fs:]), "silu")
+        gemm_gate(f64(ys[r]), ref, bf16_out=False)
