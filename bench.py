@@ -1,0 +1,479 @@
+"""Benchmark of the tensor-parallel hot path on GB300.
+
+One step = one forward of the Llama-3.1-70B-shaped tensor-parallel MLP
+prefill with t = 4 simulated ranks (n = 8192 tokens, h = 8192, f = 28672,
+SiLU-gated): per rank the merged gate_up column GEMM with the activation in
+its epilogue, per rank the down-projection row GEMM into a bf16 partial, then
+the all-reduce of the 4 partials (direct order).  `value` is the MLP's
+6*n*h*f FLOP divided by the device time of the step (inputs resident in HBM,
+all larger than L2).  The shard reduce inside the same step gives the
+second half of the metric (GB/s).  After the timed steps the other rows of
+the hot path (fused reduce, t=8, decode, embedding, LM head, the reduce
+sweep) are timed once each and reported under "detail".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the pages publish no implementation to run).  Under torchrun
+(N > 1) every rank runs an independent replica (weak scaling); rank 0
+prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TP-MLP TFLOP/s (% bf16 tensor peak); shard-reduce GB/s (% HBM peak)"
+T, N_TOK, H, F = 4, 8192, 8192, 28672
+FLOPS = 6.0 * N_TOK * H * F                 # gate + up + down GEMMs
+WORKLOAD = ("Llama-3.1-70B-shaped TP-MLP prefill: t=4 simulated ranks, n=8192 tokens, h=8192, f=28672 "
+            "(per-rank gate_up [14336,8192], down [8192,7168]), SiLU-gated, bf16 partials reduced in rank order")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) of one launch of the gate_up GEMM at the bench
+# size, from ncu (dram__bytes_read.sum + dram__bytes_write.sum); None until
+# taken for the current kernel.
+TRAFFIC_GLU_FULL = None
+TRAFFIC_NOTE = "not yet captured for this kernel version"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.path.join("/tmp", f"tp_bench_clocks_{os.getpid()}.csv"), "w+")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.flush()
+        self.out.seek(0)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s, p in zip(sm, power) if p > 300.0] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ------------------------------------------------------------------ ours
+
+def make_mlp(torch, synth, t, n, h, f, dev, seed=0):
+    fs = f // t
+    x = synth.normal_bf16((n, h), 1.0, seed, device=dev)
+    wg = synth.normal_bf16((f, h), 0.02, seed + 1, device=dev)
+    wu = synth.normal_bf16((f, h), 0.02, seed + 2, device=dev)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    del wg, wu
+    wd = synth.normal_bf16((h, f), 0.02, seed + 3, device=dev)
+    wds = [wd[:, r * fs:(r + 1) * fs].contiguous() for r in range(t)]
+    del wd
+    return x, wgu, wds
+
+
+def time_fn(torch, fn, iters, warm=2, stream=None):
+    """Mean device time (s) of fn() over iters launches, CUDA events on the stream."""
+    stream = stream or torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / iters
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from megatron_tensor_layers_gb300 import _lib as tp
+    from megatron_tensor_layers_gb300 import synth
+    from megatron_tensor_layers_gb300.build import build
+
+    build()
+    tp.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    stream = torch.cuda.current_stream()
+    x, wgu, wds = make_mlp(torch, synth, T, N_TOK, H, F, dev, seed=0)
+    fs = F // T
+    hbuf = torch.empty((N_TOK, F), dtype=torch.bfloat16, device=dev)
+    h_slices = [hbuf[:, r * fs:(r + 1) * fs] for r in range(T)]
+    parts = [torch.empty((N_TOK, H), dtype=torch.bfloat16, device=dev) for _ in range(T)]
+    y = torch.empty((N_TOK, H), dtype=torch.bfloat16, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tp.tp_linear_col(x, wgu, act="silu", y=h_slices, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        tp.tp_linear_row(h_slices, wds, reduce_results=False, partials=parts, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        tp.tp_shard_reduce(parts, out=y, mode="direct", stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if tp.tp_device_status() != 0:
+        raise RuntimeError("device status error after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank if world > 1 else (dev.index or 0)) as clocks:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    if tp.tp_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    col_t = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3 / args.steps
+    row_t = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3 / args.steps
+    red_t = sum(e[2].elapsed_time(e[3]) for e in evs) / 1e3 / args.steps
+    if dist is not None:
+        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed = tt.item()
+    ms_per_step = elapsed / args.steps * 1e3
+    value = FLOPS * world * args.steps / elapsed / 1e12
+
+    col_flops = 4.0 * N_TOK * H * F
+    red_bytes = (T + 1) * N_TOK * H * 2
+    # A timed region of a few hundred ms runs at boost clock: compare with the
+    # burst GEMM peak; only a seconds-long region is held to the sustained one.
+    long_region = elapsed >= 2.0
+    tpeak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    tkind = f"bf16 {'sustained' if long_region else 'burst'} ({peak_src})"
+    roofline = {"bound": "tensor", "kernel": "tp_gemm_kernel<256,4,GLU> (gate_up column GEMM + SiLU*up)",
+                "achieved": col_flops / col_t / 1e12, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": col_flops / col_t / 1e12 / tpeak, "peak_kind": tkind, "traffic": TRAFFIC_GLU_FULL,
+                "traffic_note": TRAFFIC_NOTE, "algorithmic_per_launch": col_flops,
+                "algorithmic_bytes_per_launch": 2.0 * (N_TOK * H + 2 * F * H + N_TOK * F),
+                "launch_ms": col_t * 1e3}
+    shard_reduce = {"value": red_bytes / red_t / 1e9, "unit": "GB/s",
+                    "frac": red_bytes / red_t / 1e9 / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"],
+                    "peak_kind": f"HBM copy ({peak_src})", "ms": red_t * 1e3, "bytes": red_bytes,
+                    "config": "t=4 bf16 partials of 8192 x 8192 (128 MiB each) -> 128 MiB, direct order"}
+    row_flops = 2.0 * N_TOK * H * F
+    detail = {"col_gate_up_ms": col_t * 1e3, "row_down_partials_ms": row_t * 1e3, "shard_reduce_ms": red_t * 1e3,
+              "row_down_tflops": row_flops / row_t / 1e12}
+
+    # ---------------- e2e: host buffers through tp_mlp_forward
+    xh = torch.empty((N_TOK, H), dtype=torch.bfloat16, pin_memory=True)
+    xh.copy_(x)
+    yh = torch.empty((N_TOK, H), dtype=torch.bfloat16, pin_memory=True)
+    xd = torch.empty_like(x)
+    ws = torch.empty(tp.tp_mlp_workspace_size(T, N_TOK, H, F, "direct", torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        tp.tp_mlp_forward(xd, wgu, wds, mode="direct", workspace=ws, y=y, stream=stream)
+        yh.copy_(y, non_blocking=True)
+
+    e2e_s = time_fn(torch, e2e_step, max(3, args.steps // 2), warm=2) if not args.no_e2e else float("nan")
+    e2e = {"value": FLOPS / e2e_s / 1e12 * world, "unit": "TFLOP/s", "h2d_bytes_per_step": N_TOK * H * 2,
+           "d2h_bytes_per_step": N_TOK * H * 2, "ms_per_step": e2e_s * 1e3,
+           "path": "pinned host X -> tp_mlp_forward (C ABI) -> pinned host Y, copies on the same stream"}
+
+    if not args.no_detail:
+        detail.update(bench_detail(torch, tp, synth, dev, peaks, wgu, wds, x))
+    del wgu, wds, hbuf, parts
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(torch, synth, dev)
+    gpu_launches = 3 * args.steps
+    res = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic: seeded N(0,1) activations, N(0,0.02) weights",
+           "config": {"workload": WORKLOAD, "t": T, "n": N_TOK, "h": H, "f": F, "reduce": "direct",
+                      "partials": "bf16", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                      "l2": "inputs larger than L2 (X 128 MiB, weights 1.41 GB, partials 512 MiB)"},
+           "tensor_frac_of_peak": value / tpeak, "tensor_peak_kind": tkind,
+           "shard_reduce": shard_reduce, "roofline": roofline, "e2e": e2e, "gpu_launches": gpu_launches,
+           "clocks": clocks.summary(), "peaks": {**peaks, "source": peak_src}, "detail": detail}
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return res
+
+
+def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
+    """Every other row of the hot path, timed once each (not part of value)."""
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    ten = peaks["bf16_tflops"]
+    # fused down-GEMM + reduce, t=4 (reuses the step's weights)
+    y = torch.empty((N_TOK, H), dtype=torch.bfloat16, device=dev)
+    ws_f = torch.empty(tp.tp_mlp_workspace_size(T, N_TOK, H, F, "fused", torch.bfloat16), dtype=torch.uint8,
+                       device=dev)
+    s = time_fn(torch, lambda: tp.tp_mlp_forward(x, wgu4, wds4, mode="fused", workspace=ws_f, y=y), 5)
+    out["prefill_t4_fused"] = {"ms": s * 1e3, "tflops": FLOPS / s / 1e12, "frac": FLOPS / s / 1e12 / ten}
+    ws_d = torch.empty(tp.tp_mlp_workspace_size(T, N_TOK, H, F, "ring", torch.bfloat16), dtype=torch.uint8,
+                       device=dev)
+    s = time_fn(torch, lambda: tp.tp_mlp_forward(x, wgu4, wds4, mode="ring", workspace=ws_d, y=y), 5)
+    out["prefill_t4_ring"] = {"ms": s * 1e3, "tflops": FLOPS / s / 1e12, "frac": FLOPS / s / 1e12 / ten}
+    # decode, t=4, n in {1, 16, 64}: weight streaming
+    wbytes = 3.0 * H * F * 2
+    for n in (1, 16, 64):
+        xs = x[:n].contiguous()
+        yd = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+        for mode in ("direct", "fused"):
+            wsn = torch.empty(max(256, tp.tp_mlp_workspace_size(T, n, H, F, mode, torch.bfloat16)),
+                              dtype=torch.uint8, device=dev)
+            s = time_fn(torch, lambda: tp.tp_mlp_forward(xs, wgu4, wds4, mode=mode, workspace=wsn, y=yd), 20)
+            out[f"decode_t4_n{n}_{mode}"] = {"us": s * 1e6, "tflops": 6.0 * n * H * F / s / 1e12,
+                                             "weight_GBps": wbytes / s / 1e9, "hbm_frac": wbytes / s / 1e9 / hbm}
+    del ws_f, ws_d
+    # t=8 prefill, separate and fused
+    x8, wgu8, wds8 = make_mlp(torch, synth, 8, N_TOK, H, F, dev, seed=50)
+    for mode in ("direct", "fused"):
+        ws8 = torch.empty(tp.tp_mlp_workspace_size(8, N_TOK, H, F, mode, torch.bfloat16), dtype=torch.uint8,
+                          device=dev)
+        s = time_fn(torch, lambda: tp.tp_mlp_forward(x8, wgu8, wds8, mode=mode, workspace=ws8, y=y), 5)
+        out[f"prefill_t8_{mode}"] = {"ms": s * 1e3, "tflops": FLOPS / s / 1e12, "frac": FLOPS / s / 1e12 / ten}
+        del ws8
+    del x8, wgu8, wds8
+    torch.cuda.empty_cache()
+    # shard-reduce sweep: t in {2,4,8}, n in {1,64,8192}, h=8192, bf16 and fp32, direct and ring
+    sweep = {}
+    for dt in (torch.bfloat16, torch.float32):
+        es = 2 if dt == torch.bfloat16 else 4
+        for t in (2, 4, 8):
+            base = [torch.randn((N_TOK * H,), device=dev).to(dt) for _ in range(t)]
+            for n in (1, 64, 8192):
+                ps = [b[: n * H] for b in base]
+                o = torch.empty((n * H,), dtype=dt, device=dev)
+                for mode in ("direct", "ring"):
+                    iters = 20 if n == 8192 else 200
+                    s = time_fn(torch, lambda: tp.tp_shard_reduce(ps, out=o, mode=mode), iters)
+                    byts = (t + 1) * n * H * es
+                    sweep[f"{'bf16' if es == 2 else 'f32'}_t{t}_n{n}_{mode}"] = {
+                        "us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm}
+            del base
+    out["shard_reduce_sweep"] = sweep
+    # vocab-parallel embedding + LM head, V=151936, h=1024, 4096 ids
+    V, hh, nt = 151936, 1024, 4096
+    table = synth.normal_bf16((V, hh), 0.02, 6, device=dev)
+    ids = synth.uniform_ids(nt, V, 5, device=dev)
+    xh = synth.normal_bf16((nt, hh), 1.0, 7, device=dev)
+    logits = torch.empty((nt, V), dtype=torch.bfloat16, device=dev)
+    for t in (2, 4):
+        per = (V + t - 1) // t
+        shards = [table[r * per:min((r + 1) * per, V)].contiguous() for r in range(t)]
+        e = torch.empty((nt, hh), dtype=torch.bfloat16, device=dev)
+        s = time_fn(torch, lambda: tp.vocab_parallel_embed(ids, shards, V, out=e), 200)
+        byts = nt * 4 + 2 * nt * hh * 2
+        out[f"embed_t{t}"] = {"us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm}
+        graph_s = graph_time(torch, lambda: tp.vocab_parallel_embed(ids, shards, V, out=e), 100)
+        if graph_s:
+            out[f"embed_t{t}"]["graph_us"] = graph_s * 1e6
+            out[f"embed_t{t}"]["graph_GBps"] = byts / graph_s / 1e9
+        s = time_fn(torch, lambda: tp.lm_head_sharded(xh, shards, V, logits=logits), 10)
+        fl = 2.0 * nt * hh * V
+        out[f"lm_head_t{t}"] = {"ms": s * 1e3, "tflops": fl / s / 1e12, "frac": fl / s / 1e12 / ten,
+                                "store_GBps": nt * V * 2 / s / 1e9}
+        per_shard = tp.lm_head_sharded(xh, shards, V, per_shard=True)
+        s = time_fn(torch, lambda: tp.tp_shard_gather(per_shard, out=logits), 10)
+        byts = 2 * nt * V * 2
+        out[f"gather_t{t}"] = {"ms": s * 1e3, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm}
+        del per_shard
+    return out
+
+
+def graph_time(torch, fn, reps):
+    """Per-launch time of fn replayed from a CUDA graph of `reps` launches."""
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(5):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / (5 * reps)
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_sample(torch, synth, dev, rows, seed=0):
+    """fp64 inputs of the bench workload for the first `rows` token rows."""
+    import oracle as O
+    fs = F // T
+    x = synth.normal_bf16((N_TOK, H), 1.0, seed, device=dev)[:rows]
+    wg = synth.normal_bf16((F, H), 0.02, seed + 1, device=dev)
+    wu = synth.normal_bf16((F, H), 0.02, seed + 2, device=dev)
+    wd = synth.normal_bf16((H, F), 0.02, seed + 3, device=dev)
+    cv = lambda a: O.bf16_bits_to_f64(synth.bits_u16(a))
+    out = (cv(x), cv(wg), cv(wu), cv(wd))
+    del wg, wu, wd
+    return out
+
+
+def cpu_baseline(torch, synth, dev, rows=16):
+    """The oracle as it stands (fp64 numpy, all host cores), on `rows` token
+    rows of the bench workload: the sharded MLP of the pages with the
+    partials summed in rank order."""
+    import oracle as O
+    xf, wg, wu, wd = oracle_sample(torch, synth, dev, rows)
+    O.mlp_sharded(xf[:1], wg, wu, wd, T)                  # touch the pages once
+    t0 = time.perf_counter()
+    O.mlp_sharded(xf, wg, wu, wd, T)
+    s = time.perf_counter() - t0
+    return {"value": 6.0 * rows * H * F / s / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{rows} of 8192 token rows of the bench workload (all weights), fp64 numpy, "
+                      f"{s:.2f} s", "seconds": s}
+
+
+def run_reference(args, rank, world):
+    """Time the oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    import torch
+    from megatron_tensor_layers_gb300 import synth
+    import oracle as O
+    dev = "cpu"
+    rows = args.ref_rows
+    xf, wg, wu, wd = oracle_sample(torch, synth, dev, rows)
+    for _ in range(args.warmup):
+        O.mlp_sharded(xf[:1], wg, wu, wd, T)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.mlp_sharded(xf, wg, wu, wd, T)
+    s = time.perf_counter() - t0
+    v = 6.0 * rows * H * F * args.steps / s / 1e12
+    sample = f"{rows} of 8192 token rows per step (all weights), fp64 numpy on {os.cpu_count()} cores"
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": s / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded N(0,1) activations, N(0,0.02) weights",
+            "config": {"workload": WORKLOAD, "t": T, "n": N_TOK, "h": H, "f": F, "reduce": "direct"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-detail", action="store_true", help="skip the per-row detail timings")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=8)
+    ap.add_argument("--tokens", type=int, default=8192,
+                    help="token count of the step (8192 is the bench workload; smaller only for profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    global N_TOK, FLOPS
+    N_TOK = args.tokens
+    FLOPS = 6.0 * N_TOK * H * F
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()
