@@ -201,6 +201,49 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f,
                          void* y, tp_dtype y_dtype, tp_stream stream);
 
 /*
+ * tp_mlp_forward for callers that cannot allocate device memory.  This entry
+ * point has no counterpart in the pages this library follows; it exists for
+ * deployment reasons.
+ *
+ * Who needs it: a host application that loads this library as a plugin and
+ * owns the whole device memory pool (and so forbids its plugins to call
+ * cudaMalloc), or a latency-critical decode loop that must not call
+ * cudaMalloc/cudaFree because they can synchronise the device and stall every
+ * stream.  Such a caller cannot provide tp_mlp_forward's workspace.
+ *
+ * What it does: exactly tp_mlp_forward (same arguments minus the workspace,
+ * same kernels, same results), with the workspace taken from a scratch array
+ * of TP_STATIC_SCRATCH_BYTES that is part of the library's device image.
+ * It allocates nothing and calls no allocating routine.  The caller still
+ * passes and owns x, the weights, the bias and y.
+ *
+ * Limit: tp_mlp_workspace_size(t, n, h, f, mode, partial_dtype) must not
+ * exceed TP_STATIC_SCRATCH_BYTES (16 MiB), else TP_ERR_WORKSPACE and nothing
+ * is launched.  Example: 64 tokens of an h=8192, f=28672 MLP at t=4 need
+ * 12.1 MB with fp32 partials; a fused reduce needs only the n*f*2 bytes of H.
+ *
+ * Costs and rules:
+ *  - Every GPU on which the library is loaded holds the 16 MiB from module
+ *    load until the process exits.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture begins on that device.
+ *  - All calls in the process share the one array per device and it keeps
+ *    the previous call's contents.  Nothing in it needs to start at zero:
+ *    each call writes every byte it later reads.  Calls that can overlap on
+ *    the GPU (unordered streams, concurrent host threads) race on the array:
+ *    order them on one stream.
+ */
+#define TP_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+tp_status tp_mlp_forward_static(int t, int64_t n, int64_t h, int64_t f,
+                                const void* x, int64_t ldx,
+                                const void* const* w_gate_up,
+                                const void* const* w_down, int64_t ld_down,
+                                const void* bias_down, tp_act act,
+                                tp_reduce_mode mode, tp_dtype partial_dtype,
+                                void* y, tp_dtype y_dtype, tp_stream stream);
+
+/*
  * VocabParallelEmbedding (page "Tensor parallelism from scratch", tp.py
  * VocabParallelEmbedding; page "vLLM source analysis 13", §2.4.1): rank r
  * owns token ids [r*per, min((r+1)*per, vocab)) with per = ceil(vocab/t).

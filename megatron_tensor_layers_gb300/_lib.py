@@ -32,8 +32,9 @@ EXPORTED = [
     "tp_status_string", "tp_abi_version", "tp_linear_col", "tp_linear_row", "tp_shard_reduce",
     "tp_mlp_workspace_size", "tp_mlp_forward", "vocab_parallel_embed", "lm_head_sharded",
     "tp_shard_gather", "tp_device_status", "tp_collective_count", "tp_reset_collective_count",
-    "tp_debug_expire_wait", "tp_set_gemm_tile_n",
+    "tp_debug_expire_wait", "tp_set_gemm_tile_n", "tp_mlp_forward_static",
 ]
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class TPError(RuntimeError):
@@ -72,6 +73,7 @@ def load() -> ctypes.CDLL:
         "tp_reset_collective_count": (None, []),
         "tp_debug_expire_wait": (I32, [ctypes.c_uint64, P]),
         "tp_set_gemm_tile_n": (I32, [I32]),
+        "tp_mlp_forward_static": (I32, [I32, I64, I64, I64, P, I64, P, P, I64, P, I32, I32, I32, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -280,3 +282,24 @@ def tp_debug_expire_wait(limit_ns: int, stream=None) -> None:
 def tp_set_gemm_tile_n(n: int) -> None:
     """Force the GEMM tile width (64/128/256) for later launches; 0 = automatic."""
     _check("tp_set_gemm_tile_n", load().tp_set_gemm_tile_n(n))
+
+
+def tp_mlp_forward_static(x: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_down: Sequence[torch.Tensor], *,
+                          bias_down: Optional[torch.Tensor] = None, act: str = "silu", mode: str = "direct",
+                          partial_dtype=torch.bfloat16, y: Optional[torch.Tensor] = None,
+                          y_dtype=torch.bfloat16, stream=None):
+    """tp_mlp_forward without a workspace argument, for callers that must not
+    allocate device memory: the scratch is the library's own fixed 16 MiB
+    device array (see include/tp.h).  Pass `y` to keep this call free of
+    allocations as well; requests larger than the array raise TPError
+    (TP_ERR_WORKSPACE)."""
+    t = len(w_gate_up)
+    n, h = x.shape
+    f = w_gate_up[0].shape[0] // 2 * t
+    if y is None:
+        y = torch.empty((n, h), dtype=y_dtype, device=x.device)
+    code = load().tp_mlp_forward_static(t, n, h, f, _ptr(x), _ld(x), _ptrs(w_gate_up), _ptrs(w_down),
+                                        _ld(w_down[0]), _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype),
+                                        _ptr(y), _dt(y.dtype), _stream(stream))
+    _check("tp_mlp_forward_static", code)
+    return y

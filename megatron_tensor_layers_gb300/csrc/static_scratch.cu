@@ -1,0 +1,71 @@
+// tp_mlp_forward_static: the tensor-parallel MLP forward for callers that
+// cannot hand the library a device workspace.
+//
+// tp_mlp_forward needs a scratch buffer (the intermediate H and, unless the
+// reduce is fused, the t partial sums) that the caller allocates.  Some
+// callers cannot do that: a host application that loads this library as a
+// plugin and owns the whole device memory pool may forbid its plugins from
+// calling cudaMalloc so that its accounting stays exact, and a
+// latency-critical decode loop cannot afford cudaMalloc/cudaFree on its path,
+// because they can synchronise the whole device and stall every stream.
+//
+// This file gives such callers one entry point that allocates nothing.  Its
+// scratch is a file-scope array in the library's device image, so it exists
+// on every GPU where the library's module is loaded, from load until the
+// process exits, whether or not the entry point is ever called.  The array
+// is TP_STATIC_SCRATCH_BYTES (16 MiB) long, enough for decode-sized batches:
+// e.g. 64 tokens of a Llama-3.1-70B-shaped MLP (h=8192, f=28672) at t=4 with
+// fp32 partials needs 12.1 MB.  Larger requests are refused with
+// TP_ERR_WORKSPACE before anything is launched.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tp.h"
+
+namespace {
+
+static_assert(TP_STATIC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-byte alignment");
+
+// The shared scratch.  Host code must not use this name as an address: on the
+// host it is only a stand-in symbol; the device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_tp_static_scratch[TP_STATIC_SCRATCH_BYTES];
+
+// Device address of the scratch on the current device, looked up once per
+// device (the first call on that device does it) and cached.
+void* static_scratch_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    static void* cache[64] = {nullptr};
+    if (cache[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_tp_static_scratch) != cudaSuccess || p == nullptr) return nullptr;
+        cache[dev] = p;
+    }
+    return cache[dev];
+}
+
+}  // namespace
+
+extern "C" tp_status tp_mlp_forward_static(int t, int64_t n, int64_t h, int64_t f, const void* x, int64_t ldx,
+                                           const void* const* w_gate_up, const void* const* w_down,
+                                           int64_t ld_down, const void* bias_down, tp_act act,
+                                           tp_reduce_mode mode, tp_dtype partial_dtype, void* y, tp_dtype y_dtype,
+                                           tp_stream stream) {
+    const size_t need = tp_mlp_workspace_size(t, n, h, f, mode, partial_dtype);
+    if (need > static_cast<size_t>(TP_STATIC_SCRATCH_BYTES)) return TP_ERR_WORKSPACE;
+    if (need == 0) {
+        // Invalid arguments, or nothing to compute: let the regular entry
+        // point's host-side checks answer, without touching the device.
+        return tp_mlp_forward(t, n, h, f, x, ldx, w_gate_up, w_down, ld_down, bias_down, act, mode, partial_dtype,
+                              nullptr, 0, y, y_dtype, stream);
+    }
+    void* scratch = static_scratch_address();
+    if (scratch == nullptr) return TP_ERR_CUDA;
+    // Every byte of the scratch that this call reads is first written by this
+    // call (H by the gate_up GEMM, each partial by its rank's down GEMM), so
+    // nothing needs clearing between calls.
+    return tp_mlp_forward(t, n, h, f, x, ldx, w_gate_up, w_down, ld_down, bias_down, act, mode, partial_dtype,
+                          scratch, TP_STATIC_SCRATCH_BYTES, y, y_dtype, stream);
+}
