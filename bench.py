@@ -41,8 +41,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the gate_up GEMM at the bench
 # size, from ncu (dram__bytes_read.sum + dram__bytes_write.sum); None until
 # taken for the current kernel.
-TRAFFIC_GLU_FULL = None
-TRAFFIC_NOTE = "not yet captured for this kernel version"
+TRAFFIC_GLU_FULL = 5811692800 + 465259520
+TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch at the bench size (1-pass "
+                "capture, profiles/tp_gemm_traffic_t4_n8192.md); 4.1x the algorithmic bytes: the weights are "
+                "streamed once per band of 16 row-tiles")
 
 
 def load_peaks():
@@ -73,7 +75,7 @@ class ClockSampler:
         try:
             self.out = open(os.path.join("/tmp", f"tp_bench_clocks_{os.getpid()}.csv"), "w+")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -216,14 +218,20 @@ def run_ours(args, rank, world, local_rank):
 
     col_flops = 4.0 * N_TOK * H * F
     red_bytes = (T + 1) * N_TOK * H * 2
-    # A timed region of a few hundred ms runs at boost clock: compare with the
-    # burst GEMM peak; only a seconds-long region is held to the sustained one.
-    long_region = elapsed >= 2.0
+    # The denominator follows the regime the step ran in: a timed region that
+    # ran into the power cap (or lasts seconds) is compared with the sustained
+    # GEMM peak, which was measured under the same cap; a short region that
+    # stayed at boost clock is compared with the burst peak.
+    clk = clocks.summary()
+    capped = "sw_power_cap" in clk.get("reasons", [])
+    long_region = capped or elapsed >= 2.0
     tpeak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
-    tkind = f"bf16 {'sustained' if long_region else 'burst'} ({peak_src})"
+    tkind = (f"bf16 {'sustained' if long_region else 'burst'} ({peak_src}; "
+             f"{'power-capped' if capped else 'no power cap'} in the timed region)")
     roofline = {"bound": "tensor", "kernel": "tp_gemm_kernel<256,4,GLU> (gate_up column GEMM + SiLU*up)",
                 "achieved": col_flops / col_t / 1e12, "peak": tpeak, "unit": "TFLOP/s",
-                "frac": col_flops / col_t / 1e12 / tpeak, "peak_kind": tkind, "traffic": TRAFFIC_GLU_FULL,
+                "frac": col_flops / col_t / 1e12 / tpeak, "peak_kind": tkind,
+                "frac_of_burst": col_flops / col_t / 1e12 / peaks["bf16_tflops"], "traffic": TRAFFIC_GLU_FULL,
                 "traffic_note": TRAFFIC_NOTE, "algorithmic_per_launch": col_flops,
                 "algorithmic_bytes_per_launch": 2.0 * (N_TOK * H + 2 * F * H + N_TOK * F),
                 "launch_ms": col_t * 1e3}
@@ -268,8 +276,9 @@ def run_ours(args, rank, world, local_rank):
                       "partials": "bf16", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                       "l2": "inputs larger than L2 (X 128 MiB, weights 1.41 GB, partials 512 MiB)"},
            "tensor_frac_of_peak": value / tpeak, "tensor_peak_kind": tkind,
+           "tensor_frac_of_burst": value / peaks["bf16_tflops"],
            "shard_reduce": shard_reduce, "roofline": roofline, "e2e": e2e, "gpu_launches": gpu_launches,
-           "clocks": clocks.summary(), "peaks": {**peaks, "source": peak_src}, "detail": detail}
+           "clocks": clk, "peaks": {**peaks, "source": peak_src}, "detail": detail}
     if cpu is not None:
         res["cpu_baseline"] = cpu
     if dist is not None:
@@ -338,17 +347,22 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
     ids = synth.uniform_ids(nt, V, 5, device=dev)
     xh = synth.normal_bf16((nt, hh), 1.0, 7, device=dev)
     logits = torch.empty((nt, V), dtype=torch.bfloat16, device=dev)
+    ids_big = synth.uniform_ids(65536, V, 15, device=dev)
     for t in (2, 4):
         per = (V + t - 1) // t
         shards = [table[r * per:min((r + 1) * per, V)].contiguous() for r in range(t)]
-        e = torch.empty((nt, hh), dtype=torch.bfloat16, device=dev)
-        s = time_fn(torch, lambda: tp.vocab_parallel_embed(ids, shards, V, out=e), 200)
-        byts = nt * 4 + 2 * nt * hh * 2
-        out[f"embed_t{t}"] = {"us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm}
-        graph_s = graph_time(torch, lambda: tp.vocab_parallel_embed(ids, shards, V, out=e), 100)
-        if graph_s:
-            out[f"embed_t{t}"]["graph_us"] = graph_s * 1e6
-            out[f"embed_t{t}"]["graph_GBps"] = byts / graph_s / 1e9
+        for tag, idv in (("", ids), ("_65536ids", ids_big)):
+            m = idv.numel()
+            e = torch.empty((m, hh), dtype=torch.bfloat16, device=dev)
+            s = time_fn(torch, lambda: tp.vocab_parallel_embed(idv, shards, V, out=e), 200 if m == nt else 50)
+            byts = m * 4 + 2 * m * hh * 2
+            rec = {"us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm, "bytes": byts}
+            graph_s = graph_time(torch, lambda: tp.vocab_parallel_embed(idv, shards, V, out=e), 100 if m == nt else 20)
+            if graph_s:
+                rec["graph_us"] = graph_s * 1e6
+                rec["graph_GBps"] = byts / graph_s / 1e9
+                rec["graph_hbm_frac"] = byts / graph_s / 1e9 / hbm
+            out[f"embed_t{t}{tag}"] = rec
         s = time_fn(torch, lambda: tp.lm_head_sharded(xh, shards, V, logits=logits), 10)
         fl = 2.0 * nt * hh * V
         out[f"lm_head_t{t}"] = {"ms": s * 1e3, "tflops": fl / s / 1e12, "frac": fl / s / 1e12 / ten,
@@ -449,7 +463,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=150)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-detail", action="store_true", help="skip the per-row detail timings")

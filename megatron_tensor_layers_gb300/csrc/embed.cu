@@ -48,40 +48,54 @@ __global__ void __launch_bounds__(256) vocab_embed_kernel(const __grid_constant_
         }
         const uint4* src = owner >= 0 ? reinterpret_cast<const uint4*>(a.table[owner]) + local * nvec : nullptr;
         uint4* dst = reinterpret_cast<uint4*>(a.out) + tok * nvec;
-        for (int64_t v = lane; v < nvec; v += 32) {
-            const uint4 row = owner >= 0 ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-            const uint32_t w[4] = {row.x, row.y, row.z, row.w};
-            float x[VEC];
-            if constexpr (BF16) {
+        // Up to U row vectors per lane are loaded before any is stored, so a
+        // warp has the whole 2 KB row (h = 1024 bf16) in flight at once.
+        constexpr int U = 4;
+        for (int64_t v0 = lane; v0 < nvec; v0 += 32 * U) {
+            uint4 row[U];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    x[2 * i] = __uint_as_float(w[i] << 16);
-                    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * 32;
+                row[u] = (owner >= 0 && v < nvec) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * 32;
+                if (v >= nvec) break;
+                const uint32_t w[4] = {row[u].x, row[u].y, row[u].z, row[u].w};
+                float x[VEC];
+                if constexpr (BF16) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        x[2 * i] = __uint_as_float(w[i] << 16);
+                        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) x[i] = __uint_as_float(w[i]);
                 }
-            } else {
+                // The all-reduce: rank 0's masked output, then ranks 1..t-1 added in order.
+                float acc[VEC];
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) x[i] = __uint_as_float(w[i]);
-            }
-            // The all-reduce: rank 0's masked output, then ranks 1..t-1 added in order.
-            float acc[VEC];
+                for (int i = 0; i < VEC; ++i) acc[i] = owner == 0 ? x[i] : 0.0f;
+                for (int r = 1; r < a.t; ++r) {
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) acc[i] = owner == 0 ? x[i] : 0.0f;
-            for (int r = 1; r < a.t; ++r) {
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) acc[i] = acc[i] + (owner == r ? x[i] : 0.0f);
-            }
-            uint4 o;
-            if constexpr (BF16) {
-                o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                               pack_bf16x2(acc[6], acc[7]));
-            } else {
-                o = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
-                               __float_as_uint(acc[3]));
-            }
-            dst[v] = o;
-            if (a.with_partials) {
-                for (int r = 0; r < a.t; ++r)
-                    reinterpret_cast<uint4*>(a.partials[r])[tok * nvec + v] = owner == r ? row : make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < VEC; ++i) acc[i] = acc[i] + (owner == r ? x[i] : 0.0f);
+                }
+                uint4 o;
+                if constexpr (BF16) {
+                    o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+                } else {
+                    o = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                                   __float_as_uint(acc[3]));
+                }
+                dst[v] = o;
+                if (a.with_partials) {
+                    for (int r = 0; r < a.t; ++r)
+                        reinterpret_cast<uint4*>(a.partials[r])[tok * nvec + v] =
+                            owner == r ? row[u] : make_uint4(0, 0, 0, 0);
+                }
             }
         }
     }

@@ -54,9 +54,18 @@ __device__ __forceinline__ void store_elem(void* p, int64_t e, float v, bool as_
         static_cast<float*>(p)[e] = v;
 }
 
+// Index of the ring chunk holding element e: the number of boundaries
+// c * chunk (c = 1 .. t-1) at or below e (compares instead of a 64-bit divide).
+__device__ __forceinline__ int chunk_of(const ReduceArgs& a, int64_t e) {
+    int c = 0;
+#pragma unroll
+    for (int i = 1; i < TP_MAX_SHARDS; ++i) c += (i < a.t && e >= i * a.chunk) ? 1 : 0;
+    return c;
+}
+
 template <bool IN_BF16>
 __device__ void reduce_scalar(const ReduceArgs& a, int64_t e) {
-    const int start = a.ring ? static_cast<int>(e / a.chunk) : 0;
+    const int start = a.ring ? chunk_of(a, e) : 0;
     float acc = load_elem<IN_BF16>(a.p[start], e);
     for (int j = 1; j < a.t; ++j) {
         int r = start + j;
@@ -105,58 +114,88 @@ __device__ __forceinline__ void store_vec(void* base, int64_t e0, const float (&
     }
 }
 
-template <bool IN_BF16>
+// G groups of 16 bytes per buffer are in flight per thread and iteration
+// (G * t 128-bit loads), so that small t still keeps enough bytes moving.
+// Launched with t <= MAXT = 8 / G.
+template <bool IN_BF16, int G>
 __global__ void __launch_bounds__(256) shard_reduce_kernel(const __grid_constant__ ReduceArgs a) {
+    constexpr int MAXT = TP_MAX_SHARDS / G;
     constexpr int VEC = IN_BF16 ? 8 : 4;
+    constexpr int EB = IN_BF16 ? 2 : 4;
     const int64_t ngroups = a.count / VEC;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (int64_t gi = tid; gi < ngroups; gi += stride) {
-        const int64_t e0 = gi * VEC;
-        int start = 0;
-        if (a.ring) {
-            const int64_t c0 = e0 / a.chunk;
-            if (c0 != (e0 + VEC - 1) / a.chunk) {   // a chunk boundary falls inside this vector
-                for (int i = 0; i < VEC; ++i) reduce_scalar<IN_BF16>(a, e0 + i);
-                continue;
-            }
-            start = static_cast<int>(c0);
-        }
-        uint4 v[TP_MAX_SHARDS];
+    for (int64_t g0 = tid; g0 < ngroups; g0 += stride * G) {
+        int start[G];
+        bool live[G];
 #pragma unroll
-        for (int j = 0; j < TP_MAX_SHARDS; ++j) {
-            if (j < a.t) {
-                int r = start + j;
-                if (r >= a.t) r -= a.t;
-                v[j] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const char*>(a.p[r]) + e0 * (IN_BF16 ? 2 : 4)));
+        for (int u = 0; u < G; ++u) {
+            const int64_t gi = g0 + u * stride;
+            live[u] = gi < ngroups;
+            start[u] = 0;
+            if (live[u] && a.ring) {
+                const int64_t e0 = gi * VEC;
+                const int c0 = chunk_of(a, e0);
+                // a vector that a chunk boundary cuts is done element by element below
+                if (c0 != chunk_of(a, e0 + VEC - 1)) live[u] = false;
+                start[u] = c0;
             }
         }
-        float acc[VEC];
-        unpack<IN_BF16>(v[0], acc);
+        uint4 v[G][MAXT];
 #pragma unroll
-        for (int j = 1; j < TP_MAX_SHARDS; ++j) {
-            if (j < a.t) {
-                float x[VEC];
-                unpack<IN_BF16>(v[j], x);
-                if (a.hop_bf16) {
+        for (int u = 0; u < G; ++u) {
 #pragma unroll
-                    for (int i = 0; i < VEC; ++i) acc[i] = round_bf16(acc[i] + x[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < VEC; ++i) acc[i] = acc[i] + x[i];
+            for (int j = 0; j < MAXT; ++j) {
+                if (live[u] && j < a.t) {
+                    int r = start[u] + j;
+                    if (r >= a.t) r -= a.t;
+                    v[u][j] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const char*>(a.p[r]) +
+                                                                     (g0 + u * stride) * VEC * EB));
                 }
             }
         }
-        if (a.out) store_vec<VEC>(a.out, e0, acc, a.out_bf16 != 0);
-        if (a.replicate) {
 #pragma unroll
-            for (int r = 0; r < TP_MAX_SHARDS; ++r)
-                if (r < a.t) store_vec<VEC>(const_cast<void*>(a.p[r]), e0, acc, IN_BF16);
+        for (int u = 0; u < G; ++u) {
+            if (!live[u]) continue;
+            const int64_t e0 = (g0 + u * stride) * VEC;
+            float acc[VEC];
+            unpack<IN_BF16>(v[u][0], acc);
+#pragma unroll
+            for (int j = 1; j < MAXT; ++j) {
+                if (j < a.t) {
+                    float x[VEC];
+                    unpack<IN_BF16>(v[u][j], x);
+                    if (a.hop_bf16) {
+#pragma unroll
+                        for (int i = 0; i < VEC; ++i) acc[i] = round_bf16(acc[i] + x[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < VEC; ++i) acc[i] = acc[i] + x[i];
+                    }
+                }
+            }
+            if (a.out) store_vec<VEC>(a.out, e0, acc, a.out_bf16 != 0);
+            if (a.replicate) {
+#pragma unroll
+                for (int r = 0; r < MAXT; ++r)
+                    if (r < a.t) store_vec<VEC>(const_cast<void*>(a.p[r]), e0, acc, IN_BF16);
+            }
         }
     }
     // ragged tail (count % VEC elements)
     const int64_t tail0 = ngroups * VEC;
     if (tid < a.count - tail0) reduce_scalar<IN_BF16>(a, tail0 + tid);
+    // ring: the vectors cut by one of the t-1 chunk boundaries, one element per thread
+    // (the smallest boundary inside a vector owns it, so no element is done twice)
+    if (a.ring && tid < static_cast<int64_t>(a.t - 1) * VEC) {
+        const int c = static_cast<int>(tid / VEC) + 1;         // boundary c * chunk, c = 1 .. t-1
+        const int64_t b = c * a.chunk;
+        const int64_t gb = b / VEC;
+        bool owner = b % VEC != 0 && gb < ngroups;
+        for (int cp = c - 1; owner && cp >= 1 && (cp * a.chunk) / VEC == gb; --cp)
+            if ((cp * a.chunk) % VEC != 0) owner = false;
+        if (owner) reduce_scalar<IN_BF16>(a, gb * VEC + tid % VEC);
+    }
 }
 
 static int sm_count_cached() {
@@ -183,14 +222,21 @@ tp_status launch_shard_reduce(const ReduceDesc& d, cudaStream_t stream) {
     a.out_bf16 = d.out_bf16;
     a.replicate = d.replicate;
     const int vec = d.in_bf16 ? 8 : 4;
+    // groups in flight per thread: about 8 loads of 16 bytes whatever t is
+    const int G = d.t <= 2 ? 4 : (d.t <= 4 ? 2 : 1);
     const int64_t groups = std::max<int64_t>(d.count / vec, d.count % vec);
     const int sms = std::max(1, sm_count_cached());
-    const int64_t want = (groups + 255) / 256;
+    const int64_t want = (groups + 256 * G - 1) / (256 * G);
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
-    if (d.in_bf16)
-        shard_reduce_kernel<true><<<grid, 256, 0, stream>>>(a);
-    else
-        shard_reduce_kernel<false><<<grid, 256, 0, stream>>>(a);
+    if (d.in_bf16) {
+        if (G == 4) shard_reduce_kernel<true, 4><<<grid, 256, 0, stream>>>(a);
+        else if (G == 2) shard_reduce_kernel<true, 2><<<grid, 256, 0, stream>>>(a);
+        else shard_reduce_kernel<true, 1><<<grid, 256, 0, stream>>>(a);
+    } else {
+        if (G == 4) shard_reduce_kernel<false, 4><<<grid, 256, 0, stream>>>(a);
+        else if (G == 2) shard_reduce_kernel<false, 2><<<grid, 256, 0, stream>>>(a);
+        else shard_reduce_kernel<false, 1><<<grid, 256, 0, stream>>>(a);
+    }
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 

@@ -450,3 +450,22 @@ def test_every_tile_width_gated(tile_n):
         w = f64(wgu[r])
         ref = O.glu(O.linear(f64(x), w[:fs]), O.linear(f64(x), w[fs:]), "silu")
         gemm_gate(f64(ys[r]), ref, bf16_out=False)
+
+
+@pytest.mark.parametrize("t", [3, 5, 8])
+@pytest.mark.parametrize("count", [20, 37, 100, 1003])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_shard_reduce_ring_chunks_shorter_than_vectors(t, count, dtype):
+    # chunk = ceil(count/t) can be shorter than a 16-byte vector, so several
+    # chunk boundaries cut the same vector; with replicate every element must
+    # still be folded exactly once from the original partials.
+    parts = _partials(t, count, dtype, 900 + t)
+    pf = [f64(p) for p in parts]
+    out = torch.empty((count,), dtype=torch.float32, device=DEV)
+    tp.tp_shard_reduce(parts, out=out, mode="ring", replicate=True)
+    torch.cuda.synchronize()
+    bufs, _ = O.ring_allreduce(pf, hop="f32")
+    exact(f64(out), bufs[0])
+    rounded = O.round_to_bf16(bufs[0]) if dtype == torch.bfloat16 else bufs[0]
+    for p in parts:
+        exact(f64(p), rounded)
