@@ -41,10 +41,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the gate_up GEMM at the bench
 # size, from ncu (dram__bytes_read.sum + dram__bytes_write.sum); None until
 # taken for the current kernel.
-TRAFFIC_GLU_FULL = 5811692800 + 465259520
-TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch at the bench size (1-pass "
-                "capture, profiles/tp_gemm_traffic_t4_n8192.md); 4.1x the algorithmic bytes: the weights are "
-                "streamed once per band of 16 row-tiles")
+TRAFFIC_GLU_FULL = None
+TRAFFIC_NOTE = ("not captured yet for the CTA-pair kernel (the 1-CTA kernel's capture is in "
+                "profiles/tp_gemm_traffic_t4_n8192.md)")
 
 
 def load_peaks():
@@ -228,7 +227,7 @@ def run_ours(args, rank, world, local_rank):
     tpeak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
     tkind = (f"bf16 {'sustained' if long_region else 'burst'} ({peak_src}; "
              f"{'power-capped' if capped else 'no power cap'} in the timed region)")
-    roofline = {"bound": "tensor", "kernel": "tp_gemm_kernel<256,4,GLU> (gate_up column GEMM + SiLU*up)",
+    roofline = {"bound": "tensor", "kernel": "tp_gemm_pair_kernel<6,GLU> (gate_up column GEMM + SiLU*up, CTA pairs)",
                 "achieved": col_flops / col_t / 1e12, "peak": tpeak, "unit": "TFLOP/s",
                 "frac": col_flops / col_t / 1e12 / tpeak, "peak_kind": tkind,
                 "frac_of_burst": col_flops / col_t / 1e12 / peaks["bf16_tflops"], "traffic": TRAFFIC_GLU_FULL,

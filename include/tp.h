@@ -317,6 +317,15 @@ void tp_reset_collective_count(void);
 tp_status tp_set_gemm_tile_n(int n);
 
 /*
+ * Use of the CTA-pair GEMM kernel (256 x 256 tiles computed by two CTAs on
+ * neighbouring SMs with tcgen05 cta_group::2) for later launches: 1 = always,
+ * -1 = never, 0 = automatic (pairs when a GEMM has at least 512 rows and two
+ * full waves of pair tiles).  For tests and tuning.  TP_ERR_INVALID_ARG for
+ * other values.
+ */
+tp_status tp_set_gemm_cta_pair(int mode);
+
+/*
  * Test hook for the failure path: launches one thread block that waits, with
  * the library's bounded wait, on a shared-memory barrier that nothing ever
  * signals.  The wait gives up after `limit_ns` nanoseconds (capped at 1 s)

@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     tp_mlp_forward,
     tp_mlp_workspace_size,
     tp_reset_collective_count,
+    tp_set_gemm_cta_pair,
     tp_set_gemm_tile_n,
     tp_shard_gather,
     tp_shard_reduce,

@@ -32,7 +32,7 @@ EXPORTED = [
     "tp_status_string", "tp_abi_version", "tp_linear_col", "tp_linear_row", "tp_shard_reduce",
     "tp_mlp_workspace_size", "tp_mlp_forward", "vocab_parallel_embed", "lm_head_sharded",
     "tp_shard_gather", "tp_device_status", "tp_collective_count", "tp_reset_collective_count",
-    "tp_debug_expire_wait", "tp_set_gemm_tile_n", "tp_mlp_forward_static",
+    "tp_debug_expire_wait", "tp_set_gemm_tile_n", "tp_mlp_forward_static", "tp_set_gemm_cta_pair",
 ]
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -73,6 +73,7 @@ def load() -> ctypes.CDLL:
         "tp_reset_collective_count": (None, []),
         "tp_debug_expire_wait": (I32, [ctypes.c_uint64, P]),
         "tp_set_gemm_tile_n": (I32, [I32]),
+        "tp_set_gemm_cta_pair": (I32, [I32]),
         "tp_mlp_forward_static": (I32, [I32, I64, I64, I64, P, I64, P, P, I64, P, I32, I32, I32, P, I32, P]),
     }
     for name, (res, args) in sig.items():
@@ -277,6 +278,11 @@ def tp_reset_collective_count() -> None:
 
 def tp_debug_expire_wait(limit_ns: int, stream=None) -> None:
     _check("tp_debug_expire_wait", load().tp_debug_expire_wait(limit_ns, _stream(stream)))
+
+
+def tp_set_gemm_cta_pair(mode: int) -> None:
+    """1: always use the CTA-pair GEMM kernel, -1: never, 0: automatic."""
+    _check("tp_set_gemm_cta_pair", load().tp_set_gemm_cta_pair(mode))
 
 
 def tp_set_gemm_tile_n(n: int) -> None:

@@ -19,6 +19,7 @@ namespace {
 
 std::atomic<uint64_t> g_collectives{0};
 std::atomic<int> g_tile_n{0};
+std::atomic<int> g_pair{0};
 
 int* status_ptr() {
     int dev = 0;
@@ -111,6 +112,7 @@ tp_status tp_linear_col(int t, int64_t n, int64_t in, int64_t out_full, const vo
     d.out_f32 = y_dtype == TP_F32;
     d.status = status_ptr();
     d.force_bn = g_tile_n.load();
+    d.pair = g_pair.load();
     for (int r = 0; r < t; ++r) {
         d.b[r] = w[r];
         d.out[r] = gather_output ? static_cast<void*>(static_cast<char*>(y[0]) + r * os * ey) : y[r];
@@ -198,6 +200,7 @@ tp_status tp_linear_row(int t, int64_t n, int64_t in_full, int64_t out, const vo
     d.b_rows = out;
     d.status = status_ptr();
     d.force_bn = g_tile_n.load();
+    d.pair = g_pair.load();
     if (fused) {
         d.groups = 1;
         d.segs = t;
@@ -290,6 +293,7 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, 
     c.out_f32 = 0;
     c.status = status_ptr();
     c.force_bn = g_tile_n.load();
+    c.pair = g_pair.load();
     for (int r = 0; r < t; ++r) {
         c.b[r] = w_gate_up[r];
         c.out[r] = hbuf + r * fs;
@@ -372,6 +376,7 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab, const void
     d.ldo = logits != nullptr ? ldl : 0;
     d.status = status_ptr();
     d.force_bn = g_tile_n.load();
+    d.pair = g_pair.load();
     int g = 0;
     for (int r = 0; r < t; ++r) {
         const int64_t start = std::min<int64_t>(r * per, vocab);
@@ -455,6 +460,12 @@ tp_status tp_device_status(tp_stream stream) {
 tp_status tp_set_gemm_tile_n(int n) {
     if (n != 0 && n != 64 && n != 128 && n != 256) return TP_ERR_INVALID_ARG;
     g_tile_n.store(n);
+    return TP_OK;
+}
+
+tp_status tp_set_gemm_cta_pair(int mode) {
+    if (mode < -1 || mode > 1) return TP_ERR_INVALID_ARG;
+    g_pair.store(mode);
     return TP_OK;
 }
 

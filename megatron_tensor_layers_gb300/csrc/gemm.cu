@@ -332,6 +332,230 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     }
 }
 
+// ---------------------------------------------------------- CTA-pair kernel
+//
+// The same computation on 256 x 256 tiles shared by a cluster of two CTAs on
+// neighbouring SMs (tcgen05 cta_group::2).  CTA r of the pair loads rows
+// [128r, 128r+128) of the tile's A rows and the r-th 128-row half of its B
+// rows (for the gated epilogue: CTA 0 the gate rows, CTA 1 the same rows of
+// up); the even CTA issues one M=256, N=256, K=16 MMA that reads both CTAs'
+// shared memory and writes each CTA's 128 rows x 256 columns into that CTA's
+// TMEM.  Per SM this halves the B bytes that TMA writes into, and the tensor
+// core reads out of, shared memory for the same FLOPs, which is what bounds
+// the single-CTA kernel.  Both CTAs' loads complete on the even CTA's
+// full barrier; MMA completion is multicast to both CTAs' stage and
+// accumulator barriers; both epilogues report back to the even CTA.
+template <int STAGES, int EPI>
+struct PairCfg {
+    static constexpr int BN = 256;                           // MMA N (full tile width)
+    static constexpr int A_BYTES = 128 * BK * 2;             // this CTA's 128 rows of A
+    static constexpr int B_BYTES = 128 * BK * 2;             // this CTA's half of B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int OUT_COLS = (EPI == EPI_GLU) ? BN / 2 : BN;
+    static constexpr int TILE_M = 256;
+    static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+};
+
+template <int STAGES, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_constant__ GemmArgs args) {
+    using Cfg = PairCfg<STAGES, EPI>;
+    constexpr int BN = Cfg::BN;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const uint32_t bar_base = base + STAGES * Cfg::STAGE_BYTES;
+    uint8_t* bar_ptr = base_ptr + STAGES * Cfg::STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * (2 * STAGES + 4) + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();          // 0: issues the MMAs; 1: its peer
+    const int cluster = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 8);              // 4 epilogue warps x 2 CTAs
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < args.groups && i < TP_MAX_SHARDS; ++i) prefetch_tmap(&args.mapB[i]);
+        prefetch_tmap(&args.mapA[0]);
+    }
+    if (warp == 1) tmem_alloc_pair<Cfg::TMEM_COLS>(smem_u32(tmem_slot));
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                                    // both CTAs' barriers exist before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int kb_per_tile = args.k_blocks * args.segs;
+    bool aborted = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
+                int g, m, n;
+                tile_coords(args, tile, g, m, n);
+                const int a_row = m * Cfg::TILE_M + static_cast<int>(rank) * 128;
+                const int b_row = (EPI == EPI_GLU) ? (rank == 0 ? n * 128 : args.glu_up_row + n * 128)
+                                                   : n * BN + static_cast<int>(rank) * 128;
+                for (int kk = 0; kk < kb_per_tile; ++kk) {
+                    const int seg = kk / args.k_blocks;
+                    const int kb = kk - seg * args.k_blocks;
+                    const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                    const int bi = args.segs > 1 ? seg : g;
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
+                        aborted = true;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
+                    const uint32_t sb = sa + Cfg::A_BYTES;
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+                    const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+                    tma_load_2d_pair(sa, &args.mapA[ai], leader_full, kb * BK, a_row);
+                    tma_load_2d_pair(sb, &args.mapB[bi], leader_full, kb * BK, b_row);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ MMA issuer (even CTA)
+            constexpr uint32_t idesc = mma_idesc_bf16(256, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kk = 0; kk < kb_per_tile; ++kk) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.status)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        tc_mma_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0 ? 1u : 0u);
+                    tc_commit_pair(empty_bar(stage), 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (aborted) break;
+                tc_commit_pair(tfull_bar(acc), 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (both CTAs)
+        const int q = warp & 3;
+        const int row_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = cluster; tile < args.total_tiles; tile += nclusters) {
+            int g, m, n;
+            tile_coords(args, tile, g, m, n);
+            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            const int64_t grow = static_cast<int64_t>(m) * Cfg::TILE_M + rank * 128 + row_in_tile;
+            const bool row_ok = grow < args.M;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            void* out = args.out[g];
+            const uint16_t* bias = static_cast<const uint16_t*>(args.bias[g]);
+            const int ncols = args.n_valid[g];
+            if (EPI == EPI_GLU) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t rg[32], ru[32];
+                    tmem_ld32(taddr + c * 32, rg);
+                    tmem_ld32(taddr + BN / 2 + c * 32, ru);
+                    tmem_ld_wait();
+                    const int col0 = n * (BN / 2) + c * 32;
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = act_fn(__uint_as_float(rg[j]), args.act) * __uint_as_float(ru[j]);
+                    if (row_ok) store_chunk(out, args.ldo, args.out_f32, grow, col0, min(32, ncols - col0), v);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + c * 32, r);
+                    tmem_ld_wait();
+                    const int col0 = n * BN + c * 32;
+                    const int nvalid = min(32, ncols - col0);
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if (bias != nullptr) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nvalid) v[j] += bf16_to_f32(bias[col0 + j]);
+                    }
+                    if (row_ok) store_chunk(out, args.ldo, args.out_f32, grow, col0, nvalid, v);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    if (aborted) spin_ns(50000);
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) spin_ns(50000);
+    cluster_sync();                                    // no MMA or remote arrive still targets the peer
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair<Cfg::TMEM_COLS>(tmem_base);
+    }
+}
+
 // ------------------------------------------------------------------ host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -403,6 +627,52 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
+template <int STAGES, int EPI>
+static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream) {
+    using Cfg = PairCfg<STAGES, EPI>;
+    a.m_tiles = static_cast<int>((d.M + Cfg::TILE_M - 1) / Cfg::TILE_M);
+    a.n_tiles = static_cast<int>((d.N + Cfg::OUT_COLS - 1) / Cfg::OUT_COLS);
+    a.total_tiles = a.groups * a.m_tiles * a.n_tiles;
+    if (a.total_tiles == 0) return TP_OK;
+    const int nA = d.segs > 1 ? d.segs : (d.a_per_group ? d.groups : 1);
+    const int nB = d.segs > 1 ? d.segs : d.groups;
+    for (int i = 0; i < nA; ++i)
+        if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, 128)) return TP_ERR_CUDA;
+    for (int i = 0; i < nB; ++i) {
+        const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
+        if (!make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, 128)) return TP_ERR_CUDA;
+    }
+    auto kern = tp_gemm_pair_kernel<STAGES, EPI>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+        return TP_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms < 2) return TP_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // A persistent grid of pairs that can all be resident at once.
+    static int max_clusters[2] = {0, 0};
+    int& mc = max_clusters[EPI == EPI_GLU ? 1 : 0];
+    if (mc <= 0) {
+        int v = 0;
+        if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess || v <= 0) v = sms / 2;
+        mc = std::min(v, sms / 2);
+    }
+    const int clusters = std::min(a.total_tiles, mc);
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TP_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
 // Estimated time units of a launch with output tile width w: whole waves of
 // tiles times the per-tile cost (proportional to the MMA N plus a fixed
 // share for the A tile).
@@ -449,6 +719,18 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
         }
     }
     if (d.force_bn) best = d.force_bn;
+    // CTA pairs for problems with at least two full waves of 256-row tiles.
+    bool pair = false;
+    if (d.pair >= 0 && sms >= 2) {
+        const int out_cols = glu ? 128 : 256;
+        const long long pair_tiles = static_cast<long long>(d.groups) * ((d.M + 255) / 256) *
+                                     ((d.N + out_cols - 1) / out_cols);
+        pair = d.pair > 0 || (d.M >= 512 && pair_tiles >= 2LL * (sms / 2) && d.force_bn == 0);
+    }
+    if (pair) {
+        if (glu) return launch_pair<6, EPI_GLU>(a, d, stream);
+        return launch_pair<6, EPI_STORE>(a, d, stream);
+    }
     if (glu) {
         if (best == 256) return launch_cfg<256, 4, EPI_GLU>(a, d, stream);
         if (best == 128) return launch_cfg<128, 6, EPI_GLU>(a, d, stream);

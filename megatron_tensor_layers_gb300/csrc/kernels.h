@@ -31,6 +31,7 @@ struct GemmDesc {
     int out_f32 = 0;
     int* status = nullptr;
     int force_bn = 0;                    // 0: chosen by cost; else 64/128/256
+    int pair = 0;                        // CTA-pair kernel: -1 never, 0 automatic, 1 always
 };
 
 tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream);

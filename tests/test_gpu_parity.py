@@ -469,3 +469,72 @@ def test_shard_reduce_ring_chunks_shorter_than_vectors(t, count, dtype):
     rounded = O.round_to_bf16(bufs[0]) if dtype == torch.bfloat16 else bufs[0]
     for p in parts:
         exact(f64(p), rounded)
+
+
+# ------------------------------------------------------ CTA-pair GEMM kernel
+
+@pytest.fixture
+def pair_on():
+    tp.tp_set_gemm_cta_pair(1)
+    yield
+    tp.tp_set_gemm_cta_pair(0)
+
+
+def test_pair_kernel_integer_exact(pair_on):
+    # ragged M (300: the second CTA of the second tile has no rows), N, K
+    t, n, k, os_ = 2, 300, 536, 200
+    x = ints((n, k), 190)
+    w = [ints((os_, k), 191 + r) for r in range(t)]
+    b = [ints((os_,), 193 + r, -8, 8) for r in range(t)]
+    y = tp.tp_linear_col(x, w, bias=b, y_dtype=torch.float32)
+    yg = tp.tp_linear_col(x, w, bias=b, gather_output=True, y_dtype=torch.float32)
+    xs = [ints((n, 136), 195 + r) for r in range(3)]
+    ws = [ints((264, 136), 198 + r) for r in range(3)]
+    yf = tp.tp_linear_row(xs, ws, mode="fused", y_dtype=torch.float32)
+    yd = tp.tp_linear_row(xs, ws, mode="direct", partial_dtype=torch.float32, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    refs = [O.linear(f64(x), f64(w[r]), f64(b[r])) for r in range(t)]
+    for r in range(t):
+        exact(f64(y[r]), refs[r])
+    exact(f64(yg), O.shard_gather(refs))
+    ref = O.reduce_direct([O.linear(f64(xs[r]), f64(ws[r])) for r in range(3)])
+    exact(f64(yf), ref)
+    exact(f64(yd), ref)
+    assert tp.tp_device_status() == 0
+
+
+@pytest.mark.parametrize("t,V,n,h", [(3, 1000, 520, 128), (4, 151936, 256, 1024)])
+def test_pair_kernel_lm_head(pair_on, t, V, n, h):
+    x = ints((n, h), 210)
+    table = ints((V, h), 211)
+    logits = tp.lm_head_sharded(x, _table_shards(table, t), V, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rows = sorted({r for r in (0, 1, 127, 128, 255, 256, n - 1) if r < n})
+    exact(f64(logits[rows]), O.lm_head_unsharded(f64(x[rows]), f64(table)))
+
+
+def test_pair_kernel_gated(pair_on):
+    t, n, h, fs = 2, 600, 320, 200
+    x = normal((n, h), 1.0, 220)
+    wgu = [normal((2 * fs, h), 0.05, 221 + r) for r in range(t)]
+    ys = tp.tp_linear_col(x, wgu, act="silu", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for r in range(t):
+        w = f64(wgu[r])
+        ref = O.glu(O.linear(f64(x), w[:fs]), O.linear(f64(x), w[fs:]), "silu")
+        gemm_gate(f64(ys[r]), ref, bf16_out=False)
+
+
+@pytest.mark.parametrize("mode", ["direct", "fused"])
+def test_pair_kernel_mlp(pair_on, mode):
+    t, n, h, f = 2, 520, 1024, 3072
+    fs = f // t
+    x = normal((n, h), 1.0, 230)
+    wg, wu, wd = normal((f, h), 0.02, 231), normal((f, h), 0.02, 232), normal((h, f), 0.02, 233)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds = [wd[:, r * fs:(r + 1) * fs] for r in range(t)]
+    y = tp.tp_mlp_forward(x, wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    xf, wgf, wuf, wdf = f64(x), f64(wg), f64(wu), f64(wd)
+    ref = O.mlp_unsharded(xf, wgf, wuf, wdf, None, "silu")
+    gemm_gate(f64(y), ref, bf16_out=False, extra=_mlp_rounding_allowance(xf, wgf, wuf, wdf, t, "silu", False))
