@@ -116,8 +116,23 @@ tp_status launch_vocab_embed(const EmbedDesc& d, cudaStream_t stream) {
     a.per = d.per;
     a.t = d.t;
     a.with_partials = d.with_partials;
-    const int64_t threads = d.n * 32;
-    const int grid = static_cast<int>(std::min<int64_t>((threads + 255) / 256, 65535));
+    // one warp per token; at most one resident wave of blocks (grid-stride beyond)
+    const int64_t want = (d.n * 32 + 255) / 256;
+    static int sms = 0, per_sm[2] = {0, 0};
+    if (sms <= 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    int& occ = per_sm[d.bf16 ? 1 : 0];
+    if (occ <= 0) {
+        if (d.bf16)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, vocab_embed_kernel<true>, 256, 0);
+        else
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, vocab_embed_kernel<false>, 256, 0);
+    }
+    const int64_t resident = static_cast<int64_t>(std::max(sms, 1)) * std::max(occ, 1);
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, resident)));
     if (d.bf16)
         vocab_embed_kernel<true><<<grid, 256, 0, stream>>>(a);
     else

@@ -44,7 +44,6 @@ namespace tpk {
 constexpr int BM = 128;          // tile rows (tokens) = TMEM lanes
 constexpr int BK = 64;           // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kThreads = 192;
-constexpr int kGroupM = 16;      // tile raster: bands of 16 row-tiles share B tiles in L2
 
 enum { EPI_STORE = 0, EPI_GLU = 1 };
 
@@ -63,6 +62,8 @@ struct GemmArgs {
     int segs;                         // K segments accumulated into one tile
     int a_per_group;                  // A map index = group (else 0); with segs > 1 it is the segment
     int glu_up_row;                   // row offset of the up block inside B (gated epilogue)
+    int group_m;                      // tile raster: bands of group_m row-tiles (about 32 MB of A rows)
+    int a_box_rows;                   // rows of A a TMA box loads (<= 128; fewer when M is small)
     int act;                          // tp_act for the gated epilogue
     int* status;                      // library status word
 };
@@ -71,10 +72,10 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g,
     const int per_group = a.m_tiles * a.n_tiles;
     g = tile / per_group;
     const int l = tile - g * per_group;
-    const int width = kGroupM * a.n_tiles;
+    const int width = a.group_m * a.n_tiles;
     const int band = l / width;
-    const int first_m = band * kGroupM;
-    const int gm = min(a.m_tiles - first_m, kGroupM);
+    const int first_m = band * a.group_m;
+    const int gm = min(a.m_tiles - first_m, a.group_m);
     const int r = l - band * width;
     m = first_m + r % gm;
     n = r / gm;
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                     }
                     const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
                     const uint32_t sb = sa + Cfg::A_BYTES;
-                    mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES);
+                    mbar_arrive_expect_tx(full_bar(stage), args.a_box_rows * 128 + Cfg::B_BYTES);
                     tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);
                     if (EPI == EPI_GLU) {
                         tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * (BN / 2));
@@ -602,6 +603,14 @@ static int sm_count() {
     return n;
 }
 
+// Row-tiles per raster band: as many as keep about 32 MB of A rows (the
+// operand a band re-reads for every column of tiles) resident in L2.
+static int raster_band(int tile_rows, int64_t k_total) {
+    const int64_t tile_bytes = static_cast<int64_t>(tile_rows) * k_total * 2;
+    const int64_t band = (32ll << 20) / std::max<int64_t>(tile_bytes, 1);
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(band, 64)));
+}
+
 template <int BN, int STAGES, int EPI>
 static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream) {
     using Cfg = GemmCfg<BN, STAGES, EPI>;
@@ -611,8 +620,12 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
     const int b_box = (EPI == EPI_GLU) ? BN / 2 : BN;
     const int nA = d.segs > 1 ? d.segs : (d.a_per_group ? d.groups : 1);
     const int nB = d.segs > 1 ? d.segs : d.groups;
+    // A box only as tall as the rows that exist (decode: a handful of tokens);
+    // the rest of the 128-row shared tile is never read into an output row.
+    a.a_box_rows = static_cast<int>(std::min<int64_t>(BM, (d.M + 7) / 8 * 8));
+    a.group_m = raster_band(BM, d.K * d.segs);
     for (int i = 0; i < nA; ++i)
-        if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, BM)) return TP_ERR_CUDA;
+        if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
     for (int i = 0; i < nB; ++i) {
         const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
         if (!make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box)) return TP_ERR_CUDA;
@@ -631,6 +644,8 @@ template <int STAGES, int EPI>
 static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream) {
     using Cfg = PairCfg<STAGES, EPI>;
     a.m_tiles = static_cast<int>((d.M + Cfg::TILE_M - 1) / Cfg::TILE_M);
+    a.group_m = raster_band(Cfg::TILE_M, d.K * d.segs);
+    a.a_box_rows = 128;
     a.n_tiles = static_cast<int>((d.N + Cfg::OUT_COLS - 1) / Cfg::OUT_COLS);
     a.total_tiles = a.groups * a.m_tiles * a.n_tiles;
     if (a.total_tiles == 0) return TP_OK;

@@ -114,50 +114,47 @@ __device__ __forceinline__ void store_vec(void* base, int64_t e0, const float (&
     }
 }
 
-// G groups of 16 bytes per buffer are in flight per thread and iteration
-// (G * t 128-bit loads), so that small t still keeps enough bytes moving.
+// One slice of the reduction per blockIdx.y: the whole buffer in DIRECT
+// order, ring chunk y in RING order.  Inside a slice every block folds the
+// t buffers in the same rotated order (y, y+1, ... mod t), with G vectors of
+// 16 bytes per buffer in flight per thread (G * t 128-bit loads) so that a
+// small t still keeps enough bytes moving.  Elements of the slice that do
+// not fill a whole aligned vector (its ends, when a chunk boundary or the
+// buffer end is not vector aligned) are folded one by one by block 0.
 // Launched with t <= MAXT = 8 / G.
 template <bool IN_BF16, int G>
 __global__ void __launch_bounds__(256) shard_reduce_kernel(const __grid_constant__ ReduceArgs a) {
     constexpr int MAXT = TP_MAX_SHARDS / G;
     constexpr int VEC = IN_BF16 ? 8 : 4;
     constexpr int EB = IN_BF16 ? 2 : 4;
-    const int64_t ngroups = a.count / VEC;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (int64_t g0 = tid; g0 < ngroups; g0 += stride * G) {
-        int start[G];
-        bool live[G];
+    const int slice = blockIdx.y;
+    const int64_t lo = a.ring ? min(static_cast<int64_t>(slice) * a.chunk, a.count) : 0;
+    const int64_t hi = a.ring ? min(lo + a.chunk, a.count) : a.count;
+    const int64_t v_lo = (lo + VEC - 1) / VEC;        // whole vectors inside [lo, hi)
+    const int64_t v_hi = hi / VEC;
+    const char* q[MAXT];
 #pragma unroll
-        for (int u = 0; u < G; ++u) {
-            const int64_t gi = g0 + u * stride;
-            live[u] = gi < ngroups;
-            start[u] = 0;
-            if (live[u] && a.ring) {
-                const int64_t e0 = gi * VEC;
-                const int c0 = chunk_of(a, e0);
-                // a vector that a chunk boundary cuts is done element by element below
-                if (c0 != chunk_of(a, e0 + VEC - 1)) live[u] = false;
-                start[u] = c0;
-            }
-        }
+    for (int j = 0; j < MAXT; ++j) {
+        int r = slice + j;
+        while (r >= a.t) r -= a.t;
+        q[j] = static_cast<const char*>(a.p[j < a.t ? r : 0]);
+    }
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t g0 = v_lo + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g0 < v_hi;
+         g0 += stride * G) {
         uint4 v[G][MAXT];
 #pragma unroll
         for (int u = 0; u < G; ++u) {
+            const int64_t gi = g0 + u * stride;
 #pragma unroll
-            for (int j = 0; j < MAXT; ++j) {
-                if (live[u] && j < a.t) {
-                    int r = start[u] + j;
-                    if (r >= a.t) r -= a.t;
-                    v[u][j] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const char*>(a.p[r]) +
-                                                                     (g0 + u * stride) * VEC * EB));
-                }
-            }
+            for (int j = 0; j < MAXT; ++j)
+                if (gi < v_hi && j < a.t) v[u][j] = __ldcs(reinterpret_cast<const uint4*>(q[j] + gi * VEC * EB));
         }
 #pragma unroll
         for (int u = 0; u < G; ++u) {
-            if (!live[u]) continue;
-            const int64_t e0 = (g0 + u * stride) * VEC;
+            const int64_t gi = g0 + u * stride;
+            if (gi >= v_hi) continue;
+            const int64_t e0 = gi * VEC;
             float acc[VEC];
             unpack<IN_BF16>(v[u][0], acc);
 #pragma unroll
@@ -182,20 +179,27 @@ __global__ void __launch_bounds__(256) shard_reduce_kernel(const __grid_constant
             }
         }
     }
-    // ragged tail (count % VEC elements)
-    const int64_t tail0 = ngroups * VEC;
-    if (tid < a.count - tail0) reduce_scalar<IN_BF16>(a, tail0 + tid);
-    // ring: the vectors cut by one of the t-1 chunk boundaries, one element per thread
-    // (the smallest boundary inside a vector owns it, so no element is done twice)
-    if (a.ring && tid < static_cast<int64_t>(a.t - 1) * VEC) {
-        const int c = static_cast<int>(tid / VEC) + 1;         // boundary c * chunk, c = 1 .. t-1
-        const int64_t b = c * a.chunk;
-        const int64_t gb = b / VEC;
-        bool owner = b % VEC != 0 && gb < ngroups;
-        for (int cp = c - 1; owner && cp >= 1 && (cp * a.chunk) / VEC == gb; --cp)
-            if ((cp * a.chunk) % VEC != 0) owner = false;
-        if (owner) reduce_scalar<IN_BF16>(a, gb * VEC + tid % VEC);
+    if (blockIdx.x == 0) {
+        // the slice's elements outside whole vectors: [lo, v_lo*VEC) and [v_hi*VEC, hi),
+        // or all of [lo, hi) when no whole vector fits
+        const int64_t head_end = v_lo < v_hi ? v_lo * VEC : hi;
+        const int64_t tail_beg = v_lo < v_hi ? v_hi * VEC : hi;
+        for (int64_t e = lo + threadIdx.x; e < head_end; e += blockDim.x) reduce_scalar<IN_BF16>(a, e);
+        for (int64_t e = tail_beg + threadIdx.x; e < hi; e += blockDim.x) reduce_scalar<IN_BF16>(a, e);
     }
+}
+
+template <bool IN_BF16, int G>
+static int resident_blocks() {
+    static int n = 0;
+    if (n <= 0) {
+        int v = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, shard_reduce_kernel<IN_BF16, G>, 256, 0) != cudaSuccess ||
+            v <= 0)
+            v = 2;
+        n = v;
+    }
+    return n;
 }
 
 static int sm_count_cached() {
@@ -207,6 +211,19 @@ static int sm_count_cached() {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (dev < 64) cache[dev] = n;
     return n;
+}
+
+template <bool IN_BF16, int G>
+static void launch_reduce_cfg(const ReduceArgs& a, int64_t count, int t, bool ring, cudaStream_t stream) {
+    constexpr int VEC = IN_BF16 ? 8 : 4;
+    const int slices = ring ? t : 1;
+    const int64_t per_slice = (ring ? (count + t - 1) / t : count) / VEC + 1;
+    const int sms = std::max(1, sm_count_cached());
+    // one persistent wave: all resident blocks of the GPU, shared by the slices
+    const int64_t resident = static_cast<int64_t>(sms) * resident_blocks<IN_BF16, G>();
+    const int64_t want = (per_slice + 256LL * G - 1) / (256LL * G);
+    const int gx = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, std::max<int64_t>(1, resident / slices))));
+    shard_reduce_kernel<IN_BF16, G><<<dim3(gx, slices, 1), 256, 0, stream>>>(a);
 }
 
 tp_status launch_shard_reduce(const ReduceDesc& d, cudaStream_t stream) {
@@ -221,21 +238,16 @@ tp_status launch_shard_reduce(const ReduceDesc& d, cudaStream_t stream) {
     a.hop_bf16 = d.hop_bf16;
     a.out_bf16 = d.out_bf16;
     a.replicate = d.replicate;
-    const int vec = d.in_bf16 ? 8 : 4;
-    // groups in flight per thread: about 8 loads of 16 bytes whatever t is
-    const int G = d.t <= 2 ? 4 : (d.t <= 4 ? 2 : 1);
-    const int64_t groups = std::max<int64_t>(d.count / vec, d.count % vec);
-    const int sms = std::max(1, sm_count_cached());
-    const int64_t want = (groups + 256 * G - 1) / (256 * G);
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
+    const bool ring = d.ring != 0;
+    // vectors in flight per thread: about 8 loads of 16 bytes whatever t is
     if (d.in_bf16) {
-        if (G == 4) shard_reduce_kernel<true, 4><<<grid, 256, 0, stream>>>(a);
-        else if (G == 2) shard_reduce_kernel<true, 2><<<grid, 256, 0, stream>>>(a);
-        else shard_reduce_kernel<true, 1><<<grid, 256, 0, stream>>>(a);
+        if (d.t <= 2) launch_reduce_cfg<true, 4>(a, d.count, d.t, ring, stream);
+        else if (d.t <= 4) launch_reduce_cfg<true, 2>(a, d.count, d.t, ring, stream);
+        else launch_reduce_cfg<true, 1>(a, d.count, d.t, ring, stream);
     } else {
-        if (G == 4) shard_reduce_kernel<false, 4><<<grid, 256, 0, stream>>>(a);
-        else if (G == 2) shard_reduce_kernel<false, 2><<<grid, 256, 0, stream>>>(a);
-        else shard_reduce_kernel<false, 1><<<grid, 256, 0, stream>>>(a);
+        if (d.t <= 2) launch_reduce_cfg<false, 4>(a, d.count, d.t, ring, stream);
+        else if (d.t <= 4) launch_reduce_cfg<false, 2>(a, d.count, d.t, ring, stream);
+        else launch_reduce_cfg<false, 1>(a, d.count, d.t, ring, stream);
     }
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
