@@ -201,6 +201,35 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f,
                          void* y, tp_dtype y_dtype, tp_stream stream);
 
 /*
+ * tp_mlp_forward for activations in host memory, with the copies overlapped
+ * with the compute (page "6.2 Tensor-parallel inference", §1: every token's
+ * output depends on its own row of X only, so the tokens can be processed
+ * in row blocks).
+ *
+ *   x_host   [n, h] bf16, contiguous, page-locked host memory (read).
+ *   y_host   [n, h] of y_dtype, contiguous, page-locked host memory (written).
+ *   x_dev    device staging for X, [n, h] bf16; y_dev device [n, h] y_dtype.
+ *   workspace  at least tp_mlp_workspace_size(t, ceil(n/chunks), h, f, mode,
+ *              partial_dtype) bytes (one row block), 256-byte aligned.
+ *   chunks   number of row blocks (1..64).  Block i's host->device copy runs
+ *            on copy_stream under the compute of block i-1, its device->host
+ *            copy under the compute of block i+1; the MLPs run on `stream`.
+ *   Other arguments as tp_mlp_forward.  When the call returns, all work is
+ *   queued and `stream` completes after the last read-back (wait on it).
+ * Errors as tp_mlp_forward; TP_ERR_WORKSPACE if the workspace is too small
+ * for one block.
+ */
+tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
+                              const void* x_host,
+                              const void* const* w_gate_up,
+                              const void* const* w_down, int64_t ld_down,
+                              const void* bias_down, tp_act act,
+                              tp_reduce_mode mode, tp_dtype partial_dtype,
+                              void* x_dev, void* workspace, size_t workspace_bytes,
+                              void* y_dev, void* y_host, tp_dtype y_dtype,
+                              int chunks, tp_stream stream, tp_stream copy_stream);
+
+/*
  * tp_mlp_forward for callers that cannot allocate device memory.  This entry
  * point has no counterpart in the pages this library follows; it exists for
  * deployment reasons.

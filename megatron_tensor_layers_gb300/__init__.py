@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     tp_linear_col,
     tp_linear_row,
     tp_mlp_forward,
+    tp_mlp_forward_host,
     tp_mlp_workspace_size,
     tp_reset_collective_count,
     tp_set_gemm_cta_pair,

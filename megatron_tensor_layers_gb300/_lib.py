@@ -32,7 +32,7 @@ EXPORTED = [
     "tp_status_string", "tp_abi_version", "tp_linear_col", "tp_linear_row", "tp_shard_reduce",
     "tp_mlp_workspace_size", "tp_mlp_forward", "vocab_parallel_embed", "lm_head_sharded",
     "tp_shard_gather", "tp_device_status", "tp_collective_count", "tp_reset_collective_count",
-    "tp_debug_expire_wait", "tp_set_gemm_tile_n", "tp_mlp_forward_static", "tp_set_gemm_cta_pair",
+    "tp_debug_expire_wait", "tp_set_gemm_tile_n", "tp_mlp_forward_static", "tp_set_gemm_cta_pair", "tp_mlp_forward_host",
 ]
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
         "tp_debug_expire_wait": (I32, [ctypes.c_uint64, P]),
         "tp_set_gemm_tile_n": (I32, [I32]),
         "tp_set_gemm_cta_pair": (I32, [I32]),
+        "tp_mlp_forward_host": (I32, [I32, I64, I64, I64, P, P, P, I64, P, I32, I32, I32, P, P, ctypes.c_size_t, P, P,
+                                      I32, I32, P, P]),
         "tp_mlp_forward_static": (I32, [I32, I64, I64, I64, P, I64, P, P, I64, P, I32, I32, I32, P, I32, P]),
     }
     for name, (res, args) in sig.items():
@@ -309,3 +311,24 @@ def tp_mlp_forward_static(x: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_
                                         _ptr(y), _dt(y.dtype), _stream(stream))
     _check("tp_mlp_forward_static", code)
     return y
+
+
+def tp_mlp_forward_host(x_host: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_down: Sequence[torch.Tensor], *,
+                        y_host: torch.Tensor, x_dev: torch.Tensor, y_dev: torch.Tensor, workspace: torch.Tensor,
+                        bias_down: Optional[torch.Tensor] = None, act: str = "silu", mode: str = "direct",
+                        partial_dtype=torch.bfloat16, chunks: int = 2, stream=None, copy_stream=None):
+    """tp_mlp_forward on pinned host activations with chunked, overlapped
+    copies (see include/tp.h).  Returns y_host; the work is complete when
+    `stream` is."""
+    assert x_host.is_pinned() and y_host.is_pinned(), "host buffers must be page-locked"
+    t = len(w_gate_up)
+    n, h = x_host.shape
+    f = w_gate_up[0].shape[0] // 2 * t
+    if copy_stream is None:
+        copy_stream = torch.cuda.Stream(device=x_dev.device)
+    code = load().tp_mlp_forward_host(t, n, h, f, _ptr(x_host), _ptrs(w_gate_up), _ptrs(w_down), _ld(w_down[0]),
+                                      _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype), _ptr(x_dev),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(y_dev),
+                                      _ptr(y_host), _dt(y_host.dtype), chunks, _stream(stream), _stream(copy_stream))
+    _check("tp_mlp_forward_host", code)
+    return y_host

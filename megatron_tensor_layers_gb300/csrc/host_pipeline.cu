@@ -1,0 +1,91 @@
+// tp_mlp_forward_host: the tensor-parallel MLP for activations that live in
+// (pinned) host memory, with the copies overlapped with the compute.
+//
+// The n tokens are cut into `chunks` row blocks.  Block i is copied to the
+// device on `copy_stream`, the MLP of block i runs on `stream` once its copy
+// has landed (an event), and its output is copied back on `copy_stream` once
+// the MLP is done (another event).  All input copies are queued first in
+// order, so the copy of block i+1 runs under the compute of block i and the
+// read-back of block i under the compute of block i+1; only the first input
+// copy and the last read-back are exposed.  Rows are independent in every
+// step of the MLP (page "6.2 Tensor-parallel inference", §1: each token's
+// output depends on its own row of X only), so splitting by rows changes no
+// result.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "tp.h"
+
+extern "C" tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f, const void* x_host,
+                                         const void* const* w_gate_up, const void* const* w_down, int64_t ld_down,
+                                         const void* bias_down, tp_act act, tp_reduce_mode mode,
+                                         tp_dtype partial_dtype, void* x_dev, void* workspace,
+                                         size_t workspace_bytes, void* y_dev, void* y_host, tp_dtype y_dtype,
+                                         int chunks, tp_stream stream, tp_stream copy_stream) {
+    if (x_host == nullptr || y_host == nullptr || x_dev == nullptr || y_dev == nullptr) return TP_ERR_INVALID_ARG;
+    if (chunks < 1 || chunks > 64 || n < 0 || h <= 0) return TP_ERR_INVALID_ARG;
+    if (y_dtype != TP_BF16 && y_dtype != TP_F32) return TP_ERR_UNSUPPORTED;
+    if (n == 0) return TP_OK;
+    const int64_t rows = (n + chunks - 1) / chunks;          // rows per block (the last may be shorter)
+    const int nblk = static_cast<int>((n + rows - 1) / rows);
+    // The workspace must hold one block's MLP; validate the arguments with it
+    // before anything is queued.
+    const size_t need = tp_mlp_workspace_size(t, rows, h, f, mode, partial_dtype);
+    if (need == 0) return TP_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return TP_ERR_WORKSPACE;
+    const size_t xrow = static_cast<size_t>(h) * 2;
+    const size_t yrow = static_cast<size_t>(h) * (y_dtype == TP_F32 ? 4 : 2);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t cp = reinterpret_cast<cudaStream_t>(copy_stream);
+
+    cudaEvent_t in_ready[64], out_ready[64];
+    int created = 0;
+    tp_status st = TP_OK;
+    for (; created < nblk; ++created) {
+        if (cudaEventCreateWithFlags(&in_ready[created], cudaEventDisableTiming) != cudaSuccess) {
+            st = TP_ERR_CUDA;
+            break;
+        }
+        if (cudaEventCreateWithFlags(&out_ready[created], cudaEventDisableTiming) != cudaSuccess) {
+            cudaEventDestroy(in_ready[created]);
+            st = TP_ERR_CUDA;
+            break;
+        }
+    }
+    // every input copy first, in order, each followed by its event
+    for (int b = 0; b < nblk && st == TP_OK; ++b) {
+        const int64_t r0 = b * rows, nr = std::min(rows, n - r0);
+        if (cudaMemcpyAsync(static_cast<char*>(x_dev) + r0 * xrow, static_cast<const char*>(x_host) + r0 * xrow,
+                            nr * xrow, cudaMemcpyHostToDevice, cp) != cudaSuccess ||
+            cudaEventRecord(in_ready[b], cp) != cudaSuccess)
+            st = TP_ERR_CUDA;
+    }
+    // compute block b once its input is on the device; read it back once computed
+    for (int b = 0; b < nblk && st == TP_OK; ++b) {
+        const int64_t r0 = b * rows, nr = std::min(rows, n - r0);
+        if (cudaStreamWaitEvent(cs, in_ready[b], 0) != cudaSuccess) {
+            st = TP_ERR_CUDA;
+            break;
+        }
+        st = tp_mlp_forward(t, nr, h, f, static_cast<char*>(x_dev) + r0 * xrow, h, w_gate_up, w_down, ld_down,
+                            bias_down, act, mode, partial_dtype, workspace, workspace_bytes,
+                            static_cast<char*>(y_dev) + r0 * yrow, y_dtype, stream);
+        if (st != TP_OK) break;
+        if (cudaEventRecord(out_ready[b], cs) != cudaSuccess || cudaStreamWaitEvent(cp, out_ready[b], 0) != cudaSuccess ||
+            cudaMemcpyAsync(static_cast<char*>(y_host) + r0 * yrow, static_cast<char*>(y_dev) + r0 * yrow, nr * yrow,
+                            cudaMemcpyDeviceToHost, cp) != cudaSuccess)
+            st = TP_ERR_CUDA;
+    }
+    // the compute stream ends after the last read-back, so callers can wait on it alone
+    if (st == TP_OK && nblk > 0) {
+        if (cudaEventRecord(in_ready[0], cp) != cudaSuccess || cudaStreamWaitEvent(cs, in_ready[0], 0) != cudaSuccess)
+            st = TP_ERR_CUDA;
+    }
+    for (int b = 0; b < created; ++b) {   // released once their pending work completes
+        cudaEventDestroy(in_ready[b]);
+        cudaEventDestroy(out_ready[b]);
+    }
+    return st;
+}

@@ -99,3 +99,27 @@ def test_reduce_embed_head_gather_reject_on_host(lib):
     assert lib.lm_head_sharded(2, 4, 16, 10, FAKE, 16, two, None, 0, None, 0, None) == 1
     cols = (ctypes.c_int64 * 2)(3, -1)
     assert lib.tp_shard_gather(2, 4, cols, 0, two, FAKE, None) == 1
+
+
+def test_tuning_knobs_through_the_binding(lib):
+    from megatron_tensor_layers_gb300 import TPError, tp_set_gemm_cta_pair, tp_set_gemm_tile_n
+    for mode in (1, -1, 0):
+        tp_set_gemm_cta_pair(mode)
+    for n in (64, 128, 256, 0):
+        tp_set_gemm_tile_n(n)
+    with pytest.raises(TPError):
+        tp_set_gemm_cta_pair(2)
+    with pytest.raises(TPError):
+        tp_set_gemm_tile_n(96)
+
+
+def test_host_pipeline_rejects_on_host(lib):
+    two = _arr(2)
+    # missing host buffers, bad chunk counts
+    assert lib.tp_mlp_forward_host(2, 8, 64, 128, None, two, two, 64, None, 1, 0, 0, FAKE, FAKE, 1 << 20, FAKE,
+                                   FAKE, 0, 1, None, None) == 1
+    assert lib.tp_mlp_forward_host(2, 8, 64, 128, FAKE, two, two, 64, None, 1, 0, 0, FAKE, FAKE, 1 << 20, FAKE,
+                                   FAKE, 0, 0, None, None) == 1
+    # a workspace smaller than one row block
+    assert lib.tp_mlp_forward_host(2, 8, 64, 128, FAKE, two, two, 64, None, 1, 0, 0, FAKE, FAKE, 16, FAKE,
+                                   FAKE, 0, 2, None, None) == 7

@@ -538,3 +538,26 @@ def test_pair_kernel_mlp(pair_on, mode):
     xf, wgf, wuf, wdf = f64(x), f64(wg), f64(wu), f64(wd)
     ref = O.mlp_unsharded(xf, wgf, wuf, wdf, None, "silu")
     gemm_gate(f64(y), ref, bf16_out=False, extra=_mlp_rounding_allowance(xf, wgf, wuf, wdf, t, "silu", False))
+
+
+@pytest.mark.parametrize("chunks", [1, 3, 4])
+def test_mlp_forward_host_matches_device_entry_point(chunks):
+    t, n, h, f = 2, 1000, 1024, 3072
+    fs = f // t
+    x = normal((n, h), 1.0, 240)
+    wg, wu, wd = normal((f, h), 0.02, 241), normal((f, h), 0.02, 242), normal((h, f), 0.02, 243)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds = [wd[:, r * fs:(r + 1) * fs] for r in range(t)]
+    y_ref = tp.tp_mlp_forward(x, wgu, wds, mode="direct", partial_dtype=torch.float32, y_dtype=torch.float32)
+    xh = torch.empty((n, h), dtype=torch.bfloat16, pin_memory=True)
+    xh.copy_(x)
+    yh = torch.full((n, h), float("nan"), dtype=torch.float32, pin_memory=True)
+    rows = (n + chunks - 1) // chunks
+    ws = torch.empty(tp.tp_mlp_workspace_size(t, rows, h, f, "direct", torch.float32), dtype=torch.uint8, device=DEV)
+    xd = torch.empty_like(x)
+    yd = torch.empty((n, h), dtype=torch.float32, device=DEV)
+    tp.tp_mlp_forward_host(xh, wgu, wds, y_host=yh, x_dev=xd, y_dev=yd, workspace=ws, mode="direct",
+                           partial_dtype=torch.float32, chunks=chunks)
+    torch.cuda.current_stream().synchronize()
+    ref = f64(y_ref)
+    gemm_gate(O.f32_bits_to_f64(yh.view(torch.int32).numpy().view(np.uint32)), ref, bf16_out=False)
