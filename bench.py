@@ -133,6 +133,20 @@ def make_mlp(torch, synth, t, n, h, f, dev, seed=0):
     return x, wgu, wds
 
 
+def max_over_ranks(dist, seconds: float, device) -> float:
+    """The slowest rank's timed region (all ranks get the same value)."""
+    import torch
+    tt = torch.tensor([seconds], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Units processed by all ranks per second of the slowest rank (weak
+    scaling: every rank runs its own replica of the workload)."""
+    return units_per_rank * world / max_seconds
+
+
 def time_fn(torch, fn, iters, warm=2, stream=None):
     """Mean device time (s) of fn() over iters launches, CUDA events on the stream."""
     stream = stream or torch.cuda.current_stream()
@@ -211,11 +225,9 @@ def run_ours(args, rank, world, local_rank):
     row_t = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3 / args.steps
     red_t = sum(e[2].elapsed_time(e[3]) for e in evs) / 1e3 / args.steps
     if dist is not None:
-        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed = tt.item()
+        elapsed = max_over_ranks(dist, elapsed, dev)
     ms_per_step = elapsed / args.steps * 1e3
-    value = FLOPS * world * args.steps / elapsed / 1e12
+    value = whole_job_value(FLOPS * args.steps, world, elapsed) / 1e12
 
     col_flops = 4.0 * N_TOK * H * F
     red_bytes = (T + 1) * N_TOK * H * 2
