@@ -39,12 +39,13 @@ __global__ void __launch_bounds__(256) vocab_embed_kernel(const __grid_constant_
     const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t nvec = a.h / VEC;
     for (int64_t tok = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; tok < a.n; tok += warps) {
-        const int64_t id = a.ids[tok];
+        const int32_t id = a.ids[tok];
         int owner = -1;
         int64_t local = 0;
-        if (id >= 0 && id < a.vocab) {
-            owner = static_cast<int>(id / a.per);
-            local = id - static_cast<int64_t>(owner) * a.per;
+        if (id >= 0 && id < a.vocab) {     // 32-bit arithmetic: ids and vocab sizes are int32
+            const uint32_t u = static_cast<uint32_t>(id), per = static_cast<uint32_t>(a.per);
+            owner = static_cast<int>(u / per);
+            local = static_cast<int64_t>(u - static_cast<uint32_t>(owner) * per);
         }
         const uint4* src = owner >= 0 ? reinterpret_cast<const uint4*>(a.table[owner]) + local * nvec : nullptr;
         uint4* dst = reinterpret_cast<uint4*>(a.out) + tok * nvec;

@@ -40,6 +40,8 @@ __all__ = [
     "ring_allreduce", "ring_fold_order",
     "vocab_parallel_embedding", "lm_head_sharded", "lm_head_unsharded", "shard_gather",
     "allreduce_time",
+    "rmsnorm", "token_chunks", "ring_reduce_scatter", "reduce_scatter_fold_order",
+    "all_gather_rows", "sequence_parallel_residual_norm",
 ]
 
 
@@ -478,6 +480,114 @@ def shard_gather(parts: Sequence[np.ndarray]) -> np.ndarray:
     """All-gather of vocab-sharded logits: the t [n, cols_r] blocks
     concatenated along the last dimension in rank order."""
     return np.concatenate([np.asarray(p, np.float64) for p in parts], axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# Sequence parallelism: the all-reduce split into reduce-scatter + all-gather
+# around the per-token residual add and RMSNorm (page "Tensor parallelism from
+# scratch", exercise 1 and its reference answer; the pre-norm residual of
+# tp.py TPTransformer: x = x + block(norm(x))).
+# ---------------------------------------------------------------------------
+
+def rmsnorm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm over the last dimension: x / sqrt(mean(x^2) + eps) * weight.
+
+    The pages name RMSNorm (tp.py imports it; "6.2 Tensor-parallel
+    inference", §6.2 table: not split, one copy per rank) without giving its
+    formula; this is the standard definition.
+    """
+    x = np.asarray(x, np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(weight, np.float64)
+
+
+def token_chunks(n: int, t: int) -> List[Tuple[int, int]]:
+    """Token rows owned by each rank after the reduce-scatter: rank r gets
+    rows [r*ceil(n/t), min((r+1)*ceil(n/t), n)) ("each card gets the full
+    result of 1/tp of the tokens")."""
+    per = (n + t - 1) // t if t > 0 else 0
+    return [(min(r * per, n), min((r + 1) * per, n)) for r in range(t)]
+
+
+def reduce_scatter_fold_order(n: int, c: int) -> List[int]:
+    """Order in which the reduce-scatter ring of :func:`ring_reduce_scatter`
+    adds the ranks' copies of chunk c: c+1, c+2, ..., c+N (mod N), so that
+    the finished chunk lands on rank c."""
+    return [(c + 1 + j) % n for j in range(n)]
+
+
+def ring_reduce_scatter(partials: Sequence[np.ndarray], chunks: Sequence[Tuple[int, int]] | None = None,
+                        hop: str = "f64") -> Tuple[List[np.ndarray], Dict[str, object]]:
+    """Reduce-scatter on a ring by message passing (vLLM source analysis 13,
+    §1.1.1): N-1 steps; at each step every rank sends one chunk to its right
+    neighbour, which adds it into its own copy (rounded as ``_hop_add``).
+
+    Which chunk a rank sends first is not fixed by the page (its figures are
+    missing).  For a reduce-scatter whose rank r must end holding chunk r
+    (the token rows it owns in sequence parallelism), rank r sends chunk
+    (r - s - 1) mod N at step s.  ``chunks`` are (lo, hi) ranges of the
+    flattened buffer (default: :func:`ring_chunks`).
+
+    Returns the N buffers after the last step (rank r's chunk r is final; its
+    other chunks hold partial sums) and counters.
+    """
+    n = len(partials)
+    shape = np.asarray(partials[0]).shape
+    bufs = [np.asarray(p, np.float64).reshape(-1).copy() for p in partials]
+    if hop == "f32":
+        bufs = [b.astype(np.float32).astype(np.float64) for b in bufs]
+    if chunks is None:
+        chunks = ring_chunks(bufs[0].size, n)
+    sent = [0] * n
+    for s in range(n - 1):
+        msgs = []
+        for r in range(n):
+            c = (r - s - 1) % n
+            lo, hi = chunks[c]
+            msgs.append(((r + 1) % n, c, bufs[r][lo:hi].copy()))
+            sent[r] += hi - lo
+        for dst, c, data in msgs:
+            lo, hi = chunks[c]
+            bufs[dst][lo:hi] = _hop_add(bufs[dst][lo:hi], data, hop)
+    return [b.reshape(shape) for b in bufs], {"steps": n - 1, "sent_per_rank": sent, "chunks": list(chunks)}
+
+
+def all_gather_rows(pieces: Sequence[np.ndarray]) -> np.ndarray:
+    """All-gather along the token dimension: the ranks' row blocks stacked in
+    rank order."""
+    return np.concatenate([np.asarray(p, np.float64) for p in pieces], axis=0)
+
+
+def sequence_parallel_residual_norm(partials: Sequence[np.ndarray], residual: np.ndarray | None,
+                                    weight: np.ndarray, eps: float, order: str = "direct"):
+    """The sequence-parallel replacement of "all-reduce, then residual add and
+    RMSNorm on every token on every rank": reduce-scatter the [n, h]
+    partials over token rows, add the residual and apply RMSNorm on each
+    rank's own rows only, all-gather the rows.
+
+    order "direct": each rank sums its rows of the t partials in rank order;
+    "ring": the reduce-scatter ring above (fp64 adds, so only the order of the
+    fold differs).  Returns (new residual [n, h], normed [n, h], per-rank
+    (residual, normed) row blocks).
+    """
+    t = len(partials)
+    p64 = [np.asarray(p, np.float64) for p in partials]
+    n, h = p64[0].shape
+    rows = token_chunks(n, t)
+    if order == "ring":
+        chunks = [(lo * h, hi * h) for lo, hi in rows]
+        bufs, _ = ring_reduce_scatter(p64, chunks=chunks, hop="f64")
+        owned = [bufs[r][lo:hi] for r, (lo, hi) in enumerate(rows)]
+    elif order == "direct":
+        owned = [reduce_direct([p[lo:hi] for p in p64]) for lo, hi in rows]
+    else:
+        raise ValueError(order)
+    res_blocks, norm_blocks = [], []
+    for r, (lo, hi) in enumerate(rows):
+        x = owned[r] if residual is None else np.asarray(residual, np.float64)[lo:hi] + owned[r]
+        res_blocks.append(x)
+        norm_blocks.append(rmsnorm(x, weight, eps))
+    return all_gather_rows(res_blocks), all_gather_rows(norm_blocks), list(zip(res_blocks, norm_blocks))
 
 
 # ---------------------------------------------------------------------------

@@ -390,3 +390,73 @@ def test_allreduce_cost_table(golden_dir):
         us = O.allreduce_time(row["bytes"], g["t"], g["bandwidth_bytes_per_s"]) * 1e6
         assert abs(us - row["approx_us"]) <= row["rel_tol"] * row["approx_us"] + 0.005
         assert row["bytes"] == row["tokens"] * 8192 * 2
+
+
+# ------------------------------------------------------- sequence parallelism
+
+def test_rmsnorm_matches_library_and_closed_forms():
+    rng = np.random.default_rng(60)
+    x = rng.standard_normal((7, 33)) * 3
+    w = rng.standard_normal(33)
+    for eps in (0.0, 1e-6, 1e-2):
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (33,), torch.from_numpy(w), eps=eps).numpy()
+        assert np.allclose(O.rmsnorm(x, w, eps), ref, rtol=1e-13, atol=1e-13)
+    # a constant row c normalises to sign(c) * weight (eps = 0)
+    c = np.full((2, 5), -2.5)
+    assert np.allclose(O.rmsnorm(c, np.arange(1.0, 6.0), 0.0), -np.arange(1.0, 6.0)[None, :].repeat(2, 0))
+    # scale invariance for eps = 0
+    assert np.allclose(O.rmsnorm(7.0 * x, w, 0.0), O.rmsnorm(x, w, 0.0), rtol=1e-13)
+
+
+def test_reduce_scatter_ownership_and_volume(golden_dir):
+    g = _golden(golden_dir, "tpscratch_sequence_parallel.json")
+    for case in g["cases"]:
+        n, k = case["n"], case["k"]
+        rng = np.random.default_rng(n * k)
+        parts = [rng.integers(-20, 20, k).astype(np.float64) for _ in range(n)]
+        total = sum(parts)
+        bufs, st = O.ring_reduce_scatter(parts)
+        assert st["steps"] == n - 1
+        assert st["sent_per_rank"] == [case["rs_per_rank"]] * n
+        for r, (lo, hi) in enumerate(st["chunks"]):
+            assert np.array_equal(bufs[r][lo:hi], total[lo:hi])          # rank r owns chunk r
+        _, ar = O.ring_allreduce(parts)
+        assert ar["sent_per_rank"] == [case["ar_per_rank"]] * n
+        ag = [a - b for a, b in zip(ar["sent_per_rank"], st["sent_per_rank"])]
+        assert ag == [case["ag_per_rank"]] * n                            # RS + AG = AR, equal halves
+        # all-gather of the owned chunks gives every rank the all-reduce result
+        gathered = np.concatenate([bufs[r][lo:hi] for r, (lo, hi) in enumerate(st["chunks"])])
+        assert np.array_equal(gathered, total)
+
+
+def test_reduce_scatter_fold_order_visible_in_bf16():
+    # chunk c is folded c+1, c+2, ..., c (mod 3): put 1.0 on rank c (the last
+    # one to add) and 2^-8 elsewhere, so every chunk gives 1 + 2^-7 exactly.
+    a, e = 1.0, 2.0 ** -8
+    p = [np.array([a, e, e]), np.array([e, a, e]), np.array([e, e, a])]
+    bufs, _ = O.ring_reduce_scatter(p, hop="bf16")
+    for r in range(3):
+        assert bufs[r][r] == 1.0 + 2 ** -7
+    assert O.reduce_scatter_fold_order(3, 0) == [1, 2, 0]
+    assert O.reduce_scatter_fold_order(4, 3) == [0, 1, 2, 3]
+    # the all-reduce convention (chunk c starts at rank c) gives 1 for these inputs
+    ar, _ = O.ring_allreduce(p, hop="bf16")
+    assert ar[0].tolist() == [1.0, 1.0, 1.0]
+
+
+@pytest.mark.parametrize("t,n", [(1, 5), (2, 8), (3, 10), (4, 9), (8, 3)])
+def test_sequence_parallel_equals_allreduce_then_norm(t, n):
+    rng = np.random.default_rng(70 + t)
+    h = 12
+    parts = [rng.standard_normal((n, h)) for _ in range(t)]
+    resid = rng.standard_normal((n, h))
+    w = rng.standard_normal(h)
+    full = resid + O.reduce_direct(parts)
+    for order in ("direct", "ring"):
+        res, normed, blocks = O.sequence_parallel_residual_norm(parts, resid, w, 1e-6, order)
+        assert np.allclose(res, full, rtol=1e-13, atol=1e-13)
+        assert np.allclose(normed, O.rmsnorm(full, w, 1e-6), rtol=1e-12, atol=1e-12)
+        assert sum(b[0].shape[0] for b in blocks) == n
+        assert [b[0].shape[0] for b in blocks] == [hi - lo for lo, hi in O.token_chunks(n, t)]
+    res0, _, _ = O.sequence_parallel_residual_norm(parts, None, w, 1e-6)
+    assert np.allclose(res0, O.reduce_direct(parts))
