@@ -359,6 +359,19 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
                         "us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm}
             del base
     out["shard_reduce_sweep"] = sweep
+    # sequence parallelism: reduce-scatter + residual + RMSNorm (all-gather in place), t=4, bf16
+    parts4 = [torch.randn((N_TOK, H), device=dev).to(torch.bfloat16) for _ in range(4)]
+    resid = torch.randn((N_TOK, H), device=dev).to(torch.bfloat16)
+    wn = torch.randn((H,), device=dev).to(torch.bfloat16)
+    res_out = torch.empty_like(resid)
+    nrm = torch.empty_like(resid)
+    for mode in ("direct", "ring"):
+        s = time_fn(torch, lambda: tp.tp_reduce_scatter_rmsnorm(parts4, wn, residual=resid, mode=mode,
+                                                                residual_out=res_out, out=nrm), 20)
+        byts = (4 + 1 + 2) * N_TOK * H * 2
+        out[f"rs_rmsnorm_t4_n{N_TOK}_{mode}"] = {"us": s * 1e6, "GBps": byts / s / 1e9,
+                                                 "hbm_frac": byts / s / 1e9 / hbm}
+    del parts4, resid, res_out, nrm
     # vocab-parallel embedding + LM head, V=151936, h=1024, 4096 ids
     V, hh, nt = 151936, 1024, 4096
     table = synth.normal_bf16((V, hh), 0.02, 6, device=dev)

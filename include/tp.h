@@ -313,6 +313,35 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab,
                           tp_dtype out_dtype, tp_stream stream);
 
 /*
+ * Sequence parallelism: the all-reduce after a row-parallel layer split into
+ * a reduce-scatter over token rows and an all-gather, with the residual add
+ * and RMSNorm done between them on each rank's own rows (page "Tensor
+ * parallelism from scratch", exercise 1: the total communication is
+ * unchanged, the per-token work drops to 1/t per rank; the pre-norm residual
+ * x = x + block(norm(x)) of its tp.py).  RMSNorm is
+ * x / sqrt(mean(x^2) + eps) * weight (the pages name it without a formula).
+ *
+ *   partials[r]  [n, h] of dtype (bf16 or f32), contiguous: the row-parallel
+ *                partial sums.
+ *   residual     NULL or [n, h] bf16: the residual stream.
+ *   weight       [h] bf16: the RMSNorm weight (one copy on every rank).
+ *   mode         TP_REDUCE_DIRECT: a rank sums its rows of the t partials in
+ *                rank order; TP_REDUCE_RING: in the order of a reduce-scatter
+ *                ring that leaves chunk r on rank r (r+1, r+2, ..., r mod t).
+ *                fp32 carry in both.
+ *   residual_out NULL or [n, h] bf16: residual + sum, rounded once; may be
+ *                the same buffer as residual.
+ *   out          [n, h] bf16: RMSNorm of the fp32 residual + sum.
+ * Rank r owns rows [r*ceil(n/t), min((r+1)*ceil(n/t), n)); every rank's rows
+ * are written in place, so the all-gather back to all tokens costs nothing.
+ * Requires h % 8 == 0 (TP_ERR_ALIGNMENT) and h <= 32768 (TP_ERR_UNSUPPORTED).
+ */
+tp_status tp_reduce_scatter_rmsnorm(int t, int64_t n, int64_t h, tp_dtype dtype,
+                                    const void* const* partials, const void* residual,
+                                    const void* weight, float eps, tp_reduce_mode mode,
+                                    void* residual_out, void* out, tp_stream stream);
+
+/*
  * All-gather of vocab-sharded outputs: shard r is [rows, cols[r]]
  * (contiguous) and lands in columns [sum(cols[:r]), sum(cols[:r+1])) of
  * out [rows, sum(cols)] (contiguous).  `cols` is a host array of t widths.

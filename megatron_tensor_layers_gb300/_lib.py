@@ -33,6 +33,7 @@ EXPORTED = [
     "tp_mlp_workspace_size", "tp_mlp_forward", "vocab_parallel_embed", "lm_head_sharded",
     "tp_shard_gather", "tp_device_status", "tp_collective_count", "tp_reset_collective_count",
     "tp_debug_expire_wait", "tp_set_gemm_tile_n", "tp_mlp_forward_static", "tp_set_gemm_cta_pair", "tp_mlp_forward_host",
+    "tp_reduce_scatter_rmsnorm",
 ]
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -74,6 +75,7 @@ def load() -> ctypes.CDLL:
         "tp_debug_expire_wait": (I32, [ctypes.c_uint64, P]),
         "tp_set_gemm_tile_n": (I32, [I32]),
         "tp_set_gemm_cta_pair": (I32, [I32]),
+        "tp_reduce_scatter_rmsnorm": (I32, [I32, I64, I64, I32, P, P, P, ctypes.c_float, I32, P, P, P]),
         "tp_mlp_forward_host": (I32, [I32, I64, I64, I64, P, P, P, I64, P, I32, I32, I32, P, P, ctypes.c_size_t, P, P,
                                       I32, I32, P, P]),
         "tp_mlp_forward_static": (I32, [I32, I64, I64, I64, P, I64, P, P, I64, P, I32, I32, I32, P, I32, P]),
@@ -332,3 +334,20 @@ def tp_mlp_forward_host(x_host: torch.Tensor, w_gate_up: Sequence[torch.Tensor],
                                       _ptr(y_host), _dt(y_host.dtype), chunks, _stream(stream), _stream(copy_stream))
     _check("tp_mlp_forward_host", code)
     return y_host
+
+
+def tp_reduce_scatter_rmsnorm(partials: Sequence[torch.Tensor], weight: torch.Tensor, *,
+                              residual: Optional[torch.Tensor] = None, eps: float = 1e-6, mode: str = "direct",
+                              residual_out: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                              stream=None):
+    """Sequence-parallel reduce-scatter + residual add + RMSNorm (all-gather
+    in place).  Returns (residual_out or None, out)."""
+    t = len(partials)
+    n, h = partials[0].shape
+    if out is None:
+        out = torch.empty((n, h), dtype=torch.bfloat16, device=partials[0].device)
+    code = load().tp_reduce_scatter_rmsnorm(t, n, h, _dt(partials[0].dtype), _ptrs(partials), _ptr(residual),
+                                            _ptr(weight), eps, MODES[mode], _ptr(residual_out), _ptr(out),
+                                            _stream(stream))
+    _check("tp_reduce_scatter_rmsnorm", code)
+    return residual_out, out

@@ -423,6 +423,40 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab, const void
     return tpk::launch_gemm(d, cs(stream));
 }
 
+tp_status tp_reduce_scatter_rmsnorm(int t, int64_t n, int64_t h, tp_dtype dtype, const void* const* partials,
+                                    const void* residual, const void* weight, float eps, tp_reduce_mode mode,
+                                    void* residual_out, void* out, tp_stream stream) {
+    TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
+    TP_CHECK(n >= 0 && h > 0 && partials != nullptr && weight != nullptr && out != nullptr, TP_ERR_INVALID_ARG);
+    TP_CHECK(mode == TP_REDUCE_DIRECT || mode == TP_REDUCE_RING, TP_ERR_INVALID_ARG);
+    TP_CHECK(eps >= 0.0f, TP_ERR_INVALID_ARG);
+    TP_CHECK(dtype_ok(dtype), TP_ERR_UNSUPPORTED);
+    TP_CHECK(h % 8 == 0, TP_ERR_ALIGNMENT);
+    TP_CHECK(h <= 32768, TP_ERR_UNSUPPORTED);
+    TP_CHECK(al16(weight) && al16(out) && (residual == nullptr || al16(residual)) &&
+                 (residual_out == nullptr || al16(residual_out)),
+             TP_ERR_ALIGNMENT);
+    for (int r = 0; r < t; ++r) {
+        TP_CHECK(partials[r] != nullptr, TP_ERR_INVALID_ARG);
+        TP_CHECK(al16(partials[r]), TP_ERR_ALIGNMENT);
+    }
+    if (n == 0) return TP_OK;
+    tpk::SeqParDesc d;
+    d.t = t;
+    d.n = n;
+    d.h = h;
+    d.in_bf16 = dtype == TP_BF16;
+    for (int r = 0; r < t; ++r) d.p[r] = partials[r];
+    d.residual = residual;
+    d.weight = weight;
+    d.residual_out = residual_out;
+    d.out = out;
+    d.eps = eps;
+    d.ring = mode == TP_REDUCE_RING;
+    g_collectives++;
+    return tpk::launch_seqpar_rmsnorm(d, cs(stream));
+}
+
 tp_status tp_shard_gather(int t, int64_t rows, const int64_t* cols, tp_dtype dtype, const void* const* shards,
                           void* out, tp_stream stream) {
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);

@@ -74,6 +74,21 @@ struct GatherDesc {
 };
 tp_status launch_shard_gather(const GatherDesc& d, cudaStream_t stream);
 
+// Reduce-scatter over token rows + residual add + RMSNorm (sequence parallelism).
+struct SeqParDesc {
+    int t = 0;
+    int64_t n = 0, h = 0;
+    int in_bf16 = 1;
+    const void* p[TP_MAX_SHARDS] = {};
+    const void* residual = nullptr;
+    const void* weight = nullptr;
+    void* residual_out = nullptr;
+    void* out = nullptr;
+    float eps = 1e-6f;
+    int ring = 0;
+};
+tp_status launch_seqpar_rmsnorm(const SeqParDesc& d, cudaStream_t stream);
+
 tp_status launch_expire_wait(uint64_t limit_ns, int* status, cudaStream_t stream);
 
 }  // namespace tpk

@@ -152,3 +152,26 @@ def test_lm_head_config_sampled_rows(t):
     rows = [0, 127, 128, n - 1] + list(np.random.default_rng(5).choice(n, 12, replace=False))
     ref, _ = O.lm_head_sharded(f64(x[rows]), f64(table), t)
     gemm_gate(f64(logits[rows]), ref, bf16_out=True)
+
+
+@pytest.mark.parametrize("order", ["direct", "ring"])
+def test_reduce_scatter_rmsnorm_bench_size(order):
+    t, n, h = 4, 8192, 8192
+    parts = [synth.normal_bf16((n, h), 1.0, 800 + r, device=DEV) for r in range(t)]
+    resid = synth.normal_bf16((n, h), 1.0, 810, device=DEV)
+    w = synth.normal_bf16((h,), 1.0, 811, device=DEV)
+    res_out = torch.empty_like(resid)
+    _, out = tp.tp_reduce_scatter_rmsnorm(parts, w, residual=resid, mode=order, residual_out=res_out)
+    torch.cuda.synchronize()
+    rows = [0, 2047, 2048, 4095, 4096, 6143, 6144, n - 1]          # both sides of every rank's boundary
+    pf = [f64(p[rows]) for p in parts]
+    full_rows = np.array(rows)
+    owners = full_rows // ((n + t - 1) // t)
+    x = np.zeros((len(rows), h))
+    for i, r in enumerate(owners):
+        seq = list(range(t)) if order == "direct" else O.reduce_scatter_fold_order(t, int(r))
+        x[i] = sum(pf[j][i] for j in seq)
+    xr = f64(resid[rows]) + x
+    normed = O.rmsnorm(xr, f64(w), 1e-6)
+    assert np.all(np.abs(f64(out[rows]) - normed) <= half_ulp_bf16(normed) + 1e-4 * np.abs(normed) + 1e-6)
+    assert np.all(np.abs(f64(res_out[rows]) - xr) <= half_ulp_bf16(xr) + 1e-5 * np.abs(xr))

@@ -561,3 +561,54 @@ def test_mlp_forward_host_matches_device_entry_point(chunks):
     torch.cuda.current_stream().synchronize()
     ref = f64(y_ref)
     gemm_gate(O.f32_bits_to_f64(yh.view(torch.int32).numpy().view(np.uint32)), ref, bf16_out=False)
+
+
+# ------------------------------------------- sequence parallelism (RS + norm)
+
+def _rs_fold_f32(pf, t, n, order):
+    """fp32 fold of each row's partials in its owner's reduce-scatter order."""
+    out = np.empty_like(pf[0])
+    for r, (lo, hi) in enumerate(O.token_chunks(n, t)):
+        seq = list(range(t)) if order == "direct" else O.reduce_scatter_fold_order(t, r)
+        acc = pf[seq[0]][lo:hi].astype(np.float32)
+        for j in seq[1:]:
+            acc = (acc + pf[j][lo:hi].astype(np.float32)).astype(np.float32)
+        out[lo:hi] = acc
+    return out
+
+
+@pytest.mark.parametrize("t,n,h", [(1, 5, 64), (2, 9, 1000), (3, 10, 256), (4, 37, 8192), (8, 20, 512)])
+@pytest.mark.parametrize("order", ["direct", "ring"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_reduce_scatter_rmsnorm(t, n, h, order, dtype):
+    parts = [(synth.normal_f32((n, h), 1.0, 500 + r, device=DEV)).to(dtype) for r in range(t)]
+    resid = normal((n, h), 1.0, 520)
+    w = normal((h,), 1.0, 521)
+    res_out = torch.empty((n, h), dtype=torch.bfloat16, device=DEV)
+    _, out = tp.tp_reduce_scatter_rmsnorm(parts, w, residual=resid, eps=1e-6, mode=order, residual_out=res_out)
+    torch.cuda.synchronize()
+    pf = [f64(p) for p in parts]
+    # the new residual: bit-exact against the fp32 fold in the owner's order, + residual, rounded once
+    x32 = (_rs_fold_f32(pf, t, n, order).astype(np.float32) + f64(resid).astype(np.float32)).astype(np.float32)
+    exact(f64(res_out), O.round_to_bf16(x32.astype(np.float64)))
+    # the normed rows against the fp64 oracle
+    _, normed, _ = O.sequence_parallel_residual_norm(pf, f64(resid), f64(w), 1e-6, order)
+    got = f64(out)
+    bound = half_ulp_bf16(normed) + 1e-4 * np.abs(normed) + 1e-6
+    assert np.all(np.abs(got - normed) <= bound), float(np.max(np.abs(got - normed) - bound))
+
+
+def test_reduce_scatter_rmsnorm_in_place_and_no_residual():
+    t, n, h = 4, 16, 256
+    parts = [normal((n, h), 1.0, 530 + r) for r in range(t)]
+    resid = normal((n, h), 1.0, 540)
+    w = normal((h,), 1.0, 541)
+    r0 = resid.clone()
+    tp.tp_reduce_scatter_rmsnorm(parts, w, residual=resid, residual_out=resid)       # in place
+    _, out0 = tp.tp_reduce_scatter_rmsnorm(parts, w)                                # no residual stream
+    torch.cuda.synchronize()
+    pf = [f64(p) for p in parts]
+    x32 = (_rs_fold_f32(pf, t, n, "direct").astype(np.float32) + f64(r0).astype(np.float32)).astype(np.float32)
+    exact(f64(resid), O.round_to_bf16(x32.astype(np.float64)))
+    _, normed, _ = O.sequence_parallel_residual_norm(pf, None, f64(w), 1e-6)
+    assert np.all(np.abs(f64(out0) - normed) <= half_ulp_bf16(normed) + 1e-4 * np.abs(normed) + 1e-6)
