@@ -8,8 +8,9 @@
 // rank order).  Ranges are disjoint, so for every token at most one rank
 // holds a real row: the kernel reads that one row (one warp per token,
 // 16-byte loads) and forms the rank-order sum of it and t-1 exact zeros in
-// float32.  That sum is bit-exact to the lookup, except that -0.0 becomes
-// +0.0 when t > 1, which is what summing the ranks' outputs gives.
+// float32, which is x + 0.0 in closed form.  That sum is bit-exact to the
+// lookup, except that -0.0 becomes +0.0 when t > 1, which is what summing
+// the ranks' outputs gives.
 // Bytes moved per token: h*b read (owner row) + h*b written (+ t*h*b for the
 // optional per-rank outputs) + 4 for the id.
 #include <cuda_runtime.h>
@@ -75,14 +76,13 @@ __global__ void __launch_bounds__(256) vocab_embed_kernel(const __grid_constant_
 #pragma unroll
                     for (int i = 0; i < VEC; ++i) x[i] = __uint_as_float(w[i]);
                 }
-                // The all-reduce: rank 0's masked output, then ranks 1..t-1 added in order.
+                // The all-reduce: the rank-order sum of the t masked outputs.  At most one of them
+                // is non-zero, the rest are exact +0.0, so for t > 1 the sum is x + 0.0 in every
+                // order (x itself, except that -0.0 becomes +0.0; NaN and Inf pass), and for t = 1
+                // it is x.  __fadd_rn keeps the addition from being contracted or dropped.
                 float acc[VEC];
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) acc[i] = owner == 0 ? x[i] : 0.0f;
-                for (int r = 1; r < a.t; ++r) {
-#pragma unroll
-                    for (int i = 0; i < VEC; ++i) acc[i] = acc[i] + (owner == r ? x[i] : 0.0f);
-                }
+                for (int i = 0; i < VEC; ++i) acc[i] = a.t > 1 ? __fadd_rn(x[i], 0.0f) : x[i];
                 uint4 o;
                 if constexpr (BF16) {
                     o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),

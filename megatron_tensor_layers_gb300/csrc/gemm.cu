@@ -64,6 +64,7 @@ struct GemmArgs {
     int glu_up_row;                   // row offset of the up block inside B (gated epilogue)
     int group_m;                      // tile raster: bands of group_m row-tiles (about 32 MB of A rows)
     int a_box_rows;                   // rows of A a TMA box loads (<= 128; fewer when M is small)
+    int rotate_k;                     // start each tile's K loop at block (tile mod k_blocks)
     int act;                          // tp_act for the gated epilogue
     int* status;                      // library status word
 };
@@ -191,9 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
             for (int tile = blockIdx.x; tile < args.total_tiles && !aborted; tile += gridDim.x) {
                 int g, m, n;
                 tile_coords(args, tile, g, m, n);
+                // With a few rows of A every CTA would read the same line of A at the same k;
+                // starting each tile's K loop elsewhere spreads those reads over L2.
+                const int rot = args.rotate_k ? tile % args.k_blocks : 0;
                 for (int kk = 0; kk < kb_per_tile; ++kk) {
                     const int seg = kk / args.k_blocks;
-                    const int kb = kk - seg * args.k_blocks;
+                    int kb = kk - seg * args.k_blocks + rot;
+                    if (kb >= args.k_blocks) kb -= args.k_blocks;
                     const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
                     const int bi = args.segs > 1 ? seg : g;
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
@@ -624,6 +629,8 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
     // the rest of the 128-row shared tile is never read into an output row.
     a.a_box_rows = static_cast<int>(std::min<int64_t>(BM, (d.M + 7) / 8 * 8));
     a.group_m = raster_band(BM, d.K * d.segs);
+    // decode-sized A, and not the fused reduce (which must accumulate shards in rank order)
+    a.rotate_k = (d.M <= 64 && d.segs == 1) ? 1 : 0;
     for (int i = 0; i < nA; ++i)
         if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
     for (int i = 0; i < nB; ++i) {

@@ -612,3 +612,39 @@ def test_reduce_scatter_rmsnorm_in_place_and_no_residual():
     exact(f64(resid), O.round_to_bf16(x32.astype(np.float64)))
     _, normed, _ = O.sequence_parallel_residual_norm(pf, None, f64(w), 1e-6)
     assert np.all(np.abs(f64(out0) - normed) <= half_ulp_bf16(normed) + 1e-4 * np.abs(normed) + 1e-6)
+
+
+# ---------------------------------------------------- QKV column-parallel linear
+
+def test_qkv_worked_example_through_linear_col():
+    # Nano-vLLM walkthrough 22, section 5: q 4 heads, k/v 2 heads, head_size 2, t=2; every row of head
+    # h holds the head's constant.  Hidden is padded from 3 to 8 columns (the ABI's row pitch); x picks
+    # column 0, so output column j of rank r is the constant of the j-th row of rank r's merged block.
+    hs, hid, t = 2, 8, 2
+
+    def by_head(nheads, base):
+        return torch.tensor([[float(base + h)] * hid for h in range(nheads) for _ in range(hs)], dtype=torch.bfloat16)
+
+    q, k, v = by_head(4, 0), by_head(2, 10), by_head(2, 20)
+    blocks = [torch.from_numpy(O.qkv_shard(q.float().numpy(), k.float().numpy(), v.float().numpy(), 4, 2, hs, t, r))
+              .to(torch.bfloat16).to(DEV) for r in range(t)]
+    x = torch.zeros((1, hid), dtype=torch.bfloat16, device=DEV)
+    x[0, 0] = 1
+    y = tp.tp_linear_col(x, blocks, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert y[0][0].tolist() == [0.0, 0.0, 1.0, 1.0, 10.0, 10.0, 20.0, 20.0]
+    assert y[1][0].tolist() == [2.0, 2.0, 3.0, 3.0, 11.0, 11.0, 21.0, 21.0]
+
+
+@pytest.mark.parametrize("t,nh,nkv,hd", [(2, 16, 8, 64), (4, 32, 8, 128), (8, 64, 8, 128)])
+def test_qkv_merged_layout_integer_exact(t, nh, nkv, hd):
+    hid, n = 256, 70
+    wq, wk, wv = ints((nh * hd, hid), 300), ints((nkv * hd, hid), 301), ints((nkv * hd, hid), 302)
+    x = ints((n, hid), 303)
+    wqf, wkf, wvf = f64(wq), f64(wk), f64(wv)
+    blocks = [synth.from_bits_u16(O.bf16_from_f64_bits(O.qkv_shard(wqf, wkf, wvf, nh, nkv, hd, t, r)), device=DEV)
+              for r in range(t)]
+    y = tp.tp_linear_col(x, blocks, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for r in range(t):
+        exact(f64(y[r]), O.linear(f64(x), O.qkv_shard(wqf, wkf, wvf, nh, nkv, hd, t, r)))
