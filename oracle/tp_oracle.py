@@ -33,7 +33,7 @@ import numpy as np
 
 __all__ = [
     "bf16_bits_to_f64", "f32_bits_to_f64", "round_to_bf16", "bf16_from_f64_bits",
-    "divide", "column_shard", "row_shard", "merged_column_shard", "qkv_shard",
+    "divide", "column_shard", "row_shard", "merged_column_shard", "qkv_shard", "qkv_shard_gqa", "kv_head_of_rank",
     "vocab_range", "linear", "silu", "gelu_tanh", "glu",
     "mlp_unsharded", "mlp_shard_partials", "mlp_sharded",
     "reduce_direct", "reduce_direct_f32", "ring_chunks", "ring_schedule",
@@ -171,6 +171,37 @@ def qkv_shard(wq: np.ndarray, wk: np.ndarray, wv: np.ndarray, num_heads: int,
     q = wq[r * nh * head_size:(r + 1) * nh * head_size]
     k = wk[r * nkv * head_size:(r + 1) * nkv * head_size]
     v = wv[r * nkv * head_size:(r + 1) * nkv * head_size]
+    return np.concatenate([q, k, v], axis=0)
+
+
+def kv_head_of_rank(num_kv_heads: int, t: int, r: int) -> List[int]:
+    """KV heads held by rank r of a head-parallel GQA attention.
+
+    6.2 Tensor-parallel inference, §2.2: with t <= num_kv_heads every rank
+    holds num_kv_heads/t distinct KV heads; with t > num_kv_heads every rank
+    holds one KV head and each KV head is replicated on t/num_kv_heads ranks
+    (t must be divisible by num_kv_heads).  Which rank holds which head is
+    in a missing figure; reading taken: consecutive ranks share a head, rank
+    r holds head r // (t/num_kv_heads), which is the head its own query
+    heads use under GQA grouping (query head q uses KV head
+    q // (num_heads/num_kv_heads)).
+    """
+    if t <= num_kv_heads:
+        per = divide(num_kv_heads, t)
+        return list(range(r * per, (r + 1) * per))
+    return [r // divide(t, num_kv_heads)]
+
+
+def qkv_shard_gqa(wq: np.ndarray, wk: np.ndarray, wv: np.ndarray, num_heads: int, num_kv_heads: int,
+                  head_size: int, t: int, r: int) -> np.ndarray:
+    """Rank r's merged [q; k; v] block when the KV heads may be replicated
+    (see :func:`kv_head_of_rank`); equals :func:`qkv_shard` when t divides
+    the KV head count."""
+    nh = divide(num_heads, t)
+    q = wq[r * nh * head_size:(r + 1) * nh * head_size]
+    heads = kv_head_of_rank(num_kv_heads, t, r)
+    k = np.concatenate([wk[h * head_size:(h + 1) * head_size] for h in heads], axis=0)
+    v = np.concatenate([wv[h * head_size:(h + 1) * head_size] for h in heads], axis=0)
     return np.concatenate([q, k, v], axis=0)
 
 

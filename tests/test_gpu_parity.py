@@ -648,3 +648,18 @@ def test_qkv_merged_layout_integer_exact(t, nh, nkv, hd):
     torch.cuda.synchronize()
     for r in range(t):
         exact(f64(y[r]), O.linear(f64(x), O.qkv_shard(wqf, wkf, wvf, nh, nkv, hd, t, r)))
+
+
+@pytest.mark.parametrize("t,nh,nkv,hd", [(8, 64, 4, 64), (4, 32, 2, 64)])
+def test_qkv_gqa_replicated_layout_integer_exact(t, nh, nkv, hd):
+    # t > KV heads: each rank's block carries one replicated KV head (6.2 Tensor-parallel inference, §2.2)
+    hid, n = 128, 40
+    wq, wk, wv = ints((nh * hd, hid), 310), ints((nkv * hd, hid), 311), ints((nkv * hd, hid), 312)
+    x = ints((n, hid), 313)
+    wqf, wkf, wvf = f64(wq), f64(wk), f64(wv)
+    blocks = [synth.from_bits_u16(O.bf16_from_f64_bits(O.qkv_shard_gqa(wqf, wkf, wvf, nh, nkv, hd, t, r)), device=DEV)
+              for r in range(t)]
+    y = tp.tp_linear_col(x, blocks, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for r in range(t):
+        exact(f64(y[r]), O.linear(f64(x), O.qkv_shard_gqa(wqf, wkf, wvf, nh, nkv, hd, t, r)))

@@ -460,3 +460,46 @@ def test_sequence_parallel_equals_allreduce_then_norm(t, n):
         assert [b[0].shape[0] for b in blocks] == [hi - lo for lo, hi in O.token_chunks(n, t)]
     res0, _, _ = O.sequence_parallel_residual_norm(parts, None, w, 1e-6)
     assert np.allclose(res0, O.reduce_direct(parts))
+
+
+# ----------------------------------------------------- GQA KV-head replication
+
+def test_gqa_kv_replication_counts(golden_dir):
+    g = _golden(golden_dir, "aiinfra62_gqa_replication.json")
+    nh, nkv = g["num_heads"], g["num_kv_heads"]
+    for case in g["cases"]:
+        t = case["t"]
+        held = [O.kv_head_of_rank(nkv, t, r) for r in range(t)]
+        assert all(len(hs) == case["kv_heads_per_rank"] for hs in held)
+        copies = {h: sum(h in hs for hs in held) for h in range(nkv)}
+        assert set(copies.values()) == {case["copies_per_kv_head"]}
+        assert sum(len(hs) for hs in held) == case["total_kv_copies"]
+        assert all(len(hs) / nkv == case["kv_fraction_per_rank"] for hs in held)
+        for r in range(t):
+            q_heads = range(r * nh // t, (r + 1) * nh // t)
+            assert len(q_heads) == case["q_heads_per_rank"]
+            # every query head of the rank attends to a KV head the rank holds (GQA grouping)
+            assert all(q // (nh // nkv) in held[r] for q in q_heads)
+    q = g["qwen3_0_6b"]
+    for t in q["tp_without_replication"]:
+        held = [O.kv_head_of_rank(q["num_kv_heads"], t, r) for r in range(t)]
+        assert sorted(h for hs in held for h in hs) == list(range(q["num_kv_heads"]))
+
+
+def test_qkv_shard_gqa_layout():
+    hs, hid = 2, 3
+    nh, nkv = 8, 2
+
+    def by_head(n, base):
+        return np.array([[float(base + h)] * hid for h in range(n) for _ in range(hs)])
+
+    wq, wk, wv = by_head(nh, 0), by_head(nkv, 100), by_head(nkv, 200)
+    # t divides the KV heads: same as the plain double cut
+    for r in range(2):
+        assert np.array_equal(O.qkv_shard_gqa(wq, wk, wv, nh, nkv, hs, 2, r), O.qkv_shard(wq, wk, wv, nh, nkv, hs, 2, r))
+    # t = 4 > 2 KV heads: ranks 0,1 hold KV head 0, ranks 2,3 hold KV head 1
+    for r in range(4):
+        blk = O.qkv_shard_gqa(wq, wk, wv, nh, nkv, hs, 4, r)
+        assert blk[:, 0].tolist() == [2 * r, 2 * r, 2 * r + 1, 2 * r + 1] + [100 + r // 2] * 2 + [200 + r // 2] * 2
+    with pytest.raises(ValueError):
+        O.qkv_shard_gqa(wq, wk, wv, nh, nkv, hs, 3, 0)        # 3 does not divide 8 query heads
