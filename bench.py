@@ -80,7 +80,15 @@ class ClockSampler:
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        # Wait for the first sample: nvidia-smi's first NVML initialisation on a fresh machine
+        # can hold the driver for a while, and must not fall into the timed region.
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 10.0:
+            self.out.flush()
+            if os.path.getsize(self.out.name) > 0:
+                break
+            time.sleep(0.05)
+        time.sleep(0.2)
         return self
 
     def __exit__(self, *exc):
@@ -280,7 +288,8 @@ def run_ours(args, rank, world, local_rank):
            "ms_by_chunks": {str(k): v * 1e3 for k, v in e2e_runs.items()}}
 
     if not args.no_detail:
-        detail.update(bench_detail(torch, tp, synth, dev, peaks, wgu, wds, x))
+        rows = tuple(args.detail_rows.split(",")) if args.detail_rows else DETAIL_ROWS
+        detail.update(bench_detail(torch, tp, synth, dev, peaks, wgu, wds, x, rows))
     del wgu, wds, hbuf, parts
 
     cpu = None
@@ -305,13 +314,34 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
-def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
-    """Every other row of the hot path, timed once each (not part of value)."""
+DETAIL_ROWS = ("prefill", "decode", "prefill_t8", "reduce_sweep", "seqpar", "embed", "lm_head")
+
+
+def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
+    """Every other row of the hot path, timed once each (not part of value).
+    `rows` selects sections (all by default; single rows serve profiling)."""
     out = {}
     hbm = peaks["hbm_gbs"]
     ten = peaks["bf16_tflops"]
     # fused down-GEMM + reduce, t=4 (reuses the step's weights)
     y = torch.empty((N_TOK, H), dtype=torch.bfloat16, device=dev)
+    if "prefill" in rows:
+        out.update(_detail_prefill(torch, tp, dev, ten, wgu4, wds4, x, y))
+    if "decode" in rows:
+        out.update(_detail_decode(torch, tp, dev, hbm, wgu4, wds4, x))
+    if "prefill_t8" in rows:
+        out.update(_detail_prefill_t8(torch, tp, synth, dev, ten, y))
+    if "reduce_sweep" in rows:
+        out["shard_reduce_sweep"] = _detail_reduce_sweep(torch, tp, dev, hbm)
+    if "seqpar" in rows:
+        out.update(_detail_seqpar(torch, tp, dev, hbm))
+    if "embed" in rows or "lm_head" in rows:
+        out.update(_detail_vocab(torch, tp, synth, dev, hbm, ten, rows))
+    return out
+
+
+def _detail_prefill(torch, tp, dev, ten, wgu4, wds4, x, y):
+    out = {}
     ws_f = torch.empty(tp.tp_mlp_workspace_size(T, N_TOK, H, F, "fused", torch.bfloat16), dtype=torch.uint8,
                        device=dev)
     # The prefill rows below are short bursts (a few launches), so they run nearer boost clock than
@@ -322,7 +352,13 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
                        device=dev)
     s = time_fn(torch, lambda: tp.tp_mlp_forward(x, wgu4, wds4, mode="ring", workspace=ws_d, y=y), 5)
     out["prefill_t4_ring"] = {"ms": s * 1e3, "tflops": FLOPS / s / 1e12, "frac": FLOPS / s / 1e12 / ten}
-    # decode, t=4, n in {1, 16, 64}: weight streaming
+    del ws_f, ws_d
+    return out
+
+
+def _detail_decode(torch, tp, dev, hbm, wgu4, wds4, x):
+    """Decode, t=4, n in {1, 16, 64}: weight streaming."""
+    out = {}
     wbytes = 3.0 * H * F * 2
     for n in (1, 16, 64):
         xs = x[:n].contiguous()
@@ -338,8 +374,12 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
             if gs:
                 rec.update({"graph_us": gs * 1e6, "graph_hbm_frac": wbytes / gs / 1e9 / hbm})
             out[f"decode_t4_n{n}_{mode}"] = rec
-    del ws_f, ws_d
-    # t=8 prefill, separate and fused
+    return out
+
+
+def _detail_prefill_t8(torch, tp, synth, dev, ten, y):
+    """t=8 prefill, separate and fused."""
+    out = {}
     x8, wgu8, wds8 = make_mlp(torch, synth, 8, N_TOK, H, F, dev, seed=50)
     for mode in ("direct", "fused"):
         ws8 = torch.empty(tp.tp_mlp_workspace_size(8, N_TOK, H, F, mode, torch.bfloat16), dtype=torch.uint8,
@@ -349,7 +389,11 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
         del ws8
     del x8, wgu8, wds8
     torch.cuda.empty_cache()
-    # shard-reduce sweep: t in {2,4,8}, n in {1,64,8192}, h=8192, bf16 and fp32, direct and ring
+    return out
+
+
+def _detail_reduce_sweep(torch, tp, dev, hbm):
+    """Shard-reduce sweep: t in {2,4,8}, n in {1,64,8192}, h=8192, bf16 and fp32, direct and ring."""
     sweep = {}
     for dt in (torch.bfloat16, torch.float32):
         es = 2 if dt == torch.bfloat16 else 4
@@ -365,8 +409,12 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
                     sweep[f"{'bf16' if es == 2 else 'f32'}_t{t}_n{n}_{mode}"] = {
                         "us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm}
             del base
-    out["shard_reduce_sweep"] = sweep
-    # sequence parallelism: reduce-scatter + residual + RMSNorm (all-gather in place), t=4, bf16
+    return sweep
+
+
+def _detail_seqpar(torch, tp, dev, hbm):
+    """Sequence parallelism: reduce-scatter + residual + RMSNorm (all-gather in place), t=4, bf16."""
+    out = {}
     parts4 = [torch.randn((N_TOK, H), device=dev).to(torch.bfloat16) for _ in range(4)]
     resid = torch.randn((N_TOK, H), device=dev).to(torch.bfloat16)
     wn = torch.randn((H,), device=dev).to(torch.bfloat16)
@@ -379,7 +427,12 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
         out[f"rs_rmsnorm_t4_n{N_TOK}_{mode}"] = {"us": s * 1e6, "GBps": byts / s / 1e9,
                                                  "hbm_frac": byts / s / 1e9 / hbm}
     del parts4, resid, res_out, nrm
-    # vocab-parallel embedding + LM head, V=151936, h=1024, 4096 ids
+    return out
+
+
+def _detail_vocab(torch, tp, synth, dev, hbm, ten, rows):
+    """Vocab-parallel embedding + LM head, V=151936, h=1024, 4096 ids."""
+    out = {}
     V, hh, nt = 151936, 1024, 4096
     table = synth.normal_bf16((V, hh), 0.02, 6, device=dev)
     ids = synth.uniform_ids(nt, V, 5, device=dev)
@@ -389,7 +442,7 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
     for t in (2, 4):
         per = (V + t - 1) // t
         shards = [table[r * per:min((r + 1) * per, V)].contiguous() for r in range(t)]
-        for tag, idv in (("", ids), ("_65536ids", ids_big)):
+        for tag, idv in ((("", ids), ("_65536ids", ids_big)) if "embed" in rows else ()):
             m = idv.numel()
             e = torch.empty((m, hh), dtype=torch.bfloat16, device=dev)
             s = time_fn(torch, lambda: tp.vocab_parallel_embed(idv, shards, V, out=e), 200 if m == nt else 50)
@@ -401,6 +454,8 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x):
                 rec["graph_GBps"] = byts / graph_s / 1e9
                 rec["graph_hbm_frac"] = byts / graph_s / 1e9 / hbm
             out[f"embed_t{t}{tag}"] = rec
+        if "lm_head" not in rows:
+            continue
         s = time_fn(torch, lambda: tp.lm_head_sharded(xh, shards, V, logits=logits), 10)
         fl = 2.0 * nt * hh * V
         out[f"lm_head_t{t}"] = {"ms": s * 1e3, "tflops": fl / s / 1e12, "frac": fl / s / 1e12 / ten,
@@ -510,6 +565,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=8192,
                     help="token count of the step (8192 is the bench workload; smaller only for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--detail-rows", default="",
+                    help="comma-separated subset of " + ",".join(DETAIL_ROWS) + " (default: all)")
     args = ap.parse_args()
     global N_TOK, FLOPS
     N_TOK = args.tokens

@@ -235,6 +235,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
+// The same arrive without release semantics: it orders nothing but the
+// thread's own program order, so it does not wait for the thread's global
+// stores to become visible.  Used where the waiter only needs to know that
+// this thread's TMEM loads are done (tcgen05.wait::ld and a tcgen05 fence
+// precede it).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+}
+
 // 2-D tiled TMA load into this CTA's shared memory whose completion bytes are
 // counted on `bar` (a cluster address, here the pair leader's barrier).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1) {

@@ -540,9 +540,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                     if (row_ok) store_chunk(out, args.ldo, args.out_f32, grow, col0, nvalid, v);
                 }
             }
+            // The MMA only needs this warp's TMEM loads finished (wait::ld above) before it
+            // overwrites the accumulator; the output stores need no ordering inside the kernel.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(tempty_bar(acc), 0));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
