@@ -119,12 +119,10 @@ tp_status launch_vocab_embed(const EmbedDesc& d, cudaStream_t stream) {
     a.with_partials = d.with_partials;
     // one warp per token; at most one resident wave of blocks (grid-stride beyond)
     const int64_t want = (d.n * 32 + 255) / 256;
-    static int sms = 0, per_sm[2] = {0, 0};
-    if (sms <= 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    static int per_sm[2] = {0, 0};            // a property of the kernel, the same on every GB300
     int& occ = per_sm[d.bf16 ? 1 : 0];
     if (occ <= 0) {
         if (d.bf16)

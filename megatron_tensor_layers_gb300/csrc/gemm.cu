@@ -683,9 +683,12 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // A persistent grid of pairs that can all be resident at once.
-    static int max_clusters[2] = {0, 0};
-    int& mc = max_clusters[EPI == EPI_GLU ? 1 : 0];
+    // A persistent grid of pairs that can all be resident at once (per device).
+    static int max_clusters[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int scratch_mc = 0;
+    int& mc = (dev >= 0 && dev < 64) ? max_clusters[dev] : scratch_mc;
     if (mc <= 0) {
         int v = 0;
         if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess || v <= 0) v = sms / 2;
@@ -726,6 +729,8 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     a.act = d.act;
     a.status = d.status;
     if (d.M == 0 || d.N == 0) return TP_OK;
+    // tile indices are 32-bit in the kernels
+    if (static_cast<int64_t>(d.groups) * ((d.M + 127) / 128) * ((d.N + 63) / 64) > INT32_MAX) return TP_ERR_UNSUPPORTED;
 
     const int sms = std::max(1, sm_count());
     const bool glu = d.glu != 0;

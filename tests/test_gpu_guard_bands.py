@@ -1,0 +1,120 @@
+"""Guard bands: every kernel writes only inside its outputs.
+
+compute-sanitizer is not available on this machine, so out-of-bounds writes are
+caught directly: each output is a strided view inside a larger buffer filled
+with a canary pattern (padding after every row and a band after the end),
+the kernels run on ragged shapes, and every canary must be intact afterwards.
+"""
+
+import pytest
+import torch
+
+from megatron_tensor_layers_gb300 import _lib as tp
+from megatron_tensor_layers_gb300 import synth
+from megatron_tensor_layers_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+CANARY_BF16 = -12345          # int16 pattern
+CANARY_F32 = -987654321       # int32 pattern
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+    tp.load()
+
+
+def guarded(rows, cols, dtype, pad_cols=24, pad_rows=3):
+    """A [rows, cols] view (row stride cols + pad_cols) inside a canary-filled buffer."""
+    ld = cols + pad_cols
+    itype, canary = (torch.int16, CANARY_BF16) if dtype == torch.bfloat16 else (torch.int32, CANARY_F32)
+    buf = torch.full(((rows + pad_rows) * ld,), canary, dtype=itype, device=DEV)
+    view = buf.view(dtype)[: rows * ld].view(rows, ld)[:, :cols]
+    mask = torch.ones(((rows + pad_rows) * ld,), dtype=torch.bool, device=DEV)
+    mask.view(-1)[: rows * ld].view(rows, ld)[:, :cols] = False
+    return view, buf, mask, canary
+
+
+def intact(buf, mask, canary):
+    return bool(torch.all(buf[mask] == canary).item())
+
+
+def ints(shape, seed, dtype=torch.bfloat16):
+    return synth.int_valued(shape, -3, 3, seed, dtype=dtype, device=DEV)
+
+
+@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
+def test_gemm_outputs_stay_inside(pair, ydt):
+    tp.tp_set_gemm_cta_pair(pair if pair else -1)
+    try:
+        t, n, k, os_ = 3, 530, 200, 136
+        x = ints((n, k), 1)
+        w = [ints((os_, k), 2 + r) for r in range(t)]
+        outs = [guarded(n, os_, ydt) for _ in range(t)]
+        tp.tp_linear_col(x, w, y=[o[0] for o in outs], y_dtype=ydt)
+        g = guarded(n, os_ * t, ydt)
+        tp.tp_linear_col(x, w, gather_output=True, y=g[0], y_dtype=ydt)
+        wgu = [ints((2 * os_, k), 9 + r) for r in range(t)]
+        hg = [guarded(n, os_, ydt) for _ in range(t)]
+        tp.tp_linear_col(x, wgu, act="silu", y=[o[0] for o in hg], y_dtype=ydt)
+        xs = [ints((n, 72), 20 + r) for r in range(t)]
+        ws = [ints((264, 72), 30 + r) for r in range(t)]
+        yf = guarded(n, 264, ydt)
+        tp.tp_linear_row(xs, ws, mode="fused", y=yf[0], y_dtype=ydt)
+        parts = [guarded(n, 264, torch.float32) for _ in range(t)]
+        tp.tp_linear_row(xs, ws, reduce_results=False, partials=[p[0] for p in parts], partial_dtype=torch.float32)
+        torch.cuda.synchronize()
+        for o in outs + [g] + hg + [yf] + parts:
+            assert intact(o[1], o[2], o[3])
+    finally:
+        tp.tp_set_gemm_cta_pair(0)
+
+
+def test_lm_head_and_gather_stay_inside():
+    t, V, n, h = 3, 1001, 300, 64
+    x = ints((n, h), 40)
+    table = ints((V, h), 41)
+    per = (V + t - 1) // t
+    shards = [table[r * per:min((r + 1) * per, V)].contiguous() for r in range(t)]
+    lg = guarded(n, V, torch.float32)
+    tp.lm_head_sharded(x, shards, V, logits=lg[0], out_dtype=torch.float32)
+    per_shard = tp.lm_head_sharded(x, shards, V, per_shard=True, out_dtype=torch.bfloat16)
+    cat_buf = torch.full((n * V + 4096,), CANARY_BF16, dtype=torch.int16, device=DEV)
+    cat = cat_buf.view(torch.bfloat16)[: n * V].view(n, V)
+    tp.tp_shard_gather(per_shard, out=cat)
+    torch.cuda.synchronize()
+    assert intact(lg[1], lg[2], lg[3])
+    assert bool(torch.all(cat_buf[n * V:] == CANARY_BF16).item())
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("mode", ["direct", "ring"])
+def test_reduce_embed_seqpar_stay_inside(dtype, mode):
+    t, count = 3, 10007
+    parts = [synth.normal_f32((count,), 1.0, 50 + r, device=DEV).to(dtype) for r in range(t)]
+    itype, canary = (torch.int16, CANARY_BF16) if dtype == torch.bfloat16 else (torch.int32, CANARY_F32)
+    ob = torch.full((count + 4096,), canary, dtype=itype, device=DEV)
+    tp.tp_shard_reduce(parts, out=ob.view(dtype)[:count], mode=mode)
+    # embedding: rows of 16 bf16 in a buffer with a guard band after the last row
+    V, h, n = 97, 16, 333
+    table = synth.normal_bf16((V, h), 1.0, 60, device=DEV)
+    per = (V + t - 1) // t
+    shards = [table[r * per:min((r + 1) * per, V)].contiguous() for r in range(t)]
+    ids = synth.uniform_ids(n, V, 61, device=DEV)
+    eb = torch.full((n * h + 4096,), CANARY_BF16, dtype=torch.int16, device=DEV)
+    tp.vocab_parallel_embed(ids, shards, V, out=eb.view(torch.bfloat16)[: n * h].view(n, h))
+    # reduce-scatter + RMSNorm
+    n2, h2 = 37, 520
+    p2 = [synth.normal_f32((n2, h2), 1.0, 70 + r, device=DEV).to(dtype) for r in range(t)]
+    w2 = synth.normal_bf16((h2,), 1.0, 80, device=DEV)
+    rb = torch.full((n2 * h2 + 4096,), CANARY_BF16, dtype=torch.int16, device=DEV)
+    nb = torch.full((n2 * h2 + 4096,), CANARY_BF16, dtype=torch.int16, device=DEV)
+    tp.tp_reduce_scatter_rmsnorm(p2, w2, mode=mode, residual_out=rb.view(torch.bfloat16)[: n2 * h2].view(n2, h2),
+                                 out=nb.view(torch.bfloat16)[: n2 * h2].view(n2, h2))
+    torch.cuda.synchronize()
+    assert bool(torch.all(ob[count:] == canary).item())
+    assert bool(torch.all(eb[n * h:] == CANARY_BF16).item())
+    assert bool(torch.all(rb[n2 * h2:] == CANARY_BF16).item())
+    assert bool(torch.all(nb[n2 * h2:] == CANARY_BF16).item())
