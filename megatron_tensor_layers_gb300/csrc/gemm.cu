@@ -125,9 +125,15 @@ __device__ __forceinline__ void store_chunk(void* base, int64_t ldo, int out_f32
     }
 }
 
-template <int BN, int STAGES, int EPI>
+// AROWS: shared-memory rows of a stage's A tile.  Launches with M <= 64
+// (decode) keep 64 rows and spend the room on a deeper B ring, since their
+// time is the weight stream and the bytes each SM keeps in flight bound it.
+// The M = 128 MMA then also reads the 64 rows that follow the A tile (the
+// same stage's B tile, already landed) as A rows 64-127; those accumulator
+// rows are never stored.
+template <int BN, int STAGES, int EPI, int AROWS = BM>
 struct GemmCfg {
-    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int A_BYTES = AROWS * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;                 // two accumulators
@@ -137,11 +143,14 @@ struct GemmCfg {
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(BN % 16 == 0 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+    static_assert(AROWS == BM || (AROWS == 64 && B_BYTES >= 64 * BK * 2),
+                  "a 64-row A tile needs at least 64 rows of B behind it in the stage");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int AROWS>
 __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_constant__ GemmArgs args) {
-    using Cfg = GemmCfg<BN, STAGES, EPI>;
+    using Cfg = GemmCfg<BN, STAGES, EPI, AROWS>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles.
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -193,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                 int g, m, n;
                 tile_coords(args, tile, g, m, n);
                 // With a few rows of A every CTA would read the same line of A at the same k;
-                // starting each tile's K loop elsewhere spreads those reads over L2.
+                // starting each tile's K loop (each segment's, with segments) elsewhere spreads
+                // those reads over L2 and the weight reads over the DRAM channels.
                 const int rot = args.rotate_k ? tile % args.k_blocks : 0;
                 for (int kk = 0; kk < kb_per_tile; ++kk) {
                     const int seg = kk / args.k_blocks;
@@ -620,9 +630,10 @@ static int raster_band(int tile_rows, int64_t k_total) {
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(band, 64)));
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int AROWS = BM>
 static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream) {
-    using Cfg = GemmCfg<BN, STAGES, EPI>;
+    using Cfg = GemmCfg<BN, STAGES, EPI, AROWS>;
+    if (AROWS < BM && d.M > AROWS) return TP_ERR_UNSUPPORTED;   // a short A tile holds one m-tile
     a.n_tiles = (d.N + Cfg::OUT_COLS - 1) / Cfg::OUT_COLS;
     a.total_tiles = a.groups * a.m_tiles * a.n_tiles;
     if (a.total_tiles == 0) return TP_OK;
@@ -633,15 +644,16 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
     // the rest of the 128-row shared tile is never read into an output row.
     a.a_box_rows = static_cast<int>(std::min<int64_t>(BM, (d.M + 7) / 8 * 8));
     a.group_m = raster_band(BM, d.K * d.segs);
-    // decode-sized A, and not the fused reduce (which must accumulate shards in rank order)
-    a.rotate_k = (d.M <= 64 && d.segs == 1) ? 1 : 0;
+    // decode-sized A; with K segments the rotation stays inside each segment,
+    // so the fused reduce still adds the shards in rank order
+    a.rotate_k = d.M <= 64 ? 1 : 0;
     for (int i = 0; i < nA; ++i)
         if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
     for (int i = 0; i < nB; ++i) {
         const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
         if (!make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box)) return TP_ERR_CUDA;
     }
-    auto kern = tp_gemm_kernel<BN, STAGES, EPI>;
+    auto kern = tp_gemm_kernel<BN, STAGES, EPI, AROWS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return TP_ERR_CUDA;
     const int sms = sm_count();
@@ -761,6 +773,16 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     if (pair) {
         if (glu) return launch_pair<kPairStages, EPI_GLU>(a, d, stream);
         return launch_pair<kPairStages, EPI_STORE>(a, d, stream);
+    }
+    if (d.M <= 64) {   // decode: 64-row A tiles, deeper B rings
+        if (glu) {
+            if (best == 256) return launch_cfg<256, 5, EPI_GLU, 64>(a, d, stream);
+            if (best == 128) return launch_cfg<128, 9, EPI_GLU, 64>(a, d, stream);
+            return launch_cfg<64, 14, EPI_GLU, 64>(a, d, stream);
+        }
+        if (best == 256) return launch_cfg<256, 5, EPI_STORE, 64>(a, d, stream);
+        if (best == 128) return launch_cfg<128, 9, EPI_STORE, 64>(a, d, stream);
+        return launch_cfg<64, 14, EPI_STORE, 64>(a, d, stream);
     }
     if (glu) {
         if (best == 256) return launch_cfg<256, 4, EPI_GLU>(a, d, stream);
