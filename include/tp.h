@@ -384,6 +384,19 @@ tp_status tp_set_gemm_tile_n(int n);
 tp_status tp_set_gemm_cta_pair(int mode);
 
 /*
+ * Use of the split-K kernel for the fused reduce (TP_REDUCE_FUSED) at decode
+ * sizes (at most 64 token rows): a cluster of CTAs shares each output tile,
+ * each CTA accumulating whole shards, and the CTAs add their fp32
+ * accumulators in rank order through distributed shared memory.  mode 0 =
+ * automatic (when the output has fewer 256-wide tiles than the GPU has SMs),
+ * -1 = never, 1 = whenever the shape allows it (at most 64 rows, at least two
+ * shards).  max_clusters > 0 caps the clusters resident at once, so that each
+ * cluster walks several tiles; 0 = as many as fit.  For tests and tuning.
+ * TP_ERR_INVALID_ARG for other values.
+ */
+tp_status tp_set_gemm_split(int mode, int max_clusters);
+
+/*
  * Test hook for the failure path: launches one thread block that waits, with
  * the library's bounded wait, on a shared-memory barrier that nothing ever
  * signals.  The wait gives up after `limit_ns` nanoseconds (capped at 1 s)

@@ -23,6 +23,7 @@ from ._lib import (  # noqa: F401
     tp_reduce_scatter_rmsnorm,
     tp_reset_collective_count,
     tp_set_gemm_cta_pair,
+    tp_set_gemm_split,
     tp_set_gemm_tile_n,
     tp_shard_gather,
     tp_shard_reduce,

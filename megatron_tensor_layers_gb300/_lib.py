@@ -33,7 +33,7 @@ EXPORTED = [
     "tp_mlp_workspace_size", "tp_mlp_forward", "vocab_parallel_embed", "lm_head_sharded",
     "tp_shard_gather", "tp_device_status", "tp_collective_count", "tp_reset_collective_count",
     "tp_debug_expire_wait", "tp_set_gemm_tile_n", "tp_mlp_forward_static", "tp_set_gemm_cta_pair", "tp_mlp_forward_host",
-    "tp_reduce_scatter_rmsnorm",
+    "tp_reduce_scatter_rmsnorm", "tp_set_gemm_split",
 ]
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -75,6 +75,7 @@ def load() -> ctypes.CDLL:
         "tp_debug_expire_wait": (I32, [ctypes.c_uint64, P]),
         "tp_set_gemm_tile_n": (I32, [I32]),
         "tp_set_gemm_cta_pair": (I32, [I32]),
+        "tp_set_gemm_split": (I32, [I32, I32]),
         "tp_reduce_scatter_rmsnorm": (I32, [I32, I64, I64, I32, P, P, P, ctypes.c_float, I32, P, P, P]),
         "tp_mlp_forward_host": (I32, [I32, I64, I64, I64, P, P, P, I64, P, I32, I32, I32, P, P, ctypes.c_size_t, P, P,
                                       I32, I32, P, P]),
@@ -287,6 +288,13 @@ def tp_debug_expire_wait(limit_ns: int, stream=None) -> None:
 def tp_set_gemm_cta_pair(mode: int) -> None:
     """1: always use the CTA-pair GEMM kernel, -1: never, 0: automatic."""
     _check("tp_set_gemm_cta_pair", load().tp_set_gemm_cta_pair(mode))
+
+
+def tp_set_gemm_split(mode: int, max_clusters: int = 0) -> None:
+    """Split-K kernel of the fused reduce at decode sizes: 1 always (when the
+    shape allows it), -1 never, 0 automatic; max_clusters > 0 caps the
+    clusters resident at once."""
+    _check("tp_set_gemm_split", load().tp_set_gemm_split(mode, max_clusters))
 
 
 def tp_set_gemm_tile_n(n: int) -> None:

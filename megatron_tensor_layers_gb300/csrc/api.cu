@@ -20,6 +20,16 @@ namespace {
 std::atomic<uint64_t> g_collectives{0};
 std::atomic<int> g_tile_n{0};
 std::atomic<int> g_pair{0};
+std::atomic<int> g_split{0};
+std::atomic<int> g_split_clusters{0};
+
+// The GEMM tuning knobs in effect for a launch.
+void apply_knobs(tpk::GemmDesc& d) {
+    d.force_bn = g_tile_n.load();
+    d.pair = g_pair.load();
+    d.split = g_split.load();
+    d.split_clusters = g_split_clusters.load();
+}
 
 int* status_ptr() {
     int dev = 0;
@@ -111,8 +121,7 @@ tp_status tp_linear_col(int t, int64_t n, int64_t in, int64_t out_full, const vo
     d.ldo = ldy;
     d.out_f32 = y_dtype == TP_F32;
     d.status = status_ptr();
-    d.force_bn = g_tile_n.load();
-    d.pair = g_pair.load();
+    apply_knobs(d);
     for (int r = 0; r < t; ++r) {
         d.b[r] = w[r];
         d.out[r] = gather_output ? static_cast<void*>(static_cast<char*>(y[0]) + r * os * ey) : y[r];
@@ -199,8 +208,7 @@ tp_status tp_linear_row(int t, int64_t n, int64_t in_full, int64_t out, const vo
     d.ldb = ldw;
     d.b_rows = out;
     d.status = status_ptr();
-    d.force_bn = g_tile_n.load();
-    d.pair = g_pair.load();
+    apply_knobs(d);
     if (fused) {
         d.groups = 1;
         d.segs = t;
@@ -292,8 +300,7 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, 
     c.ldo = f;
     c.out_f32 = 0;
     c.status = status_ptr();
-    c.force_bn = g_tile_n.load();
-    c.pair = g_pair.load();
+    apply_knobs(c);
     for (int r = 0; r < t; ++r) {
         c.b[r] = w_gate_up[r];
         c.out[r] = hbuf + r * fs;
@@ -375,8 +382,7 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab, const void
     d.out_f32 = out_dtype == TP_F32;
     d.ldo = logits != nullptr ? ldl : 0;
     d.status = status_ptr();
-    d.force_bn = g_tile_n.load();
-    d.pair = g_pair.load();
+    apply_knobs(d);
     int g = 0;
     for (int r = 0; r < t; ++r) {
         const int64_t start = std::min<int64_t>(r * per, vocab);
@@ -500,6 +506,13 @@ tp_status tp_set_gemm_tile_n(int n) {
 tp_status tp_set_gemm_cta_pair(int mode) {
     if (mode < -1 || mode > 1) return TP_ERR_INVALID_ARG;
     g_pair.store(mode);
+    return TP_OK;
+}
+
+tp_status tp_set_gemm_split(int mode, int max_clusters) {
+    if (mode < -1 || mode > 1 || max_clusters < 0) return TP_ERR_INVALID_ARG;
+    g_split.store(mode);
+    g_split_clusters.store(max_clusters);
     return TP_OK;
 }
 

@@ -66,6 +66,7 @@ struct GemmArgs {
     int a_box_rows;                   // rows of A a TMA box loads (<= 128; fewer when M is small)
     int rotate_k;                     // start each tile's K loop at block (tile mod k_blocks)
     int act;                          // tp_act for the gated epilogue
+    int split;                        // split-K kernel: CTAs per cluster sharing one output tile
     int* status;                      // library status word
 };
 
@@ -576,6 +577,277 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
     }
 }
 
+// ------------------------------------------------------- split-K cluster kernel
+//
+// The fused reduce for decode-sized M (<= 64 token rows): with one row-tile
+// the plain kernels have only N / BN output tiles, too few for every SM at
+// BN = 256, and narrower tiles stream the weights slowly (every MMA
+// instruction costs about the same issue time whatever its N: at N = 64 a
+// 64-wide K block took 280 ns per SM, a 3.7 TB/s ceiling on 128 SMs).  Here
+// a cluster of CS CTAs shares each BN-wide output tile: CTA r runs the K loop
+// of shards [r*segs/CS, (r+1)*segs/CS) in order into its own TMEM, stages
+// its fp32 accumulator rows in its shared memory, and then every CTA adds,
+// for its share of the tile's 32-column chunks (chunk c belongs to rank
+// c mod CS), the CS staged copies in rank order over distributed shared
+// memory, adds the rank-0 bias and stores.  So the shards are still summed
+// in rank order in fp32 and no partial leaves the chip (page "6.2
+// Tensor-parallel inference", §1: Y = sum_i act(X A_i) B_i).
+//
+// Per tile and CTA: wait for the accumulator; wait until every peer has read
+// this CTA's staging of the previous tile (`drained`); stage; free the
+// accumulator; release-arrive on every peer's `staged`; acquire-wait on its
+// own `staged`; reduce and store its chunks; release-arrive on every peer's
+// `drained`.  Waits are bounded like every other wait of the library, and a
+// cluster barrier before exit keeps each CTA's shared memory alive while
+// its peers may still read it.
+template <int BN, int STAGES>
+struct SplitCfg {
+    static constexpr int ROWS = 64;                          // staged rows (M <= 64)
+    static constexpr int A_BYTES = ROWS * BK * 2;            // 64-row A tile (see GemmCfg's AROWS)
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGING_BYTES = ROWS * BN * 4;      // fp32 accumulator rows
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int NBARS = 2 * STAGES + 6;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NBARS * 8 + 16;
+    static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __grid_constant__ GemmArgs args) {
+    using Cfg = SplitCfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const uint32_t staging = base + STAGES * Cfg::STAGE_BYTES;
+    float4* staging_ptr = reinterpret_cast<float4*>(base_ptr + STAGES * Cfg::STAGE_BYTES);
+    const uint32_t bar_base = staging + Cfg::STAGING_BYTES;
+    uint8_t* bar_ptr = base_ptr + STAGES * Cfg::STAGE_BYTES + Cfg::STAGING_BYTES;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t staged_bar = bar_base + 8u * (2 * STAGES + 4);
+    const uint32_t drained_bar = bar_base + 8u * (2 * STAGES + 5);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * Cfg::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * Cfg::NBARS + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cs = args.split;
+    const int crank = static_cast<int>(cluster_ctarank());
+    const int cluster = blockIdx.x / cs;
+    const int nclusters = gridDim.x / cs;
+    const int segs_per = args.segs / cs;                 // whole shards per CTA
+    const int seg0 = crank * segs_per;
+    const int kb_rank = args.k_blocks * segs_per;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 128);
+        }
+        mbar_init(staged_bar, (cs - 1) * 128);           // every epilogue thread of every peer
+        mbar_init(drained_bar, (cs - 1) * 128);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < segs_per; ++i) {
+            prefetch_tmap(&args.mapA[seg0 + i]);
+            prefetch_tmap(&args.mapB[seg0 + i]);
+        }
+    }
+    if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(smem_u32(tmem_slot));
+    tc_fence_before();
+    cluster_sync();                                      // every CTA's barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    bool aborted = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
+                int g, m, n;
+                tile_coords(args, tile, g, m, n);
+                const int rot = args.rotate_k ? tile % args.k_blocks : 0;
+                for (int kk = 0; kk < kb_rank; ++kk) {
+                    const int sl = kk / args.k_blocks;
+                    const int seg = seg0 + sl;
+                    int kb = kk - sl * args.k_blocks + rot;
+                    if (kb >= args.k_blocks) kb -= args.k_blocks;
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
+                        aborted = true;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
+                    mbar_arrive_expect_tx(full_bar(stage), args.a_box_rows * 128 + Cfg::B_BYTES);
+                    tma_load_2d(sa, &args.mapA[seg], full_bar(stage), kb * BK, m * BM);
+                    tma_load_2d(sa + Cfg::A_BYTES, &args.mapB[seg], full_bar(stage), kb * BK, n * BN);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = mma_idesc_bf16(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kk = 0; kk < kb_rank; ++kk) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.status)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0 ? 1u : 0u);
+                    tc_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (aborted) break;
+                tc_commit(tfull_bar(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;                   // accumulator row = TMEM lane
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t j = 0;                                  // tiles done by this CTA
+        for (int tile = cluster; tile < args.total_tiles; tile += nclusters, ++j) {
+            int g, m, n;
+            tile_coords(args, tile, g, m, n);
+            const int64_t grow = static_cast<int64_t>(m) * BM + row;
+            const bool row_ok = row < Cfg::ROWS && grow < args.M;
+            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
+                aborted = true;
+                break;
+            }
+            // every peer has read this CTA's staging of the previous tile
+            if (j > 0 && !mbar_wait_cluster(drained_bar, (j - 1) & 1u, abort_flag, args.status)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(taddr + c * 32, r);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        staging_ptr[(c * 8 + i) * Cfg::ROWS + row] =
+                            make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                        __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));                // the accumulator is free for the next tile
+            for (int p = 0; p < cs; ++p)
+                if (p != crank) mbar_arrive_cluster(mapa_shared(staged_bar, static_cast<uint32_t>(p)));
+            if (cs > 1 && !mbar_wait_cluster(staged_bar, j & 1u, abort_flag, args.status)) {
+                aborted = true;
+                break;
+            }
+            void* out = args.out[0];
+            const uint16_t* bias = static_cast<const uint16_t*>(args.bias[0]);
+            const int ncols = args.n_valid[0];
+#pragma unroll 1
+            for (int c = crank; c < BN / 32; c += cs) {
+                const int col0 = n * BN + c * 32;
+                const int nvalid = min(32, ncols - col0);
+                if (!row_ok || nvalid <= 0) continue;
+                float v[32];
+#pragma unroll 1
+                for (int p = 0; p < cs; ++p) {           // rank order
+                    float4 x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        x[i] = ld_shared_cluster_f4(mapa_shared(
+                            staging + static_cast<uint32_t>(((c * 8 + i) * Cfg::ROWS + row) * 16), static_cast<uint32_t>(p)));
+                    if (p == 0) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            v[4 * i] = x[i].x;
+                            v[4 * i + 1] = x[i].y;
+                            v[4 * i + 2] = x[i].z;
+                            v[4 * i + 3] = x[i].w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            v[4 * i] += x[i].x;
+                            v[4 * i + 1] += x[i].y;
+                            v[4 * i + 2] += x[i].z;
+                            v[4 * i + 3] += x[i].w;
+                        }
+                    }
+                }
+                if (bias != nullptr) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (e < nvalid) v[e] += bf16_to_f32(bias[col0 + e]);
+                }
+                store_chunk(out, args.ldo, args.out_f32, grow, col0, nvalid, v);
+            }
+            for (int p = 0; p < cs; ++p)
+                if (p != crank) mbar_arrive_cluster(mapa_shared(drained_bar, static_cast<uint32_t>(p)));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    if (aborted) spin_ns(50000);
+    tc_fence_before();
+    cluster_sync();                                      // peers may still read this CTA's staging until here
+    if (*abort_flag) spin_ns(50000);
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc<Cfg::TMEM_COLS>(tmem_base);
+    }
+}
+
+
 // ------------------------------------------------------------------ host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -714,6 +986,80 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
+template <int BN, int STAGES>
+static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream_t stream) {
+    using Cfg = SplitCfg<BN, STAGES>;
+    if (d.M > Cfg::ROWS || d.groups != 1 || d.segs % cs != 0 || cs < 2 || cs > 8) return TP_ERR_UNSUPPORTED;
+    a.split = cs;
+    a.m_tiles = 1;
+    a.n_tiles = static_cast<int>((d.N + BN - 1) / BN);
+    a.total_tiles = a.n_tiles;
+    a.group_m = 1;
+    a.a_box_rows = static_cast<int>((d.M + 7) / 8 * 8);
+    a.rotate_k = 1;
+    for (int i = 0; i < d.segs; ++i) {
+        if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
+        if (!make_map(&a.mapB[i], d.b[i], d.b_rows, d.K, d.ldb, BN)) return TP_ERR_CUDA;
+    }
+    auto kern = tp_gemm_splitk_kernel<BN, STAGES>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+        return TP_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs * a.total_tiles, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // persistent: no more clusters than can be resident at once (cached per device and size)
+    static int max_clusters[64][9] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int scratch_mc = 0;
+    int& mc = (dev >= 0 && dev < 64) ? max_clusters[dev][cs] : scratch_mc;
+    if (mc <= 0) {
+        int v = 0;
+        if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess || v <= 0) return TP_ERR_CUDA;
+        mc = v;
+    }
+    const int cap = d.split_clusters > 0 ? std::min(mc, d.split_clusters) : mc;
+    cfg.gridDim = dim3(cs * std::min(a.total_tiles, cap), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TP_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// Split-K plan for the fused reduce at decode sizes: the tile width (256 or
+// 128) and cluster size (a divisor of the shard count, at most 8) that put
+// the most CTAs to work without exceeding one per SM.  Returns the cluster
+// size, 0 when no split applies.
+static int split_plan(const GemmDesc& d, int sms, int& bn) {
+    if (d.segs < 2 || d.glu || d.M > 64 || d.groups != 1 || d.split < 0) return 0;
+    if (d.split == 0 && (d.force_bn != 0 || d.pair > 0)) return 0;
+    const bool always = d.split > 0;
+    int best_cs = 0, best_ctas = 0;
+    bn = 0;
+    for (int w : {256, 128}) {
+        const int64_t tiles = (d.N + w - 1) / w;
+        if (tiles >= sms && !always) continue;           // the plain kernel already fills the GPU
+        for (int cs = std::min(d.segs, 8); cs >= 2; --cs) {
+            if (d.segs % cs != 0 || (tiles * cs > sms && !always)) continue;
+            const int ctas = static_cast<int>(std::min<int64_t>(tiles * cs, sms));
+            if (ctas > best_ctas) {
+                best_ctas = ctas;
+                best_cs = cs;
+                bn = w;
+            }
+            break;
+        }
+    }
+    return best_cs;
+}
+
 // Estimated time units of a launch with output tile width w: whole waves of
 // tiles times the per-tile cost (proportional to the MMA N plus a fixed
 // share for the A tile).
@@ -773,6 +1119,12 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     if (pair) {
         if (glu) return launch_pair<kPairStages, EPI_GLU>(a, d, stream);
         return launch_pair<kPairStages, EPI_STORE>(a, d, stream);
+    }
+    int split_bn = 0;
+    const int cs = split_plan(d, sms, split_bn);
+    if (cs >= 2) {
+        if (split_bn == 256) return launch_split<256, 4>(a, d, cs, stream);
+        return launch_split<128, 8>(a, d, cs, stream);
     }
     if (d.M <= 64) {   // decode: 64-row A tiles, deeper B rings
         if (glu) {

@@ -32,6 +32,8 @@ struct GemmDesc {
     int* status = nullptr;
     int force_bn = 0;                    // 0: chosen by cost; else 64/128/256
     int pair = 0;                        // CTA-pair kernel: -1 never, 0 automatic, 1 always
+    int split = 0;                       // split-K kernel (fused reduce, M <= 64): -1 never, 0 automatic, 1 always
+    int split_clusters = 0;              // > 0: at most this many split-K clusters resident
 };
 
 tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream);

@@ -102,15 +102,21 @@ def test_reduce_embed_head_gather_reject_on_host(lib):
 
 
 def test_tuning_knobs_through_the_binding(lib):
-    from megatron_tensor_layers_gb300 import TPError, tp_set_gemm_cta_pair, tp_set_gemm_tile_n
+    from megatron_tensor_layers_gb300 import TPError, tp_set_gemm_cta_pair, tp_set_gemm_split, tp_set_gemm_tile_n
     for mode in (1, -1, 0):
         tp_set_gemm_cta_pair(mode)
     for n in (64, 128, 256, 0):
         tp_set_gemm_tile_n(n)
+    for mode, cap in ((1, 3), (-1, 0), (0, 0)):
+        tp_set_gemm_split(mode, cap)
     with pytest.raises(TPError):
         tp_set_gemm_cta_pair(2)
     with pytest.raises(TPError):
         tp_set_gemm_tile_n(96)
+    with pytest.raises(TPError):
+        tp_set_gemm_split(2)
+    with pytest.raises(TPError):
+        tp_set_gemm_split(0, -1)
 
 
 def test_host_pipeline_rejects_on_host(lib):

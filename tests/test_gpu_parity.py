@@ -663,3 +663,51 @@ def test_qkv_gqa_replicated_layout_integer_exact(t, nh, nkv, hd):
     torch.cuda.synchronize()
     for r in range(t):
         exact(f64(y[r]), O.linear(f64(x), O.qkv_shard_gqa(wqf, wkf, wvf, nh, nkv, hd, t, r)))
+
+
+# --------------------------------------------- split-K kernel of the fused reduce
+
+@pytest.fixture
+def split_knob(request):
+    mode, cap = request.param
+    tp.tp_set_gemm_split(mode, cap)
+    yield mode, cap
+    tp.tp_set_gemm_split(0, 0)
+
+
+# (mode, max clusters): automatic; always with every cluster resident; always with one
+# cluster walking every tile and with three (the staging hand-off between tiles)
+@pytest.mark.parametrize("split_knob", [(0, 0), (1, 0), (1, 1), (1, 3)], indirect=True)
+@pytest.mark.parametrize("t,n,ks,out", [(2, 1, 64, 1000), (3, 9, 200, 520), (4, 64, 128, 8192), (5, 17, 64, 300),
+                                        (8, 33, 96, 2056)])
+def test_fused_row_split_k_integer_exact(split_knob, t, n, ks, out):
+    x = [ints((n, ks), 60 + r) for r in range(t)]
+    w = [ints((out, ks), 70 + r) for r in range(t)]
+    bias = ints((out,), 80, -8, 8)
+    y = tp.tp_linear_row(x, w, bias=bias, mode="fused", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    parts = [O.linear(f64(x[r]), f64(w[r]), f64(bias) if r == 0 else None) for r in range(t)]
+    exact(f64(y), O.reduce_direct(parts))
+
+
+@pytest.mark.parametrize("t", [2, 4, 8])
+@pytest.mark.parametrize("n", [1, 16, 64])
+def test_fused_row_split_k_float_and_deterministic(t, n):
+    ks, out = 256, 4096
+    x = [normal((n, ks), 1.0, 90 + r) for r in range(t)]
+    w = [normal((out, ks), 0.02, 100 + r) for r in range(t)]
+    y1 = tp.tp_linear_row(x, w, mode="fused")
+    y2 = tp.tp_linear_row(x, w, mode="fused")
+    y32 = tp.tp_linear_row(x, w, mode="fused", y_dtype=torch.float32)
+    tp.tp_set_gemm_split(-1, 0)
+    try:
+        y_plain = tp.tp_linear_row(x, w, mode="fused", y_dtype=torch.float32)
+    finally:
+        tp.tp_set_gemm_split(0, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    ref = O.reduce_direct([O.linear(f64(x[r]), f64(w[r])) for r in range(t)])
+    gemm_gate(f64(y1), ref, bf16_out=True)
+    gemm_gate(f64(y32), ref, bf16_out=False)
+    gemm_gate(f64(y_plain), ref, bf16_out=False)
