@@ -314,7 +314,7 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
-DETAIL_ROWS = ("prefill", "decode", "prefill_t8", "reduce_sweep", "seqpar", "embed", "lm_head")
+DETAIL_ROWS = ("prefill", "decode", "prefill_t8", "reduce_sweep", "seqpar", "embed", "lm_head", "tiny")
 
 
 def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
@@ -337,6 +337,8 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
         out.update(_detail_seqpar(torch, tp, dev, hbm))
     if "embed" in rows or "lm_head" in rows:
         out.update(_detail_vocab(torch, tp, synth, dev, hbm, ten, rows))
+    if "tiny" in rows:
+        out.update(_detail_tiny(torch, tp, synth, dev))
     return out
 
 
@@ -389,6 +391,25 @@ def _detail_prefill_t8(torch, tp, synth, dev, ten, y):
         del ws8
     del x8, wgu8, wds8
     torch.cuda.empty_cache()
+    return out
+
+
+def _detail_tiny(torch, tp, synth, dev):
+    """The tiny TP-MLP (t=2, h=1024, f=3072, n=8): a latency row, in us per MLP
+    (gate_up GEMM + down GEMM + reduce, or the fused down+reduce)."""
+    out = {}
+    t, n, h, f = 2, 8, 1024, 3072
+    x, wgu, wds = make_mlp(torch, synth, t, n, h, f, dev, seed=90)
+    y = torch.empty((n, h), dtype=torch.bfloat16, device=dev)
+    for mode in ("direct", "ring", "fused"):
+        ws = torch.empty(max(256, tp.tp_mlp_workspace_size(t, n, h, f, mode, torch.bfloat16)), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: tp.tp_mlp_forward(x, wgu, wds, mode=mode, workspace=ws, y=y)
+        rec = {"us": time_fn(torch, fn, 100) * 1e6, "weight_MB": 3.0 * h * f * 2 / 1e6}
+        gs = graph_time(torch, fn, 100)
+        if gs:
+            rec["graph_us"] = gs * 1e6
+        out[f"tiny_t2_n8_{mode}"] = rec
     return out
 
 

@@ -57,6 +57,13 @@ def decode_step(model: DecodeModel, t: int, batch: int, hbm_bytes_per_s: float, 
     return {"step_s": total, "comm_s": comm, "tokens_per_s": batch / total, "tokens_per_s_per_gpu": batch / total / t}
 
 
+def allreduces_per_forward(layers: int) -> int:
+    """All-reduces in one forward of a TP transformer: one after each
+    layer's attention output projection and one after its MLP, plus one for
+    the vocab-parallel embedding (the LM head gathers instead)."""
+    return 2 * layers + 1
+
+
 def comm_per_forward(layers: int, hidden: int, tokens: int, t: int, busbw: float, alpha_s: float) -> float:
     """Seconds of all-reduce in one forward of `tokens` tokens (2 per layer)."""
     return 2 * layers * allreduce_time(tokens * hidden * 2, t, busbw, alpha_s)

@@ -46,3 +46,9 @@ def test_simulated_allreduce_and_cli(capsys):
     assert rows[2]["nvlink_tp8_us"] == pytest.approx(522, rel=0.01)     # the page's "about 520 us"
     cm._main([])
     assert "42.55" in capsys.readouterr().out
+
+
+def test_allreduces_per_forward_of_the_page(golden_dir):
+    g = _golden(golden_dir, "tpscratch_allreduce_count.json")
+    assert cm.allreduces_per_forward(g["layers"]) == g["prefill_forward_allreduces"]
+    assert g["allreduce_per_layer"] * g["layers"] + g["embedding_allreduce"] == g["prefill_forward_allreduces"]

@@ -711,3 +711,32 @@ def test_fused_row_split_k_float_and_deterministic(t, n):
     gemm_gate(f64(y1), ref, bf16_out=True)
     gemm_gate(f64(y32), ref, bf16_out=False)
     gemm_gate(f64(y_plain), ref, bf16_out=False)
+
+
+def test_allreduce_count_of_a_28_layer_forward(golden_dir):
+    """The call sequence of one prefill forward at TP=2 (embedding, then per
+    layer the attention output projection and the MLP, then the LM head) on
+    tiny shapes: the library counts one collective per all-reduce the page
+    counts, and the LM head adds its gather."""
+    import json, os
+    with open(os.path.join(golden_dir, "tpscratch_allreduce_count.json")) as fh:
+        g = json.load(fh)
+    t, layers, n, h, f, V = g["tp"], g["layers"], 8, 64, 128, 100
+    per = (V + t - 1) // t
+    table = normal((V, h), 0.02, 11)
+    shards = [table[r * per:min((r + 1) * per, V)].contiguous() for r in range(t)]
+    ids = synth.uniform_ids(n, V, 12, device=DEV)
+    wo = [normal((h, h // t), 0.02, 13 + r) for r in range(t)]
+    wgu = [normal((2 * f // t, h), 0.02, 20 + r) for r in range(t)]
+    wds = [normal((h, f // t), 0.02, 30 + r) for r in range(t)]
+    tp.tp_reset_collective_count()
+    x = tp.vocab_parallel_embed(ids, shards, V)
+    for _ in range(layers):
+        heads = [x[:, r * (h // t):(r + 1) * (h // t)].contiguous() for r in range(t)]   # stands in for attention
+        x = x + tp.tp_linear_row(heads, wo)
+        x = x + tp.tp_mlp_forward(x, wgu, wds)
+    torch.cuda.synchronize()
+    assert tp.tp_collective_count() == g["prefill_forward_allreduces"]
+    tp.lm_head_sharded(x, shards, V)
+    torch.cuda.synchronize()
+    assert tp.tp_collective_count() == g["prefill_forward_allreduces"] + 1
