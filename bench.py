@@ -155,19 +155,23 @@ def whole_job_value(units_per_rank: float, world: int, max_seconds: float) -> fl
     return units_per_rank * world / max_seconds
 
 
-def time_fn(torch, fn, iters, warm=2, stream=None):
-    """Mean device time (s) of fn() over iters launches, CUDA events on the stream."""
+def time_fn(torch, fn, iters, warm=2, stream=None, repeats=3):
+    """Device time (s) of one fn() call: CUDA events on the stream around
+    `iters` back-to-back calls, the median over `repeats` such windows."""
     stream = stream or torch.cuda.current_stream()
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(iters):
-        fn()
-    b.record(stream)
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) / 1e3 / iters
+    times = []
+    for _ in range(repeats):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / 1e3 / iters)
+    return sorted(times)[len(times) // 2]
 
 
 def run_ours(args, rank, world, local_rank):
@@ -490,7 +494,8 @@ def _detail_vocab(torch, tp, synth, dev, hbm, ten, rows):
 
 
 def graph_time(torch, fn, reps):
-    """Per-launch time of fn replayed from a CUDA graph of `reps` launches."""
+    """Per-launch time of fn replayed from a CUDA graph of `reps` launches
+    (median of three timed windows)."""
     try:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -504,13 +509,16 @@ def graph_time(torch, fn, reps):
                 fn()
         g.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(5):
-            g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / 1e3 / (5 * reps)
+        times = []
+        for _ in range(3):                       # median of three windows of 5 replays
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(5):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) / 1e3 / (5 * reps))
+        return sorted(times)[1]
     except Exception:
         return None
 

@@ -579,28 +579,33 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
 
 // ------------------------------------------------------- split-K cluster kernel
 //
-// The fused reduce for decode-sized M (<= 64 token rows): with one row-tile
-// the plain kernels have only N / BN output tiles, too few for every SM at
-// BN = 256, and narrower tiles stream the weights slowly (every MMA
-// instruction costs about the same issue time whatever its N: at N = 64 a
-// 64-wide K block took 280 ns per SM, a 3.7 TB/s ceiling on 128 SMs).  Here
-// a cluster of CS CTAs shares each BN-wide output tile: CTA r runs the K loop
-// of shards [r*segs/CS, (r+1)*segs/CS) in order into its own TMEM, stages
-// its fp32 accumulator rows in its shared memory, and then every CTA adds,
-// for its share of the tile's 32-column chunks (chunk c belongs to rank
-// c mod CS), the CS staged copies in rank order over distributed shared
-// memory, adds the rank-0 bias and stores.  So the shards are still summed
-// in rank order in fp32 and no partial leaves the chip (page "6.2
-// Tensor-parallel inference", §1: Y = sum_i act(X A_i) B_i).
+// GEMMs with at most 64 token rows (decode, small batches).  Their time is
+// the weight stream or, for small weights, the serial K loop of a tile, and
+// the plain kernels leave SMs idle or use narrow tiles that stream slowly
+// (every MMA instruction costs about the same issue time whatever its N: at
+// N = 64 a 64-wide K block took 280 ns per SM, a 3.7 TB/s ceiling on 128
+// SMs).  Here a cluster of CS CTAs shares each BN-wide output tile: CTA r
+// runs K blocks [r*KB/CS, (r+1)*KB/CS) of the tile's KB = k_blocks * segs
+// blocks, in order, into its own TMEM (for the fused reduce these are whole
+// shards when CS divides t), stages its fp32 accumulator rows in its shared
+// memory, and then every CTA adds, for its share of the tile's 32-column
+// output chunks (chunk c belongs to rank c mod CS), the CS staged copies in
+// rank order over distributed shared memory and runs the epilogue (bias,
+// or act(gate) * up for the gated tile, whose gate and up columns are both
+// summed first).  The K blocks are therefore still summed in order in fp32:
+// for the fused reduce the shards in rank order (page "6.2 Tensor-parallel
+// inference", §1: Y = sum_i act(X A_i) B_i), and no partial leaves the chip.
 //
-// Per tile and CTA: wait for the accumulator; wait until every peer has read
-// this CTA's staging of the previous tile (`drained`); stage; free the
-// accumulator; release-arrive on every peer's `staged`; acquire-wait on its
-// own `staged`; reduce and store its chunks; release-arrive on every peer's
-// `drained`.  Waits are bounded like every other wait of the library, and a
+// Per tile and CTA: wait for the accumulator; wait until every thread of the
+// cluster has read this CTA's staging of the previous tile (`drained`);
+// stage; free the accumulator; release-arrive on the `staged` barrier of
+// every CTA of the cluster (its own included: the four epilogue warps share
+// the reduction, so a row staged by one warp is read by another);
+// acquire-wait on its own `staged`; reduce and store its chunks;
+// release-arrive on every CTA's `drained`.  Waits are bounded like every other wait of the library, and a
 // cluster barrier before exit keeps each CTA's shared memory alive while
 // its peers may still read it.
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI>
 struct SplitCfg {
     static constexpr int ROWS = 64;                          // staged rows (M <= 64)
     static constexpr int A_BYTES = ROWS * BK * 2;            // 64-row A tile (see GemmCfg's AROWS)
@@ -610,14 +615,53 @@ struct SplitCfg {
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NBARS = 2 * STAGES + 6;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NBARS * 8 + 16;
+    static constexpr int OUT_CHUNKS = (EPI == EPI_GLU ? BN / 2 : BN) / 32;   // 32-column output chunks per tile
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-template <int BN, int STAGES>
+// The 32 fp32 values of accumulator columns [col, col + 32) of `row`, summed
+// over the cluster's CS staged copies in rank order; the loads of two ranks
+// are in flight together.
+template <int ROWS>
+__device__ __forceinline__ void gather_chunk(uint32_t staging, int col, int row, int cs, float (&v)[32]) {
+    const uint32_t off = staging + static_cast<uint32_t>(((col / 4) * ROWS + row) * 16);
+#pragma unroll 1
+    for (int p = 0; p < cs; p += 2) {
+        const bool two = p + 1 < cs;
+        float4 x[8], y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            x[i] = ld_shared_cluster_f4(mapa_shared(off + i * ROWS * 16, static_cast<uint32_t>(p)));
+            if (two) y[i] = ld_shared_cluster_f4(mapa_shared(off + i * ROWS * 16, static_cast<uint32_t>(p + 1)));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (p == 0) {
+                v[4 * i] = x[i].x;
+                v[4 * i + 1] = x[i].y;
+                v[4 * i + 2] = x[i].z;
+                v[4 * i + 3] = x[i].w;
+            } else {
+                v[4 * i] += x[i].x;
+                v[4 * i + 1] += x[i].y;
+                v[4 * i + 2] += x[i].z;
+                v[4 * i + 3] += x[i].w;
+            }
+            if (two) {
+                v[4 * i] += y[i].x;
+                v[4 * i + 1] += y[i].y;
+                v[4 * i + 2] += y[i].z;
+                v[4 * i + 3] += y[i].w;
+            }
+        }
+    }
+}
+
+template <int BN, int STAGES, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __grid_constant__ GemmArgs args) {
-    using Cfg = SplitCfg<BN, STAGES>;
+    using Cfg = SplitCfg<BN, STAGES, EPI>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -641,9 +685,10 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
     const int crank = static_cast<int>(cluster_ctarank());
     const int cluster = blockIdx.x / cs;
     const int nclusters = gridDim.x / cs;
-    const int segs_per = args.segs / cs;                 // whole shards per CTA
-    const int seg0 = crank * segs_per;
-    const int kb_rank = args.k_blocks * segs_per;
+    // this CTA's K blocks of every tile, in the order (segment, block) of the whole K
+    const int kb_all = args.k_blocks * args.segs;
+    const int kb_lo = static_cast<int>(static_cast<int64_t>(crank) * kb_all / cs);
+    const int kb_hi = static_cast<int>(static_cast<int64_t>(crank + 1) * kb_all / cs);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -654,16 +699,17 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), 128);
         }
-        mbar_init(staged_bar, (cs - 1) * 128);           // every epilogue thread of every peer
-        mbar_init(drained_bar, (cs - 1) * 128);
+        // every epilogue thread of the cluster (this CTA's own threads too: a row is staged
+        // by one warp and may be reduced by another)
+        mbar_init(staged_bar, cs * 128);
+        mbar_init(drained_bar, cs * 128);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        for (int i = 0; i < segs_per; ++i) {
-            prefetch_tmap(&args.mapA[seg0 + i]);
-            prefetch_tmap(&args.mapB[seg0 + i]);
-        }
+        const int nmaps = args.segs > 1 ? args.segs : args.groups;
+        for (int i = 0; i < nmaps && i < TP_MAX_SHARDS; ++i) prefetch_tmap(&args.mapB[i]);
+        prefetch_tmap(&args.mapA[0]);
     }
     if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(smem_u32(tmem_slot));
     tc_fence_before();
@@ -680,20 +726,29 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
                 int g, m, n;
                 tile_coords(args, tile, g, m, n);
+                // rotate_k: each CTA holds whole segments; start each segment's loop elsewhere
                 const int rot = args.rotate_k ? tile % args.k_blocks : 0;
-                for (int kk = 0; kk < kb_rank; ++kk) {
-                    const int sl = kk / args.k_blocks;
-                    const int seg = seg0 + sl;
-                    int kb = kk - sl * args.k_blocks + rot;
+                for (int kk = kb_lo; kk < kb_hi; ++kk) {
+                    const int seg = kk / args.k_blocks;
+                    int kb = kk - seg * args.k_blocks + rot;
                     if (kb >= args.k_blocks) kb -= args.k_blocks;
+                    const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                    const int bi = args.segs > 1 ? seg : g;
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
                         aborted = true;
                         break;
                     }
                     const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
+                    const uint32_t sb = sa + Cfg::A_BYTES;
                     mbar_arrive_expect_tx(full_bar(stage), args.a_box_rows * 128 + Cfg::B_BYTES);
-                    tma_load_2d(sa, &args.mapA[seg], full_bar(stage), kb * BK, m * BM);
-                    tma_load_2d(sa + Cfg::A_BYTES, &args.mapB[seg], full_bar(stage), kb * BK, n * BN);
+                    tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);
+                    if (EPI == EPI_GLU) {
+                        tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * (BN / 2));
+                        tma_load_2d(sb + (BN / 2) * 128, &args.mapB[bi], full_bar(stage), kb * BK,
+                                    args.glu_up_row + n * (BN / 2));
+                    } else {
+                        tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * BN);
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -716,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kk = 0; kk < kb_rank; ++kk) {
+                for (int kk = kb_lo; kk < kb_hi; ++kk) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, args.status)) {
                         aborted = true;
                         break;
@@ -727,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
                     const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0 ? 1u : 0u);
+                        tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk > kb_lo || k > 0) ? 1u : 0u);
                     tc_commit(empty_bar(stage));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -781,54 +836,41 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));                // the accumulator is free for the next tile
             for (int p = 0; p < cs; ++p)
-                if (p != crank) mbar_arrive_cluster(mapa_shared(staged_bar, static_cast<uint32_t>(p)));
-            if (cs > 1 && !mbar_wait_cluster(staged_bar, j & 1u, abort_flag, args.status)) {
+                mbar_arrive_cluster(mapa_shared(staged_bar, static_cast<uint32_t>(p)));
+            if (!mbar_wait_cluster(staged_bar, j & 1u, abort_flag, args.status)) {
                 aborted = true;
                 break;
             }
-            void* out = args.out[0];
-            const uint16_t* bias = static_cast<const uint16_t*>(args.bias[0]);
-            const int ncols = args.n_valid[0];
+            void* out = args.out[g];
+            const uint16_t* bias = static_cast<const uint16_t*>(args.bias[g]);
+            const int ncols = args.n_valid[g];
+            // all four epilogue warps reduce: rows (q & 1) * 32 + lane, the owned chunks split in two halves
+            const int rrow = (q & 1) * 32 + lane;
+            const int64_t rgrow = static_cast<int64_t>(m) * BM + rrow;
 #pragma unroll 1
-            for (int c = crank; c < BN / 32; c += cs) {
-                const int col0 = n * BN + c * 32;
+            for (int c = crank + (q >> 1) * cs; c < Cfg::OUT_CHUNKS; c += 2 * cs) {
+                const int col0 = n * (Cfg::OUT_CHUNKS * 32) + c * 32;
                 const int nvalid = min(32, ncols - col0);
-                if (!row_ok || nvalid <= 0) continue;
+                if (rgrow >= args.M || nvalid <= 0) continue;
                 float v[32];
-#pragma unroll 1
-                for (int p = 0; p < cs; ++p) {           // rank order
-                    float4 x[8];
+                if (EPI == EPI_GLU) {
+                    float u[32];
+                    gather_chunk<Cfg::ROWS>(staging, c * 32, rrow, cs, v);
+                    gather_chunk<Cfg::ROWS>(staging, BN / 2 + c * 32, rrow, cs, u);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        x[i] = ld_shared_cluster_f4(mapa_shared(
-                            staging + static_cast<uint32_t>(((c * 8 + i) * Cfg::ROWS + row) * 16), static_cast<uint32_t>(p)));
-                    if (p == 0) {
+                    for (int e = 0; e < 32; ++e) v[e] = act_fn(v[e], args.act) * u[e];
+                } else {
+                    gather_chunk<Cfg::ROWS>(staging, c * 32, rrow, cs, v);
+                    if (bias != nullptr) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            v[4 * i] = x[i].x;
-                            v[4 * i + 1] = x[i].y;
-                            v[4 * i + 2] = x[i].z;
-                            v[4 * i + 3] = x[i].w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            v[4 * i] += x[i].x;
-                            v[4 * i + 1] += x[i].y;
-                            v[4 * i + 2] += x[i].z;
-                            v[4 * i + 3] += x[i].w;
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            if (e < nvalid) v[e] += bf16_to_f32(bias[col0 + e]);
                     }
                 }
-                if (bias != nullptr) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (e < nvalid) v[e] += bf16_to_f32(bias[col0 + e]);
-                }
-                store_chunk(out, args.ldo, args.out_f32, grow, col0, nvalid, v);
+                store_chunk(out, args.ldo, args.out_f32, rgrow, col0, nvalid, v);
             }
             for (int p = 0; p < cs; ++p)
-                if (p != crank) mbar_arrive_cluster(mapa_shared(drained_bar, static_cast<uint32_t>(p)));
+                mbar_arrive_cluster(mapa_shared(drained_bar, static_cast<uint32_t>(p)));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -846,7 +888,6 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
         tmem_dealloc<Cfg::TMEM_COLS>(tmem_base);
     }
 }
-
 
 // ------------------------------------------------------------------ host
 
@@ -986,22 +1027,29 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI>
 static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream_t stream) {
-    using Cfg = SplitCfg<BN, STAGES>;
-    if (d.M > Cfg::ROWS || d.groups != 1 || d.segs % cs != 0 || cs < 2 || cs > 8) return TP_ERR_UNSUPPORTED;
+    using Cfg = SplitCfg<BN, STAGES, EPI>;
+    const int kb_all = a.k_blocks * d.segs;
+    if (d.M > Cfg::ROWS || cs < 2 || cs > 8 || cs > kb_all) return TP_ERR_UNSUPPORTED;
     a.split = cs;
     a.m_tiles = 1;
-    a.n_tiles = static_cast<int>((d.N + BN - 1) / BN);
-    a.total_tiles = a.n_tiles;
+    a.n_tiles = static_cast<int>((d.N + Cfg::OUT_CHUNKS * 32 - 1) / (Cfg::OUT_CHUNKS * 32));
+    a.total_tiles = d.groups * a.n_tiles;
     a.group_m = 1;
     a.a_box_rows = static_cast<int>((d.M + 7) / 8 * 8);
-    a.rotate_k = 1;
-    for (int i = 0; i < d.segs; ++i) {
+    // whole segments per CTA: spread the weight reads by starting each segment's K loop elsewhere
+    a.rotate_k = (d.segs > 1 && d.segs % cs == 0) ? 1 : 0;
+    const int nA = d.segs > 1 ? d.segs : (d.a_per_group ? d.groups : 1);
+    const int nB = d.segs > 1 ? d.segs : d.groups;
+    const int b_box = EPI == EPI_GLU ? BN / 2 : BN;
+    for (int i = 0; i < nA; ++i)
         if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
-        if (!make_map(&a.mapB[i], d.b[i], d.b_rows, d.K, d.ldb, BN)) return TP_ERR_CUDA;
+    for (int i = 0; i < nB; ++i) {
+        const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
+        if (!make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box)) return TP_ERR_CUDA;
     }
-    auto kern = tp_gemm_splitk_kernel<BN, STAGES>;
+    auto kern = tp_gemm_splitk_kernel<BN, STAGES, EPI>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return TP_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1033,28 +1081,32 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
-// Split-K plan for the fused reduce at decode sizes: the tile width (256 or
-// 128) and cluster size (a divisor of the shard count, at most 8) that put
-// the most CTAs to work without exceeding one per SM.  Returns the cluster
-// size, 0 when no split applies.
+// Split-K plan for GEMMs of at most 64 rows: the tile width (256 or 128) and
+// cluster size that put the most CTAs to work, one per SM at most, with at
+// least two K blocks per CTA.  Returns the cluster size, 0 for no split
+// (not the fused reduce, the plain kernel already has a tile for every SM,
+// or K is too short).
 static int split_plan(const GemmDesc& d, int sms, int& bn) {
-    if (d.segs < 2 || d.glu || d.M > 64 || d.groups != 1 || d.split < 0) return 0;
-    if (d.split == 0 && (d.force_bn != 0 || d.pair > 0)) return 0;
+    if (d.M > 64 || d.split < 0) return 0;
+    // automatic only for the fused reduce: with one output per shard the plain kernel has
+    // t times the tiles and was as fast or faster in every measured shape
+    if (d.split == 0 && (d.force_bn != 0 || d.pair > 0 || d.segs < 2)) return 0;
     const bool always = d.split > 0;
+    const int64_t kb_all = (d.K + BK - 1) / BK * d.segs;
+    const int cs_max = static_cast<int>(std::min<int64_t>(8, kb_all / 2));
     int best_cs = 0, best_ctas = 0;
     bn = 0;
     for (int w : {256, 128}) {
-        const int64_t tiles = (d.N + w - 1) / w;
+        const int out_cols = d.glu ? w / 2 : w;
+        const int64_t tiles = d.groups * ((d.N + out_cols - 1) / out_cols);
         if (tiles >= sms && !always) continue;           // the plain kernel already fills the GPU
-        for (int cs = std::min(d.segs, 8); cs >= 2; --cs) {
-            if (d.segs % cs != 0 || (tiles * cs > sms && !always)) continue;
-            const int ctas = static_cast<int>(std::min<int64_t>(tiles * cs, sms));
-            if (ctas > best_ctas) {
-                best_ctas = ctas;
-                best_cs = cs;
-                bn = w;
-            }
-            break;
+        const int cs = always ? cs_max : static_cast<int>(std::min<int64_t>(cs_max, sms / tiles));
+        if (cs < 2) continue;
+        const int ctas = static_cast<int>(std::min<int64_t>(tiles * cs, sms));
+        if (ctas > best_ctas) {
+            best_ctas = ctas;
+            best_cs = cs;
+            bn = w;
         }
     }
     return best_cs;
@@ -1123,8 +1175,12 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     int split_bn = 0;
     const int cs = split_plan(d, sms, split_bn);
     if (cs >= 2) {
-        if (split_bn == 256) return launch_split<256, 4>(a, d, cs, stream);
-        return launch_split<128, 8>(a, d, cs, stream);
+        if (glu) {
+            if (split_bn == 256) return launch_split<256, 4, EPI_GLU>(a, d, cs, stream);
+            return launch_split<128, 8, EPI_GLU>(a, d, cs, stream);
+        }
+        if (split_bn == 256) return launch_split<256, 4, EPI_STORE>(a, d, cs, stream);
+        return launch_split<128, 8, EPI_STORE>(a, d, cs, stream);
     }
     if (d.M <= 64) {   // decode: 64-row A tiles, deeper B rings
         if (glu) {

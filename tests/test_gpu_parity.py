@@ -691,6 +691,50 @@ def test_fused_row_split_k_integer_exact(split_knob, t, n, ks, out):
     exact(f64(y), O.reduce_direct(parts))
 
 
+@pytest.mark.parametrize("split_knob", [(0, 0), (1, 0), (1, 2)], indirect=True)
+@pytest.mark.parametrize("t,n,ks,out", [(3, 5, 512, 100), (2, 64, 1024, 600), (1, 8, 320, 256)])
+def test_split_k_within_shards_integer_exact(split_knob, t, n, ks, out):
+    """K ranges that cut through shards (cluster size not dividing t), the
+    row GEMM writing per-shard partials, and the column GEMM, all through the
+    split-K kernel when it applies."""
+    x = [ints((n, ks), 110 + r) for r in range(t)]
+    w = [ints((out, ks), 120 + r) for r in range(t)]
+    bias = ints((out,), 130, -8, 8)
+    parts = [O.linear(f64(x[r]), f64(w[r]), f64(bias) if r == 0 else None) for r in range(t)]
+    if t > 1:
+        y = tp.tp_linear_row(x, w, bias=bias, mode="fused", y_dtype=torch.float32)
+        p32 = tp.tp_linear_row(x, w, bias=bias, reduce_results=False, partial_dtype=torch.float32)
+        torch.cuda.synchronize()
+        exact(f64(y), O.reduce_direct(parts))
+        for r in range(t):
+            exact(f64(p32[r]), parts[r])
+    # column parallel: shard r of the output is x[0] @ w[r]^T (+ its bias slice)
+    bcol = [ints((out,), 140 + r, -8, 8) for r in range(t)]
+    yc = tp.tp_linear_col(x[0], w, bias=bcol, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    for r in range(t):
+        exact(f64(yc[r]), O.linear(f64(x[0]), f64(w[r]), f64(bcol[r])))
+
+
+@pytest.mark.parametrize("split_knob", [(0, 0), (1, 1)], indirect=True)
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
+@pytest.mark.parametrize("t,n,h,f", [(2, 8, 1024, 3072), (4, 33, 512, 2048), (3, 1, 256, 600)])
+def test_split_k_gated_column(split_knob, act, t, n, h, f):
+    x = normal((n, h), 1.0, 150)
+    wg = normal((f, h), 0.02, 151)
+    wu = normal((f, h), 0.02, 152)
+    fs = f // t
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    hs = tp.tp_linear_col(x, wgu, act=act)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    xf, wgf, wuf = f64(x), f64(wg), f64(wu)
+    for r in range(t):
+        ref = O.glu(O.linear(xf, wgf[r * fs:(r + 1) * fs]), O.linear(xf, wuf[r * fs:(r + 1) * fs]), act)
+        gemm_gate(f64(hs[r]), ref, bf16_out=True)
+
+
 @pytest.mark.parametrize("t", [2, 4, 8])
 @pytest.mark.parametrize("n", [1, 16, 64])
 def test_fused_row_split_k_float_and_deterministic(t, n):
