@@ -88,7 +88,19 @@ __device__ __forceinline__ float act_fn(float g, int act) {
         const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
         return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
     }
-    return g / (1.0f + __expf(-g));  // SiLU
+    // SiLU.  The approximate divide (two special-function ops with the exponential instead of
+    // an IEEE divide's longer sequence) errs by about 2 ulp of fp32, far below the bf16
+    // rounding of the stored H; for g below about -87 the denominator passes 2^126 and the
+    // result is 0, which is also what a bf16 H would hold.
+    return __fdividef(g, 1.0f + __expf(-g));
+}
+
+// Store one output element (bf16 or fp32) at (row, col).
+__device__ __forceinline__ void store_one(void* base, int64_t ldo, int out_f32, int64_t row, int col, float v) {
+    if (out_f32)
+        static_cast<float*>(base)[row * ldo + col] = v;
+    else
+        static_cast<uint16_t*>(base)[row * ldo + col] = f32_to_bf16(v);
 }
 
 // Store 32 consecutive fp32 values of one output row, columns [col0, col0 + nvalid).
@@ -132,6 +144,15 @@ __device__ __forceinline__ void store_chunk(void* base, int64_t ldo, int out_f32
 // The M = 128 MMA then also reads the 64 rows that follow the A tile (the
 // same stage's B tile, already landed) as A rows 64-127; those accumulator
 // rows are never stored.
+//
+// STG_BYTES: the gated decode configurations also keep, per epilogue warp
+// that can hold rows (the first two), a 32-row staging area of one 32-column
+// chunk of gate and up accumulators (65 floats a row: 64 values and a pad
+// that keeps both the row-wise writes and the column-wise reads free of bank
+// conflicts).  A warp with fewer than 32 rows below M stages them there and
+// then has every lane compute one output column over those rows, instead of
+// each row's lane computing all 32 columns (one token of decode: 1
+// activation per lane instead of 32).
 template <int BN, int STAGES, int EPI, int AROWS = BM>
 struct GemmCfg {
     static constexpr int A_BYTES = AROWS * BK * 2;
@@ -139,7 +160,9 @@ struct GemmCfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;                 // two accumulators
     static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int STG_ROW = 65;
+    static constexpr int STG_BYTES = (EPI == EPI_GLU && AROWS < BM) ? 2 * 32 * STG_ROW * 4 : 0;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES;
     static constexpr int OUT_COLS = (EPI == EPI_GLU) ? BN / 2 : BN;   // output columns per tile
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(BN % 16 == 0 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
@@ -157,8 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw_addr);
-    const uint32_t bar_base = base + STAGES * Cfg::STAGE_BYTES;
-    uint8_t* bar_ptr = base_ptr + STAGES * Cfg::STAGE_BYTES;
+    float* stg_base = reinterpret_cast<float*>(base_ptr + STAGES * Cfg::STAGE_BYTES);
+    const uint32_t bar_base = base + STAGES * Cfg::STAGE_BYTES + Cfg::STG_BYTES;
+    uint8_t* bar_ptr = base_ptr + STAGES * Cfg::STAGE_BYTES + Cfg::STG_BYTES;
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
     auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
@@ -186,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
         prefetch_tmap(&args.mapA[0]);
     }
     if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(smem_u32(tmem_slot));
+    __syncwarp();                                      // CTA barriers below are warp-aligned
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -293,11 +318,45 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
             tc_fence_after();
             const int64_t grow = static_cast<int64_t>(m) * BM + row_in_tile;
             const bool row_ok = grow < args.M;
+            // Accumulator rows past M hold whatever the rest of the A tile held; a warp with no
+            // row below M skips the tile, and the others feed 0 through the activation there.
+            const bool warp_live = static_cast<int64_t>(m) * BM + q * 32 < args.M;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             void* out = args.out[g];
             const uint16_t* bias = static_cast<const uint16_t*>(args.bias[g]);
             const int ncols = args.n_valid[g];
-            if (EPI == EPI_GLU) {
+            // rows of this warp below M (1..32 when warp_live)
+            const int64_t left = args.M - (static_cast<int64_t>(m) * BM + q * 32);
+            const int live = left < 32 ? static_cast<int>(left) : 32;
+            if (!warp_live) {
+            } else if (EPI == EPI_GLU && Cfg::STG_BYTES > 0 && live < 32) {
+                // few rows: stage them, then lane j computes column j of every live row
+                float* st = stg_base + (q & 1) * 32 * Cfg::STG_ROW;
+                const int64_t row0 = static_cast<int64_t>(m) * BM + q * 32;
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t rg[32], ru[32];
+                    tmem_ld32(taddr + c * 32, rg);
+                    tmem_ld32(taddr + BN / 2 + c * 32, ru);
+                    tmem_ld_wait();
+                    if (lane < live) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            st[lane * Cfg::STG_ROW + j] = __uint_as_float(rg[j]);
+                            st[lane * Cfg::STG_ROW + 32 + j] = __uint_as_float(ru[j]);
+                        }
+                    }
+                    __syncwarp();
+                    const int col = n * (BN / 2) + c * 32 + lane;
+                    if (col < ncols) {
+#pragma unroll 1
+                        for (int r = 0; r < live; ++r)
+                            store_one(out, args.ldo, args.out_f32, row0 + r, col,
+                                      act_fn(st[r * Cfg::STG_ROW + lane], args.act) * st[r * Cfg::STG_ROW + 32 + lane]);
+                    }
+                    __syncwarp();                         // the next chunk reuses the staging rows
+                }
+            } else if (EPI == EPI_GLU) {
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; ++c) {
                     uint32_t rg[32], ru[32];
@@ -307,7 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                     const int col0 = n * (BN / 2) + c * 32;
                     float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = act_fn(__uint_as_float(rg[j]), args.act) * __uint_as_float(ru[j]);
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = act_fn(row_ok ? __uint_as_float(rg[j]) : 0.0f, args.act) * __uint_as_float(ru[j]);
                     if (row_ok) store_chunk(out, args.ldo, args.out_f32, grow, col0, min(32, ncols - col0), v);
                 }
             } else {
@@ -339,6 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     }
 
     if (aborted) spin_ns(50000);    // let issued TMA copies and MMAs land before teardown
+    // The producer and MMA roles ran on lane 0 alone; the barrier below is
+    // warp-aligned, so each warp first waits for all of its lanes.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) spin_ns(50000);
@@ -418,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
         prefetch_tmap(&args.mapA[0]);
     }
     if (warp == 1) tmem_alloc_pair<Cfg::TMEM_COLS>(smem_u32(tmem_slot));
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     cluster_sync();                                    // both CTAs' barriers exist before any remote use
@@ -517,11 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
             tc_fence_after();
             const int64_t grow = static_cast<int64_t>(m) * Cfg::TILE_M + rank * 128 + row_in_tile;
             const bool row_ok = grow < args.M;
+            const bool warp_live = static_cast<int64_t>(m) * Cfg::TILE_M + rank * 128 + q * 32 < args.M;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             void* out = args.out[g];
             const uint16_t* bias = static_cast<const uint16_t*>(args.bias[g]);
             const int ncols = args.n_valid[g];
-            if (EPI == EPI_GLU) {
+            if (!warp_live) {          // rows past M (ragged last row-tile): nothing to read or store
+            } else if (EPI == EPI_GLU) {
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; ++c) {
                     uint32_t rg[32], ru[32];
@@ -531,7 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                     const int col0 = n * (BN / 2) + c * 32;
                     float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = act_fn(__uint_as_float(rg[j]), args.act) * __uint_as_float(ru[j]);
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = act_fn(row_ok ? __uint_as_float(rg[j]) : 0.0f, args.act) * __uint_as_float(ru[j]);
                     if (row_ok) store_chunk(out, args.ldo, args.out_f32, grow, col0, min(32, ncols - col0), v);
                 }
             } else {
@@ -566,6 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
     }
 
     if (aborted) spin_ns(50000);
+    __syncwarp();                                      // reconverge the lane-0 roles (aligned barriers below)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) spin_ns(50000);
@@ -712,6 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
         prefetch_tmap(&args.mapA[0]);
     }
     if (warp == 1) tmem_alloc<Cfg::TMEM_COLS>(smem_u32(tmem_slot));
+    __syncwarp();
     tc_fence_before();
     cluster_sync();                                      // every CTA's barriers exist before any remote arrive
     tc_fence_after();
@@ -820,8 +889,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             }
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            const bool warp_live = q * 32 < Cfg::ROWS && static_cast<int64_t>(m) * BM + q * 32 < args.M;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < (warp_live ? BN / 32 : 0); ++c) {
                 uint32_t r[32];
                 tmem_ld32(taddr + c * 32, r);
                 tmem_ld_wait();
@@ -879,6 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
     }
 
     if (aborted) spin_ns(50000);
+    __syncwarp();                                        // reconverge the lane-0 roles (aligned barrier below)
     tc_fence_before();
     cluster_sync();                                      // peers may still read this CTA's staging until here
     if (*abort_flag) spin_ns(50000);
@@ -1185,8 +1256,8 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     if (d.M <= 64) {   // decode: 64-row A tiles, deeper B rings
         if (glu) {
             if (best == 256) return launch_cfg<256, 5, EPI_GLU, 64>(a, d, stream);
-            if (best == 128) return launch_cfg<128, 9, EPI_GLU, 64>(a, d, stream);
-            return launch_cfg<64, 14, EPI_GLU, 64>(a, d, stream);
+            if (best == 128) return launch_cfg<128, 8, EPI_GLU, 64>(a, d, stream);
+            return launch_cfg<64, 13, EPI_GLU, 64>(a, d, stream);
         }
         if (best == 256) return launch_cfg<256, 5, EPI_STORE, 64>(a, d, stream);
         if (best == 128) return launch_cfg<128, 9, EPI_STORE, 64>(a, d, stream);
