@@ -62,7 +62,8 @@ struct GemmArgs {
     int segs;                         // K segments accumulated into one tile
     int a_per_group;                  // A map index = group (else 0); with segs > 1 it is the segment
     int glu_up_row;                   // row offset of the up block inside B (gated epilogue)
-    int group_m;                      // tile raster: bands of group_m row-tiles (about 32 MB of A rows)
+    int group_m;                      // tile raster: bands of group_m row-tiles (about kRasterBandMB of A rows)
+    int bands_span_groups;            // 1: a band covers every group's columns (groups share A)
     int a_box_rows;                   // rows of A a TMA box loads (<= 128; fewer when M is small)
     int rotate_k;                     // start each tile's K loop at block (tile mod k_blocks)
     int act;                          // tp_act for the gated epilogue
@@ -70,17 +71,30 @@ struct GemmArgs {
     int* status;                      // library status word
 };
 
+// Tile index -> (group, row-tile, column-tile).  Tiles run in bands of
+// group_m row-tiles; inside a band the row-tile varies fastest, so the band's
+// A rows stay in L2 while its columns of B stream past.  Bands either repeat
+// per group (groups outermost) or, when the groups share A, cover the columns
+// of every group, so A is read once for all groups.
 __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g, int& m, int& n) {
-    const int per_group = a.m_tiles * a.n_tiles;
-    g = tile / per_group;
-    const int l = tile - g * per_group;
-    const int width = a.group_m * a.n_tiles;
+    const int cols = a.bands_span_groups ? a.groups * a.n_tiles : a.n_tiles;
+    const int per_span = a.m_tiles * cols;
+    const int outer = tile / per_span;                   // the group (0 when bands span the groups)
+    const int l = tile - outer * per_span;
+    const int width = a.group_m * cols;
     const int band = l / width;
     const int first_m = band * a.group_m;
     const int gm = min(a.m_tiles - first_m, a.group_m);
     const int r = l - band * width;
     m = first_m + r % gm;
-    n = r / gm;
+    const int col = r / gm;
+    if (a.bands_span_groups) {
+        g = col / a.n_tiles;
+        n = col - g * a.n_tiles;
+    } else {
+        g = outer;
+        n = col;
+    }
 }
 
 __device__ __forceinline__ float act_fn(float g, int act) {
@@ -1006,11 +1020,13 @@ static int sm_count() {
     return n;
 }
 
-// Row-tiles per raster band: as many as keep about 32 MB of A rows (the
-// operand a band re-reads for every column of tiles) resident in L2.
+// Row-tiles per raster band: as many as keep about kRasterBandMB of A rows
+// (the operand a band re-reads for every column of tiles) resident in L2.
+constexpr int kRasterBandMB = 64;
+constexpr int kBandsSpanGroups = 1;
 static int raster_band(int tile_rows, int64_t k_total) {
     const int64_t tile_bytes = static_cast<int64_t>(tile_rows) * k_total * 2;
-    const int64_t band = (32ll << 20) / std::max<int64_t>(tile_bytes, 1);
+    const int64_t band = (static_cast<int64_t>(kRasterBandMB) << 20) / std::max<int64_t>(tile_bytes, 1);
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(band, 64)));
 }
 
@@ -1052,6 +1068,7 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
     using Cfg = PairCfg<STAGES, EPI>;
     a.m_tiles = static_cast<int>((d.M + Cfg::TILE_M - 1) / Cfg::TILE_M);
     a.group_m = raster_band(Cfg::TILE_M, d.K * d.segs);
+    a.bands_span_groups = (kBandsSpanGroups && d.groups > 1 && !d.a_per_group && d.segs == 1) ? 1 : 0;
     a.a_box_rows = 128;
     a.n_tiles = static_cast<int>((d.N + Cfg::OUT_COLS - 1) / Cfg::OUT_COLS);
     a.total_tiles = a.groups * a.m_tiles * a.n_tiles;
