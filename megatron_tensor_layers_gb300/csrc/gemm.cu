@@ -678,15 +678,18 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
 // for the fused reduce the shards in rank order (page "6.2 Tensor-parallel
 // inference", §1: Y = sum_i act(X A_i) B_i), and no partial leaves the chip.
 //
-// Per tile and CTA: wait for the accumulator; wait until every thread of the
-// cluster has read this CTA's staging of the previous tile (`drained`);
-// stage; free the accumulator; release-arrive on the `staged` barrier of
-// every CTA of the cluster (its own included: the four epilogue warps share
-// the reduction, so a row staged by one warp is read by another);
-// acquire-wait on its own `staged`; reduce and store its chunks;
-// release-arrive on every CTA's `drained`.  Waits are bounded like every other wait of the library, and a
-// cluster barrier before exit keeps each CTA's shared memory alive while
-// its peers may still read it.
+// Per tile and CTA: wait for the accumulator; wait until every epilogue warp
+// of the cluster has read this CTA's staging of the previous tile
+// (`drained`); stage; free the accumulator; each warp (lane 0, after a warp
+// barrier) release-arrives on the `staged` barrier of every CTA of the
+// cluster, its own included; acquire-wait on its own `staged`; the 128
+// epilogue threads reduce and store this CTA's chunks, one 4-column group of
+// one row per item with the CS peer loads in flight together; each warp
+// arrives on every CTA's `drained`.  One arrival per warp instead of per
+// thread: with CS = 8 a tile otherwise cost each CTA 1024 remote arrivals
+// on each barrier.  Waits are bounded like every other wait of the library,
+// and a cluster barrier before exit keeps each CTA's shared memory alive
+// while its peers may still read it.
 template <int BN, int STAGES, int EPI>
 struct SplitCfg {
     static constexpr int ROWS = 64;                          // staged rows (M <= 64)
@@ -703,40 +706,49 @@ struct SplitCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-// The 32 fp32 values of accumulator columns [col, col + 32) of `row`, summed
-// over the cluster's CS staged copies in rank order; the loads of two ranks
-// are in flight together.
+// Four fp32 accumulator values (float4 column `f4col` of `row`) summed over
+// the cluster's CS staged copies in rank order; the CS loads are issued
+// together before the sum.
 template <int ROWS>
-__device__ __forceinline__ void gather_chunk(uint32_t staging, int col, int row, int cs, float (&v)[32]) {
-    const uint32_t off = staging + static_cast<uint32_t>(((col / 4) * ROWS + row) * 16);
-#pragma unroll 1
-    for (int p = 0; p < cs; p += 2) {
-        const bool two = p + 1 < cs;
-        float4 x[8], y[8];
+__device__ __forceinline__ float4 gather_f4(uint32_t staging, int f4col, int row, int cs) {
+    const uint32_t off = staging + static_cast<uint32_t>((f4col * ROWS + row) * 16);
+    float4 x[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            x[i] = ld_shared_cluster_f4(mapa_shared(off + i * ROWS * 16, static_cast<uint32_t>(p)));
-            if (two) y[i] = ld_shared_cluster_f4(mapa_shared(off + i * ROWS * 16, static_cast<uint32_t>(p + 1)));
+    for (int p = 0; p < 8; ++p)
+        if (p < cs) x[p] = ld_shared_cluster_f4(mapa_shared(off, static_cast<uint32_t>(p)));
+    float4 v = x[0];
+#pragma unroll
+    for (int p = 1; p < 8; ++p) {
+        if (p < cs) {
+            v.x += x[p].x;
+            v.y += x[p].y;
+            v.z += x[p].z;
+            v.w += x[p].w;
         }
+    }
+    return v;
+}
+
+// Store four consecutive values of one output row, columns [col0, col0 + nvalid).
+__device__ __forceinline__ void store_quad(void* base, int64_t ldo, int out_f32, int64_t row, int col0, int nvalid,
+                                           const float (&v)[4]) {
+    if (out_f32) {
+        float* p = static_cast<float*>(base) + row * ldo + col0;
+        if (nvalid == 4 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+            *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (p == 0) {
-                v[4 * i] = x[i].x;
-                v[4 * i + 1] = x[i].y;
-                v[4 * i + 2] = x[i].z;
-                v[4 * i + 3] = x[i].w;
-            } else {
-                v[4 * i] += x[i].x;
-                v[4 * i + 1] += x[i].y;
-                v[4 * i + 2] += x[i].z;
-                v[4 * i + 3] += x[i].w;
-            }
-            if (two) {
-                v[4 * i] += y[i].x;
-                v[4 * i + 1] += y[i].y;
-                v[4 * i + 2] += y[i].z;
-                v[4 * i + 3] += y[i].w;
-            }
+            for (int e = 0; e < 4; ++e)
+                if (e < nvalid) p[e] = v[e];
+        }
+    } else {
+        uint16_t* p = static_cast<uint16_t*>(base) + row * ldo + col0;
+        if (nvalid == 4 && (reinterpret_cast<uintptr_t>(p) & 7) == 0) {
+            *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < nvalid) p[e] = f32_to_bf16(v[e]);
         }
     }
 }
@@ -781,10 +793,10 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), 128);
         }
-        // every epilogue thread of the cluster (this CTA's own threads too: a row is staged
-        // by one warp and may be reduced by another)
-        mbar_init(staged_bar, cs * 128);
-        mbar_init(drained_bar, cs * 128);
+        // one arrival per epilogue warp of every CTA of the cluster (this CTA's own warps
+        // too: a row staged by one warp is reduced by others)
+        mbar_init(staged_bar, cs * 4);
+        mbar_init(drained_bar, cs * 4);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -919,8 +931,12 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             }
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));                // the accumulator is free for the next tile
-            for (int p = 0; p < cs; ++p)
-                mbar_arrive_cluster(mapa_shared(staged_bar, static_cast<uint32_t>(p)));
+            // The warp's staged rows are visible to the cluster once lane 0's release arrive is:
+            // the warp barrier orders every lane's writes before it.
+            __syncwarp();
+            if (lane == 0)
+                for (int p = 0; p < cs; ++p)
+                    mbar_arrive_cluster(mapa_shared(staged_bar, static_cast<uint32_t>(p)));
             if (!mbar_wait_cluster(staged_bar, j & 1u, abort_flag, args.status)) {
                 aborted = true;
                 break;
@@ -928,33 +944,43 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             void* out = args.out[g];
             const uint16_t* bias = static_cast<const uint16_t*>(args.bias[g]);
             const int ncols = args.n_valid[g];
-            // all four epilogue warps reduce: rows (q & 1) * 32 + lane, the owned chunks split in two halves
-            const int rrow = (q & 1) * 32 + lane;
-            const int64_t rgrow = static_cast<int64_t>(m) * BM + rrow;
+            // The 128 epilogue threads share the reduction: item = (owned chunk, live row,
+            // 4-column group), the 4-column group fastest so that 8 threads store one row's
+            // 32 columns together.  Chunk c belongs to rank c mod CS.
+            const int64_t left = args.M - static_cast<int64_t>(m) * BM;
+            const int rows = left < Cfg::ROWS ? static_cast<int>(left) : Cfg::ROWS;
+            const int owned = (Cfg::OUT_CHUNKS - crank + cs - 1) / cs;
+            const int items = owned * rows * 8;
 #pragma unroll 1
-            for (int c = crank + (q >> 1) * cs; c < Cfg::OUT_CHUNKS; c += 2 * cs) {
-                const int col0 = n * (Cfg::OUT_CHUNKS * 32) + c * 32;
-                const int nvalid = min(32, ncols - col0);
-                if (rgrow >= args.M || nvalid <= 0) continue;
-                float v[32];
+            for (int it = static_cast<int>(threadIdx.x) - 64; it < items; it += 128) {
+                const int i = it & 7;
+                const int rest = it >> 3;
+                const int r = rest % rows;
+                const int c = crank + (rest / rows) * cs;
+                const int col0 = n * (Cfg::OUT_CHUNKS * 32) + c * 32 + 4 * i;
+                if (col0 >= ncols) continue;
+                const int nvalid = min(4, ncols - col0);
+                const float4 a = gather_f4<Cfg::ROWS>(staging, c * 8 + i, r, cs);
+                float v[4] = {a.x, a.y, a.z, a.w};
                 if (EPI == EPI_GLU) {
-                    float u[32];
-                    gather_chunk<Cfg::ROWS>(staging, c * 32, rrow, cs, v);
-                    gather_chunk<Cfg::ROWS>(staging, BN / 2 + c * 32, rrow, cs, u);
+                    const float4 u = gather_f4<Cfg::ROWS>(staging, (BN / 2) / 4 + c * 8 + i, r, cs);
+                    v[0] = act_fn(v[0], args.act) * u.x;
+                    v[1] = act_fn(v[1], args.act) * u.y;
+                    v[2] = act_fn(v[2], args.act) * u.z;
+                    v[3] = act_fn(v[3], args.act) * u.w;
+                } else if (bias != nullptr) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = act_fn(v[e], args.act) * u[e];
-                } else {
-                    gather_chunk<Cfg::ROWS>(staging, c * 32, rrow, cs, v);
-                    if (bias != nullptr) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (e < nvalid) v[e] += bf16_to_f32(bias[col0 + e]);
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        if (e < nvalid) v[e] += bf16_to_f32(bias[col0 + e]);
                 }
-                store_chunk(out, args.ldo, args.out_f32, rgrow, col0, nvalid, v);
+                store_quad(out, args.ldo, args.out_f32, static_cast<int64_t>(m) * BM + r, col0, nvalid, v);
             }
-            for (int p = 0; p < cs; ++p)
-                mbar_arrive_cluster(mapa_shared(drained_bar, static_cast<uint32_t>(p)));
+            // This warp has read (and consumed) its share of every peer's staging; a relaxed
+            // arrive suffices, since no peer needs this warp's output stores ordered.
+            __syncwarp();
+            if (lane == 0)
+                for (int p = 0; p < cs; ++p)
+                    mbar_arrive_cluster_relaxed(mapa_shared(drained_bar, static_cast<uint32_t>(p)));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
