@@ -131,9 +131,12 @@ tp_status tp_linear_col(int t, int64_t n, int64_t in, int64_t out_full, const vo
     return tpk::launch_gemm(d, cs(stream));
 }
 
-tp_status tp_shard_reduce(int t, int64_t count, tp_dtype dtype, const void* const* partials, void* out,
-                          tp_dtype out_dtype, tp_reduce_mode mode, tp_dtype hop_dtype, int replicate,
-                          tp_stream stream) {
+// pdl = 1: the previous launch of the stream is a kernel of the same call (the
+// GEMM that wrote the partials); the reduce may start early and waits for it
+// in the kernel.
+static tp_status shard_reduce_impl(int t, int64_t count, tp_dtype dtype, const void* const* partials, void* out,
+                                   tp_dtype out_dtype, tp_reduce_mode mode, tp_dtype hop_dtype, int replicate,
+                                   int pdl, tp_stream stream) {
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
     TP_CHECK(count >= 0 && partials != nullptr, TP_ERR_INVALID_ARG);
     TP_CHECK(mode == TP_REDUCE_DIRECT || mode == TP_REDUCE_RING, TP_ERR_INVALID_ARG);
@@ -158,14 +161,25 @@ tp_status tp_shard_reduce(int t, int64_t count, tp_dtype dtype, const void* cons
     d.ring = mode == TP_REDUCE_RING;
     d.hop_bf16 = (mode == TP_REDUCE_RING && hop_dtype == TP_BF16) ? 1 : 0;
     d.replicate = replicate;
+    d.pdl = pdl;
     g_collectives++;
     return tpk::launch_shard_reduce(d, cs(stream));
 }
 
-tp_status tp_linear_row(int t, int64_t n, int64_t in_full, int64_t out, const void* const* x, int64_t ldx,
-                        const void* const* w, int64_t ldw, const void* bias, int reduce_results, tp_reduce_mode mode,
-                        tp_dtype partial_dtype, void* const* partials, int64_t ldp, void* y, int64_t ldy,
-                        tp_dtype y_dtype, tp_stream stream) {
+tp_status tp_shard_reduce(int t, int64_t count, tp_dtype dtype, const void* const* partials, void* out,
+                          tp_dtype out_dtype, tp_reduce_mode mode, tp_dtype hop_dtype, int replicate,
+                          tp_stream stream) {
+    return shard_reduce_impl(t, count, dtype, partials, out, out_dtype, mode, hop_dtype, replicate, 0, stream);
+}
+
+// pdl_first = 1: the previous launch of the stream is a kernel of the same
+// call that wrote x (tp_mlp_forward's gate_up GEMM); the GEMM may start early,
+// loading weights until that kernel ends.  The reduce after the GEMM always
+// may.
+static tp_status linear_row_impl(int t, int64_t n, int64_t in_full, int64_t out, const void* const* x, int64_t ldx,
+                                 const void* const* w, int64_t ldw, const void* bias, int reduce_results,
+                                 tp_reduce_mode mode, tp_dtype partial_dtype, void* const* partials, int64_t ldp,
+                                 void* y, int64_t ldy, tp_dtype y_dtype, int pdl_first, tp_stream stream) {
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
     TP_CHECK(n >= 0 && in_full > 0 && out > 0, TP_ERR_INVALID_ARG);
     TP_CHECK(n <= INT32_MAX && out <= INT32_MAX && in_full <= INT32_MAX, TP_ERR_INVALID_ARG);
@@ -208,6 +222,7 @@ tp_status tp_linear_row(int t, int64_t n, int64_t in_full, int64_t out, const vo
     d.ldb = ldw;
     d.b_rows = out;
     d.status = status_ptr();
+    d.pdl = pdl_first;
     apply_knobs(d);
     if (fused) {
         d.groups = 1;
@@ -235,8 +250,16 @@ tp_status tp_linear_row(int t, int64_t n, int64_t in_full, int64_t out, const vo
     d.out_f32 = partial_dtype == TP_F32;
     tp_status st = tpk::launch_gemm(d, cs(stream));
     if (st != TP_OK || !reduce_results) return st;
-    return tp_shard_reduce(t, n * out, partial_dtype, reinterpret_cast<const void* const*>(partials), y, y_dtype,
-                           mode, partial_dtype, 0, stream);
+    return shard_reduce_impl(t, n * out, partial_dtype, reinterpret_cast<const void* const*>(partials), y, y_dtype,
+                             mode, partial_dtype, 0, 1, stream);
+}
+
+tp_status tp_linear_row(int t, int64_t n, int64_t in_full, int64_t out, const void* const* x, int64_t ldx,
+                        const void* const* w, int64_t ldw, const void* bias, int reduce_results, tp_reduce_mode mode,
+                        tp_dtype partial_dtype, void* const* partials, int64_t ldp, void* y, int64_t ldy,
+                        tp_dtype y_dtype, tp_stream stream) {
+    return linear_row_impl(t, n, in_full, out, x, ldx, w, ldw, bias, reduce_results, mode, partial_dtype, partials,
+                           ldp, y, ldy, y_dtype, 0, stream);
 }
 
 size_t tp_mlp_workspace_size(int t, int64_t n, int64_t h, int64_t f, tp_reduce_mode mode, tp_dtype partial_dtype) {
@@ -311,8 +334,8 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, 
     // 2) row-parallel down projection + the all-reduce.
     const void* hx[TP_MAX_SHARDS];
     for (int r = 0; r < t; ++r) hx[r] = hbuf + r * fs;
-    return tp_linear_row(t, n, f, h, hx, f, w_down, ld_down, bias_down, 1, mode, partial_dtype, parts, h, y, h,
-                         y_dtype, stream);
+    return linear_row_impl(t, n, f, h, hx, f, w_down, ld_down, bias_down, 1, mode, partial_dtype, parts, h, y, h,
+                           y_dtype, 1, stream);
 }
 
 tp_status vocab_parallel_embed(int t, int64_t vocab, int64_t h, const int32_t* ids, int64_t n,

@@ -107,6 +107,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// ------------------------------------------------ programmatic dependent launch
+
+// Wait until the grid that precedes this one in the stream has completed and
+// its memory writes are visible.  A launch that did not opt into
+// programmatic serialization has no such grid pending and returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next grid of the stream, if it opted in, be scheduled before this
+// one ends (its CTAs take SMs as this grid's CTAs leave them).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 
 // 2-D tiled bulk-tensor load global -> shared, completing on `bar`.

@@ -229,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) pdl_trigger();       // the next grid of the stream may take freed SMs
 
     const int kb_per_tile = args.k_blocks * args.segs;
     bool aborted = false;
@@ -236,6 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
+            // With a programmatic launch the previous grid of the stream may still be running
+            // (A can be its output).  Waiting before the first load keeps this loop as lean as
+            // it was: at decode sizes the producer's issue rate bounds the weight stream, and a
+            // variant that loaded the first ring of weights before the wait ran 6 % slower.
+            pdl_wait();
             int stage = 0;
             uint32_t phase = 0;
             for (int tile = blockIdx.x; tile < args.total_tiles && !aborted; tile += gridDim.x) {
@@ -501,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
     cluster_sync();                                    // both CTAs' barriers exist before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) pdl_trigger();
 
     const int kb_per_tile = args.k_blocks * args.segs;
     bool aborted = false;
@@ -508,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
+            pdl_wait();                                // A may be the previous grid's output
             int stage = 0;
             uint32_t phase = 0;
             for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
@@ -811,38 +819,64 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
     cluster_sync();                                      // every CTA's barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) pdl_trigger();
     bool aborted = false;
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
+            // rotate_k: each CTA holds whole segments; start each segment's loop elsewhere
+            auto kblock = [&](int kk, int rot, int g, int& kb, int& ai, int& bi) {
+                const int seg = kk / args.k_blocks;
+                kb = kk - seg * args.k_blocks + rot;
+                if (kb >= args.k_blocks) kb -= args.k_blocks;
+                ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                bi = args.segs > 1 ? seg : g;
+            };
+            auto load_b = [&](uint32_t sb, int bi, uint32_t bar, int kb, int n) {
+                if (EPI == EPI_GLU) {
+                    tma_load_2d(sb, &args.mapB[bi], bar, kb * BK, n * (BN / 2));
+                    tma_load_2d(sb + (BN / 2) * 128, &args.mapB[bi], bar, kb * BK, args.glu_up_row + n * (BN / 2));
+                } else {
+                    tma_load_2d(sb, &args.mapB[bi], bar, kb * BK, n * BN);
+                }
+            };
+            // B of the first ring fill before waiting for the previous grid of the stream
+            // (only A can be its output; see the single-CTA kernel)
+            int pre = 0;
+            if (cluster < args.total_tiles) {
+                int g, m, n;
+                tile_coords(args, cluster, g, m, n);
+                const int rot = args.rotate_k ? cluster % args.k_blocks : 0;
+                pre = min(STAGES, kb_hi - kb_lo);
+                for (int i = 0; i < pre; ++i) {
+                    int kb, ai, bi;
+                    kblock(kb_lo + i, rot, g, kb, ai, bi);
+                    mbar_arrive_expect_tx(full_bar(i), args.a_box_rows * 128 + Cfg::B_BYTES);
+                    load_b(base + i * Cfg::STAGE_BYTES + Cfg::A_BYTES, bi, full_bar(i), kb, n);
+                }
+            }
+            pdl_wait();
             int stage = 0;
             uint32_t phase = 0;
             for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
                 int g, m, n;
                 tile_coords(args, tile, g, m, n);
-                // rotate_k: each CTA holds whole segments; start each segment's loop elsewhere
                 const int rot = args.rotate_k ? tile % args.k_blocks : 0;
                 for (int kk = kb_lo; kk < kb_hi; ++kk) {
-                    const int seg = kk / args.k_blocks;
-                    int kb = kk - seg * args.k_blocks + rot;
-                    if (kb >= args.k_blocks) kb -= args.k_blocks;
-                    const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
-                    const int bi = args.segs > 1 ? seg : g;
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
-                        aborted = true;
-                        break;
-                    }
+                    int kb, ai, bi;
+                    kblock(kk, rot, g, kb, ai, bi);
                     const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
-                    const uint32_t sb = sa + Cfg::A_BYTES;
-                    mbar_arrive_expect_tx(full_bar(stage), args.a_box_rows * 128 + Cfg::B_BYTES);
-                    tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);
-                    if (EPI == EPI_GLU) {
-                        tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * (BN / 2));
-                        tma_load_2d(sb + (BN / 2) * 128, &args.mapB[bi], full_bar(stage), kb * BK,
-                                    args.glu_up_row + n * (BN / 2));
+                    if (tile == cluster && kk - kb_lo < pre) {
+                        tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);   // armed, B in flight
                     } else {
-                        tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * BN);
+                        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
+                            aborted = true;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full_bar(stage), args.a_box_rows * 128 + Cfg::B_BYTES);
+                        tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);
+                        load_b(sa + Cfg::A_BYTES, bi, full_bar(stage), kb, n);
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -1056,6 +1090,14 @@ static int raster_band(int tile_rows, int64_t k_total) {
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(band, 64)));
 }
 
+// Programmatic dependent launch for a GEMM that follows another kernel of the
+// same library call (GemmDesc::pdl): the attribute lets it start before that
+// kernel ends; its producer then waits (pdl_wait) before loading A.
+static void set_pdl(cudaLaunchAttribute& at) {
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+}
+
 template <int BN, int STAGES, int EPI, int AROWS = BM>
 static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream) {
     using Cfg = GemmCfg<BN, STAGES, EPI, AROWS>;
@@ -1085,7 +1127,16 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
     const int sms = sm_count();
     if (sms <= 0) return TP_ERR_CUDA;
     const int grid = std::min(a.total_tiles, sms);
-    kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    set_pdl(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = d.pdl ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
@@ -1117,11 +1168,12 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl(attr[1]);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // A persistent grid of pairs that can all be resident at once (per device).
@@ -1137,6 +1189,7 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
     }
     const int clusters = std::min(a.total_tiles, mc);
     cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.numAttrs = d.pdl ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
@@ -1171,11 +1224,12 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl(attr[1]);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // persistent: no more clusters than can be resident at once (cached per device and size)
@@ -1191,6 +1245,7 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
     }
     const int cap = d.split_clusters > 0 ? std::min(mc, d.split_clusters) : mc;
     cfg.gridDim = dim3(cs * std::min(a.total_tiles, cap), 1, 1);
+    cfg.numAttrs = d.pdl ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }

@@ -34,6 +34,11 @@ struct GemmDesc {
     int pair = 0;                        // CTA-pair kernel: -1 never, 0 automatic, 1 always
     int split = 0;                       // split-K kernel (fused reduce, M <= 64): -1 never, 0 automatic, 1 always
     int split_clusters = 0;              // > 0: at most this many split-K clusters resident
+    // 1: the previous launch of the stream is a kernel of the same library call, which
+    // may have written A but writes no B.  The launch may then start before that kernel
+    // ends (programmatic dependent launch); its producer waits for the kernel before
+    // loading A (the split-K kernel loads its first ring of B before that wait).
+    int pdl = 0;
 };
 
 tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream);
@@ -49,6 +54,7 @@ struct ReduceDesc {
     int ring = 0;
     int hop_bf16 = 0;
     int replicate = 0;
+    int pdl = 0;                         // 1: may start before the previous kernel of the call ends
 };
 tp_status launch_shard_reduce(const ReduceDesc& d, cudaStream_t stream);
 

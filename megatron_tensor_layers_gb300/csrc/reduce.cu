@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(256) shard_reduce_kernel(const __grid_constant
     constexpr int MAXT = TP_MAX_SHARDS / G;
     constexpr int VEC = IN_BF16 ? 8 : 4;
     constexpr int EB = IN_BF16 ? 2 : 4;
+    pdl_wait();                                       // the partials may be the previous grid's output
     const int slice = blockIdx.y;
     const int64_t lo = a.ring ? min(static_cast<int64_t>(slice) * a.chunk, a.count) : 0;
     const int64_t hi = a.ring ? min(lo + a.chunk, a.count) : a.count;
@@ -214,7 +215,7 @@ static int sm_count_cached() {
 }
 
 template <bool IN_BF16, int G>
-static void launch_reduce_cfg(const ReduceArgs& a, int64_t count, int t, bool ring, cudaStream_t stream) {
+static void launch_reduce_cfg(const ReduceArgs& a, int64_t count, int t, bool ring, int pdl, cudaStream_t stream) {
     constexpr int VEC = IN_BF16 ? 8 : 4;
     const int slices = ring ? t : 1;
     const int64_t per_slice = (ring ? (count + t - 1) / t : count) / VEC + 1;
@@ -223,7 +224,16 @@ static void launch_reduce_cfg(const ReduceArgs& a, int64_t count, int t, bool ri
     const int64_t resident = static_cast<int64_t>(sms) * resident_blocks<IN_BF16, G>();
     const int64_t want = (per_slice + 256LL * G - 1) / (256LL * G);
     const int gx = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, std::max<int64_t>(1, resident / slices))));
-    shard_reduce_kernel<IN_BF16, G><<<dim3(gx, slices, 1), 256, 0, stream>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, slices, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // start early, wait in the kernel
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaLaunchKernelEx(&cfg, shard_reduce_kernel<IN_BF16, G>, a);
 }
 
 tp_status launch_shard_reduce(const ReduceDesc& d, cudaStream_t stream) {
@@ -241,13 +251,13 @@ tp_status launch_shard_reduce(const ReduceDesc& d, cudaStream_t stream) {
     const bool ring = d.ring != 0;
     // vectors in flight per thread: about 8 loads of 16 bytes whatever t is
     if (d.in_bf16) {
-        if (d.t <= 2) launch_reduce_cfg<true, 4>(a, d.count, d.t, ring, stream);
-        else if (d.t <= 4) launch_reduce_cfg<true, 2>(a, d.count, d.t, ring, stream);
-        else launch_reduce_cfg<true, 1>(a, d.count, d.t, ring, stream);
+        if (d.t <= 2) launch_reduce_cfg<true, 4>(a, d.count, d.t, ring, d.pdl, stream);
+        else if (d.t <= 4) launch_reduce_cfg<true, 2>(a, d.count, d.t, ring, d.pdl, stream);
+        else launch_reduce_cfg<true, 1>(a, d.count, d.t, ring, d.pdl, stream);
     } else {
-        if (d.t <= 2) launch_reduce_cfg<false, 4>(a, d.count, d.t, ring, stream);
-        else if (d.t <= 4) launch_reduce_cfg<false, 2>(a, d.count, d.t, ring, stream);
-        else launch_reduce_cfg<false, 1>(a, d.count, d.t, ring, stream);
+        if (d.t <= 2) launch_reduce_cfg<false, 4>(a, d.count, d.t, ring, d.pdl, stream);
+        else if (d.t <= 4) launch_reduce_cfg<false, 2>(a, d.count, d.t, ring, d.pdl, stream);
+        else launch_reduce_cfg<false, 1>(a, d.count, d.t, ring, d.pdl, stream);
     }
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
