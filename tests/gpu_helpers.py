@@ -70,3 +70,21 @@ def exact(y_gpu: np.ndarray, y_ref: np.ndarray):
         bad = np.argwhere(~same)[:5]
         raise AssertionError(f"{int((~same).sum())} elements differ; first flat idx {bad.ravel().tolist()}: "
                              f"gpu {y_gpu[ok][~same][:5]} ref {y_ref[ok][~same][:5]}")
+
+
+def mlp_rounding_allowance(xf, wg, wu, wd, t, act, partial_bf16):
+    """Per-element bound of the bf16 roundings inside the sharded MLP
+    (intermediate H, partials), from the oracle's own values."""
+    fs = wg.shape[0] // t
+    extra = 0.0
+    parts = []
+    for r in range(t):
+        blk = O.merged_column_shard([wg, wu], t, r)
+        h = O.glu(O.linear(xf, blk[:fs]), O.linear(xf, blk[fs:]), act)
+        bd = O.row_shard(wd, t, r)
+        extra = extra + half_ulp_bf16(h) @ np.abs(bd).T
+        parts.append(O.linear(h, bd))
+    if partial_bf16:
+        for p in parts:
+            extra = extra + half_ulp_bf16(p)
+    return extra

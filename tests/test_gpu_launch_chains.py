@@ -1,0 +1,114 @@
+"""The kernels of one call run as a chain (gate_up GEMM -> down GEMM -> shard
+reduce) in which each later kernel may start before the previous one ends
+(programmatic dependent launch) and waits inside the kernel before reading
+what that kernel wrote.  These tests check the chain where an ordering bug
+would show: replayed from a CUDA graph, back to back without a host sync and
+with the workspace reused, and against the CPU oracle.  Every kernel here is
+deterministic (fixed fold order, no atomics), so repeated results must be
+bit-identical.
+"""
+
+import pytest
+import torch
+
+import oracle as O
+from megatron_tensor_layers_gb300 import _lib as tp
+from megatron_tensor_layers_gb300 import synth
+from megatron_tensor_layers_gb300.build import build
+
+from gpu_helpers import f64, gemm_gate, mlp_rounding_allowance
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+    tp.load()
+    torch.cuda.init()
+    yield
+    assert tp.tp_device_status() == 0
+
+
+def _mlp(t, n, h, f, seed):
+    fs = f // t
+    x = synth.normal_bf16((n, h), 1.0, seed, device=DEV)
+    wg = synth.normal_bf16((f, h), 0.02, seed + 1, device=DEV)
+    wu = synth.normal_bf16((f, h), 0.02, seed + 2, device=DEV)
+    wd = synth.normal_bf16((h, f), 0.02, seed + 3, device=DEV)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds = [wd[:, r * fs:(r + 1) * fs].contiguous() for r in range(t)]
+    return x, wg, wu, wd, wgu, wds
+
+
+def _same_bits(a, b):
+    assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                       b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+
+
+@pytest.mark.parametrize("mode", ["direct", "ring", "fused"])
+@pytest.mark.parametrize("t,n,h,f", [(2, 8, 1024, 3072), (4, 1, 512, 2048), (4, 200, 512, 2048)])
+def test_mlp_graph_replay_bit_identical_to_eager(mode, t, n, h, f):
+    x, wg, wu, wd, wgu, wds = _mlp(t, n, h, f, 300)
+    ws = torch.empty(max(256, tp.tp_mlp_workspace_size(t, n, h, f, mode, torch.bfloat16)), dtype=torch.uint8,
+                     device=DEV)
+    y_graph = torch.empty((n, h), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tp.tp_mlp_forward(x, wgu, wds, mode=mode, workspace=ws, y=y_graph)   # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tp.tp_mlp_forward(x, wgu, wds, mode=mode, workspace=ws, y=y_graph)
+    for seed in (310, 311, 312):
+        x.copy_(synth.normal_bf16((n, h), 1.0, seed, device=DEV))
+        y_graph.zero_()
+        g.replay()
+        y_eager = tp.tp_mlp_forward(x, wgu, wds, mode=mode)
+        torch.cuda.synchronize()
+        _same_bits(y_graph, y_eager)
+    assert tp.tp_device_status() == 0
+
+
+@pytest.mark.parametrize("mode", ["direct", "fused"])
+def test_mlp_back_to_back_calls_share_workspace(mode):
+    """Several calls queued without a host sync, one workspace: each call's
+    first kernel keeps ordinary stream order, so it cannot overwrite H or the
+    partials while the previous call's later kernels still read them."""
+    t, n, h, f = 4, 16, 1024, 4096
+    x, wg, wu, wd, wgu, wds = _mlp(t, n, h, f, 320)
+    xs = [synth.normal_bf16((n, h), 1.0, 330 + i, device=DEV) for i in range(6)]
+    ws = torch.empty(max(256, tp.tp_mlp_workspace_size(t, n, h, f, mode, torch.float32)), dtype=torch.uint8,
+                     device=DEV)
+    ys = [torch.empty((n, h), dtype=torch.float32, device=DEV) for _ in xs]
+    for xi, yi in zip(xs, ys):
+        tp.tp_mlp_forward(xi, wgu, wds, mode=mode, partial_dtype=torch.float32, workspace=ws, y=yi,
+                          y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    wgf, wuf, wdf = f64(wg), f64(wu), f64(wd)
+    for xi, yi in zip(xs, ys):
+        xf = f64(xi)
+        ref = O.mlp_unsharded(xf, wgf, wuf, wdf, None, "silu")
+        gemm_gate(f64(yi), ref, bf16_out=False, extra=mlp_rounding_allowance(xf, wgf, wuf, wdf, t, "silu", False))
+        alone = tp.tp_mlp_forward(xi, wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
+        torch.cuda.synchronize()
+        _same_bits(yi, alone)
+
+
+def test_row_linear_chain_then_reduce_in_every_order():
+    """tp_linear_row with the reduce chained after the GEMM, in both fold
+    orders, equals the GEMM's partials reduced by a separate call."""
+    t, n, ks, out = 4, 40, 256, 520
+    x = [synth.normal_bf16((n, ks), 1.0, 340 + r, device=DEV) for r in range(t)]
+    w = [synth.normal_bf16((out, ks), 0.02, 350 + r, device=DEV) for r in range(t)]
+    for mode in ("direct", "ring"):
+        y = tp.tp_linear_row(x, w, mode=mode, y_dtype=torch.float32, partial_dtype=torch.float32)
+        parts = tp.tp_linear_row(x, w, reduce_results=False, partial_dtype=torch.float32)
+        y2 = tp.tp_shard_reduce(parts, out_dtype=torch.float32, mode=mode)
+        torch.cuda.synchronize()
+        _same_bits(y, y2)

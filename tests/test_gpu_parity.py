@@ -16,6 +16,7 @@ from megatron_tensor_layers_gb300 import synth
 from megatron_tensor_layers_gb300.build import build
 
 from gpu_helpers import exact, f64, gemm_gate, half_ulp_bf16
+from gpu_helpers import mlp_rounding_allowance as _mlp_rounding_allowance
 
 pytestmark = pytest.mark.gpu
 
@@ -204,24 +205,6 @@ def test_shard_reduce_ring_order_observable():
 
 
 # -------------------------------------------------------------------- MLP
-
-def _mlp_rounding_allowance(xf, wg, wu, wd, t, act, partial_bf16):
-    """Per-element bound of the bf16 roundings inside the sharded MLP
-    (intermediate H, partials), from the oracle's own values."""
-    fs = wg.shape[0] // t
-    extra = 0.0
-    parts = []
-    for r in range(t):
-        blk = O.merged_column_shard([wg, wu], t, r)
-        h = O.glu(O.linear(xf, blk[:fs]), O.linear(xf, blk[fs:]), act)
-        bd = O.row_shard(wd, t, r)
-        extra = extra + half_ulp_bf16(h) @ np.abs(bd).T
-        parts.append(O.linear(h, bd))
-    if partial_bf16:
-        for p in parts:
-            extra = extra + half_ulp_bf16(p)
-    return extra
-
 
 @pytest.mark.parametrize("mode", ["direct", "ring", "fused"])
 @pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
