@@ -430,10 +430,17 @@ def _detail_reduce_sweep(torch, tp, dev, hbm):
                 o = torch.empty((n * H,), dtype=dt, device=dev)
                 for mode in ("direct", "ring"):
                     iters = 20 if n == 8192 else 200
-                    s = time_fn(torch, lambda: tp.tp_shard_reduce(ps, out=o, mode=mode), iters)
+                    fn = lambda: tp.tp_shard_reduce(ps, out=o, mode=mode)
+                    s = time_fn(torch, fn, iters)
                     byts = (t + 1) * n * H * es
-                    sweep[f"{'bf16' if es == 2 else 'f32'}_t{t}_n{n}_{mode}"] = {
-                        "us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm}
+                    rec = {"us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm}
+                    if n < 8192:
+                        # small messages: eager calls time the host's launch rate; a CUDA-graph
+                        # replay gives the device latency of one reduce (the all-reduce's alpha)
+                        gs = graph_time(torch, fn, 50)
+                        if gs:
+                            rec["graph_us"] = gs * 1e6
+                    sweep[f"{'bf16' if es == 2 else 'f32'}_t{t}_n{n}_{mode}"] = rec
             del base
     return sweep
 

@@ -112,8 +112,13 @@ def _main(argv: Optional[List[str]] = None) -> None:
         with open(argv[0]) as f:
             line = json.loads(f.read().splitlines()[0])
         measured["hbm_bytes_per_s"] = line["shard_reduce"]["value"] * 1e9
+        sweep = line.get("detail", {}).get("shard_reduce_sweep", {})
+        n1 = sweep.get("bf16_t4_n1_direct", {}).get("graph_us")
+        if n1:   # a one-token reduce is all latency: take it as the per-reduce fixed cost
+            measured["launch_s"] = n1 * 1e-6
     print("\nOne all-reduce of n tokens x 8192 x 2 bytes: NVLink TP=8 bandwidth term vs this library's")
-    print("simulated t=4 reduce on one GB300 (one HBM pass + launch):")
+    print(f"simulated t=4 reduce on one GB300 (one HBM pass at {measured['hbm_bytes_per_s'] / 1e12:.2f} TB/s "
+          f"+ {measured['launch_s'] * 1e6:.2f} us fixed):")
     for r in gb300_table(measured):
         print(f"  n={r['tokens']:>5}  {r['bytes'] / 2**20:8.3f} MiB  NVLink {r['nvlink_tp8_us']:9.2f} us   "
               f"GB300 simulated {r['gb300_sim_us']:9.2f} us")

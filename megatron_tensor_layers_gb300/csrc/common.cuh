@@ -288,6 +288,20 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     }
 }
 
+// Bounded waits for a whole warp whose lanes go on to execute warp-collective
+// instructions (tcgen05.ld, __syncwarp): every lane waits, and the warp gives
+// up as one when any lane gave up, so a lane that saw the phase complete while
+// another timed out never runs a .sync.aligned instruction without it.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+    const bool ok = mbar_wait(bar, parity, abort, status);
+    return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                       int* status) {
+    const bool ok = mbar_wait_cluster(bar, parity, abort, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // 16-byte load from the shared memory of a CTA of the cluster (address from mapa).
 __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
     float4 v;

@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
         for (int tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x) {
             int g, m, n;
             tile_coords(args, tile, g, m, n);
-            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
+            if (!mbar_wait_warp(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
                 aborted = true;
                 break;
             }
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
         for (int tile = cluster; tile < args.total_tiles; tile += nclusters) {
             int g, m, n;
             tile_coords(args, tile, g, m, n);
-            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
+            if (!mbar_wait_warp(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
                 aborted = true;
                 break;
             }
@@ -938,12 +938,12 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             tile_coords(args, tile, g, m, n);
             const int64_t grow = static_cast<int64_t>(m) * BM + row;
             const bool row_ok = row < Cfg::ROWS && grow < args.M;
-            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
+            if (!mbar_wait_warp(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
                 aborted = true;
                 break;
             }
             // every peer has read this CTA's staging of the previous tile
-            if (j > 0 && !mbar_wait_cluster(drained_bar, (j - 1) & 1u, abort_flag, args.status)) {
+            if (j > 0 && !mbar_wait_cluster_warp(drained_bar, (j - 1) & 1u, abort_flag, args.status)) {
                 aborted = true;
                 break;
             }
@@ -971,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             if (lane == 0)
                 for (int p = 0; p < cs; ++p)
                     mbar_arrive_cluster(mapa_shared(staged_bar, static_cast<uint32_t>(p)));
-            if (!mbar_wait_cluster(staged_bar, j & 1u, abort_flag, args.status)) {
+            if (!mbar_wait_cluster_warp(staged_bar, j & 1u, abort_flag, args.status)) {
                 aborted = true;
                 break;
             }
