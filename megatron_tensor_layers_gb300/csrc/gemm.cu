@@ -455,10 +455,16 @@ struct PairCfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    // Store epilogue: per epilogue warp, 32 output rows of 128 bytes (64 bf16 or 32 fp32
+    // columns) plus a 16-byte pad, so that a warp writes whole 128-byte lines of 4 rows per
+    // store instruction instead of one 16-byte piece of 32 rows.
+    static constexpr int STG_PITCH = 144;
+    static constexpr int STG_BYTES = (EPI == EPI_STORE) ? 4 * 32 * STG_PITCH : 0;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES;
     static constexpr int OUT_COLS = (EPI == EPI_GLU) ? BN / 2 : BN;
     static constexpr int TILE_M = 256;
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
 template <int STAGES, int EPI>
@@ -469,8 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw_addr);
-    const uint32_t bar_base = base + STAGES * Cfg::STAGE_BYTES;
-    uint8_t* bar_ptr = base_ptr + STAGES * Cfg::STAGE_BYTES;
+    uint8_t* stg_base = base_ptr + STAGES * Cfg::STAGE_BYTES;
+    const uint32_t bar_base = base + STAGES * Cfg::STAGE_BYTES + Cfg::STG_BYTES;
+    uint8_t* bar_ptr = base_ptr + STAGES * Cfg::STAGE_BYTES + Cfg::STG_BYTES;
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
     auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
@@ -624,12 +631,24 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                     if (row_ok) store_chunk(out, args.ldo, args.out_f32, grow, col0, min(32, ncols - col0), v);
                 }
             } else {
+                // The warp stages whole 128-byte lines of its 32 rows (one 32-column chunk of fp32,
+                // two of bf16) in shared memory and writes 4 rows' lines per store instruction
+                // instead of one 16-byte piece of 32 rows.  Lines follow the absolute address, so
+                // a shard whose columns start 64 bytes into a line (a vocab slice, say) stages
+                // from its second chunk.  Chunks outside a whole valid line, and rows whose
+                // stride is not a multiple of 128 bytes, take the per-row stores.
+                const int es = args.out_f32 ? 4 : 2;
+                const bool lines = ((args.ldo * es) & 127) == 0;
+                uint8_t* st = stg_base + q * 32 * Cfg::STG_PITCH;
+                const int64_t row0 = static_cast<int64_t>(m) * Cfg::TILE_M + rank * 128 + q * 32;
+                int line_col = -1;                     // first column of a half-staged bf16 line
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
+                    const int col0 = n * BN + c * 32;
+                    if (col0 >= ncols) break;
                     uint32_t r[32];
                     tmem_ld32(taddr + c * 32, r);
                     tmem_ld_wait();
-                    const int col0 = n * BN + c * 32;
                     const int nvalid = min(32, ncols - col0);
                     float v[32];
 #pragma unroll
@@ -639,7 +658,43 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                         for (int j = 0; j < 32; ++j)
                             if (j < nvalid) v[j] += bf16_to_f32(bias[col0 + j]);
                     }
-                    if (row_ok) store_chunk(out, args.ldo, args.out_f32, grow, col0, nvalid, v);
+                    const uint32_t off = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(out) + static_cast<uint64_t>(col0) * es) & 127u;
+                    int flush_col = -1;
+                    if (lines && args.out_f32 && off == 0 && nvalid == 32) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4*>(st + lane * Cfg::STG_PITCH + j * 16) =
+                                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        flush_col = col0;
+                    } else if (lines && !args.out_f32 && ((off == 0 && col0 + 64 <= ncols && c + 1 < BN / 32) ||
+                                                          (off == 64 && line_col >= 0))) {
+                        const int half = off == 0 ? 0 : 64;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<uint4*>(st + lane * Cfg::STG_PITCH + half + j * 16) =
+                                make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                           pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                        if (off == 0) {
+                            line_col = col0;
+                        } else {
+                            flush_col = line_col;
+                            line_col = -1;
+                        }
+                    } else if (row_ok) {
+                        store_chunk(out, args.ldo, args.out_f32, grow, col0, nvalid, v);
+                    }
+                    if (flush_col >= 0) {
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int rr = i * 4 + (lane >> 3);
+                            const int64_t gr = row0 + rr;
+                            if (gr < args.M)
+                                *reinterpret_cast<uint4*>(static_cast<char*>(out) + (gr * args.ldo + flush_col) * es + (lane & 7) * 16) =
+                                    *reinterpret_cast<const uint4*>(st + rr * Cfg::STG_PITCH + (lane & 7) * 16);
+                        }
+                        __syncwarp();                 // the next line reuses the staging rows
+                    }
                 }
             }
             // The MMA only needs this warp's TMEM loads finished (wait::ld above) before it
