@@ -287,9 +287,20 @@ __global__ void __launch_bounds__(256) shard_gather_kernel(const __grid_constant
         const char* src = static_cast<const char*>(a.s[r]) + row * bytes;
         char* dst = static_cast<char*>(a.out) + (row * a.total_cols + a.off[r]) * a.elem;
         if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) | bytes) & 15) == 0) {
+            // four 16-byte loads in flight per thread before their stores
             const int64_t nv = bytes / 16;
-            for (int64_t i = threadIdx.x; i < nv; i += blockDim.x)
-                reinterpret_cast<uint4*>(dst)[i] = __ldcs(reinterpret_cast<const uint4*>(src) + i);
+            const uint4* s4 = reinterpret_cast<const uint4*>(src);
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            const int64_t bd = blockDim.x;
+            for (int64_t i = threadIdx.x; i < nv; i += 4 * bd) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (i + u * bd < nv) v[u] = __ldcs(s4 + i + u * bd);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (i + u * bd < nv) __stcs(d4 + i + u * bd, v[u]);
+            }
         } else if (a.elem == 4) {
             for (int64_t i = threadIdx.x; i < a.cols[r]; i += blockDim.x)
                 reinterpret_cast<uint32_t*>(dst)[i] = reinterpret_cast<const uint32_t*>(src)[i];
