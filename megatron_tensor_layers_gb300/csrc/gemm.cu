@@ -29,6 +29,15 @@
 //           they drain one accumulator while the MMA fills the other.
 // Every barrier wait is bounded (1 s); a wait that expires records
 // TP_ERR_TIMEOUT and the CTA unwinds and exits normally.
+//
+// Inside one library call the second and later GEMMs (and the reduce) are
+// launched with programmatic stream serialization: they may start while the
+// previous kernel of the call drains, and their producer executes
+// griddepcontrol.wait before loading anything that kernel may have written.
+// Three kernels share this structure: tp_gemm_kernel (one CTA per tile),
+// tp_gemm_pair_kernel (256 x 256 tiles on a CTA pair, cta_group::2) and
+// tp_gemm_splitk_kernel (the K loop of a decode-sized tile split over a
+// cluster, accumulators added over distributed shared memory).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
