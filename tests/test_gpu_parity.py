@@ -496,6 +496,27 @@ def test_pair_kernel_lm_head(pair_on, t, V, n, h):
     exact(f64(logits[rows]), O.lm_head_unsharded(f64(x[rows]), f64(table)))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_pair_kernel_line_staged_stores(pair_on, dtype):
+    """The CTA-pair store epilogue writes whole 128-byte output lines through
+    shared memory when the row pitch allows it.  Logits in a buffer with a
+    320-column pitch: with bf16 the second shard starts 64 bytes into a line
+    (its first chunk falls back to per-row stores), every shard ends in a
+    partial line, the last row-tile is ragged; the pad columns must stay
+    untouched and every logit exact."""
+    t, V, n, h, pitch = 3, 288, 520, 128, 320
+    x = ints((n, h), 260)
+    table = ints((V, h), 261)
+    canary = -12345.0
+    buf = torch.full((n, pitch), canary, dtype=dtype, device=DEV)
+    logits = buf[:, :V]
+    tp.lm_head_sharded(x, _table_shards(table, t), V, logits=logits, out_dtype=dtype)
+    torch.cuda.synchronize()
+    exact(f64(logits.contiguous()), O.lm_head_unsharded(f64(x), f64(table)))
+    assert bool(torch.all(buf[:, V:] == canary).item())
+    assert tp.tp_device_status() == 0
+
+
 def test_pair_kernel_gated(pair_on):
     t, n, h, fs = 2, 600, 320, 200
     x = normal((n, h), 1.0, 220)
