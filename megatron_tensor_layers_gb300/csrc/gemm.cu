@@ -260,12 +260,17 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                 // starting each tile's K loop (each segment's, with segments) elsewhere spreads
                 // those reads over L2 and the weight reads over the DRAM channels.
                 const int rot = args.rotate_k ? tile % args.k_blocks : 0;
+                // (segment, block) advanced incrementally: no division in the issue loop
+                int seg = 0, kin = 0;
                 for (int kk = 0; kk < kb_per_tile; ++kk) {
-                    const int seg = kk / args.k_blocks;
-                    int kb = kk - seg * args.k_blocks + rot;
+                    int kb = kin + rot;
                     if (kb >= args.k_blocks) kb -= args.k_blocks;
                     const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
                     const int bi = args.segs > 1 ? seg : g;
+                    if (++kin == args.k_blocks) {
+                        kin = 0;
+                        ++seg;
+                    }
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
                         aborted = true;
                         break;
@@ -540,11 +545,15 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                 const int a_row = m * Cfg::TILE_M + static_cast<int>(rank) * 128;
                 const int b_row = (EPI == EPI_GLU) ? (rank == 0 ? n * 128 : args.glu_up_row + n * 128)
                                                    : n * BN + static_cast<int>(rank) * 128;
+                int seg = 0, kb = 0;                   // (segment, block), advanced without division
                 for (int kk = 0; kk < kb_per_tile; ++kk) {
-                    const int seg = kk / args.k_blocks;
-                    const int kb = kk - seg * args.k_blocks;
                     const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
                     const int bi = args.segs > 1 ? seg : g;
+                    const int kcol = kb * BK;
+                    if (++kb == args.k_blocks) {
+                        kb = 0;
+                        ++seg;
+                    }
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
                         aborted = true;
                         break;
@@ -553,8 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                     const uint32_t sb = sa + Cfg::A_BYTES;
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
                     const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
-                    tma_load_2d_pair(sa, &args.mapA[ai], leader_full, kb * BK, a_row);
-                    tma_load_2d_pair(sb, &args.mapB[bi], leader_full, kb * BK, b_row);
+                    tma_load_2d_pair(sa, &args.mapA[ai], leader_full, kcol, a_row);
+                    tma_load_2d_pair(sb, &args.mapB[bi], leader_full, kcol, b_row);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -927,9 +936,16 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
                 int g, m, n;
                 tile_coords(args, tile, g, m, n);
                 const int rot = args.rotate_k ? tile % args.k_blocks : 0;
+                int seg = kb_lo / args.k_blocks, kin = kb_lo - (kb_lo / args.k_blocks) * args.k_blocks;
                 for (int kk = kb_lo; kk < kb_hi; ++kk) {
-                    int kb, ai, bi;
-                    kblock(kk, rot, g, kb, ai, bi);
+                    int kb = kin + rot;                    // (segment, block) advanced without division
+                    if (kb >= args.k_blocks) kb -= args.k_blocks;
+                    const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                    const int bi = args.segs > 1 ? seg : g;
+                    if (++kin == args.k_blocks) {
+                        kin = 0;
+                        ++seg;
+                    }
                     const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
                     if (tile == cluster && kk - kb_lo < pre) {
                         tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);   // armed, B in flight
