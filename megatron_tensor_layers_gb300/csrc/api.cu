@@ -121,6 +121,7 @@ tp_status tp_linear_col(int t, int64_t n, int64_t in, int64_t out_full, const vo
     d.ldo = ldy;
     d.out_f32 = y_dtype == TP_F32;
     d.status = status_ptr();
+    d.pdl = 2;                       // may overlap the previous kernel's tail; loads wait for it
     apply_knobs(d);
     for (int r = 0; r < t; ++r) {
         d.b[r] = w[r];
@@ -131,9 +132,9 @@ tp_status tp_linear_col(int t, int64_t n, int64_t in, int64_t out_full, const vo
     return tpk::launch_gemm(d, cs(stream));
 }
 
-// pdl = 1: the previous launch of the stream is a kernel of the same call (the
-// GEMM that wrote the partials); the reduce may start early and waits for it
-// in the kernel.
+// pdl = 1: the reduce may start before the previous kernel of the stream ends
+// (programmatic dependent launch); every thread waits for that kernel before
+// its first load.
 static tp_status shard_reduce_impl(int t, int64_t count, tp_dtype dtype, const void* const* partials, void* out,
                                    tp_dtype out_dtype, tp_reduce_mode mode, tp_dtype hop_dtype, int replicate,
                                    int pdl, tp_stream stream) {
@@ -169,13 +170,13 @@ static tp_status shard_reduce_impl(int t, int64_t count, tp_dtype dtype, const v
 tp_status tp_shard_reduce(int t, int64_t count, tp_dtype dtype, const void* const* partials, void* out,
                           tp_dtype out_dtype, tp_reduce_mode mode, tp_dtype hop_dtype, int replicate,
                           tp_stream stream) {
-    return shard_reduce_impl(t, count, dtype, partials, out, out_dtype, mode, hop_dtype, replicate, 0, stream);
+    return shard_reduce_impl(t, count, dtype, partials, out, out_dtype, mode, hop_dtype, replicate, 1, stream);
 }
 
 // pdl_first = 1: the previous launch of the stream is a kernel of the same
-// call that wrote x (tp_mlp_forward's gate_up GEMM); the GEMM may start early,
-// loading weights until that kernel ends.  The reduce after the GEMM always
-// may.
+// call that wrote x (tp_mlp_forward's gate_up GEMM), so the split-K GEMM may
+// load weights before waiting for it; 0: the first kernel of the call, which
+// loads nothing before that wait.  Every launch may start early.
 static tp_status linear_row_impl(int t, int64_t n, int64_t in_full, int64_t out, const void* const* x, int64_t ldx,
                                  const void* const* w, int64_t ldw, const void* bias, int reduce_results,
                                  tp_reduce_mode mode, tp_dtype partial_dtype, void* const* partials, int64_t ldp,
@@ -222,7 +223,7 @@ static tp_status linear_row_impl(int t, int64_t n, int64_t in_full, int64_t out,
     d.ldb = ldw;
     d.b_rows = out;
     d.status = status_ptr();
-    d.pdl = pdl_first;
+    d.pdl = pdl_first ? 1 : 2;
     apply_knobs(d);
     if (fused) {
         d.groups = 1;
@@ -323,6 +324,7 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, 
     c.ldo = f;
     c.out_f32 = 0;
     c.status = status_ptr();
+    c.pdl = 2;
     apply_knobs(c);
     for (int r = 0; r < t; ++r) {
         c.b[r] = w_gate_up[r];
@@ -405,6 +407,7 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab, const void
     d.out_f32 = out_dtype == TP_F32;
     d.ldo = logits != nullptr ? ldl : 0;
     d.status = status_ptr();
+    d.pdl = 2;
     apply_knobs(d);
     int g = 0;
     for (int r = 0; r < t; ++r) {

@@ -77,6 +77,7 @@ struct GemmArgs {
     int rotate_k;                     // start each tile's K loop at block (tile mod k_blocks)
     int act;                          // tp_act for the gated epilogue
     int split;                        // split-K kernel: CTAs per cluster sharing one output tile
+    int pdl_prefetch;                 // 1: B may be loaded before waiting for the previous grid
     int* status;                      // library status word
 };
 
@@ -914,10 +915,10 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
                     tma_load_2d(sb, &args.mapB[bi], bar, kb * BK, n * BN);
                 }
             };
-            // B of the first ring fill before waiting for the previous grid of the stream
-            // (only A can be its output; see the single-CTA kernel)
+            // B of the first ring fill before waiting for the previous grid of the stream, when
+            // that grid is a kernel of the same call (only A can be its output)
             int pre = 0;
-            if (cluster < args.total_tiles) {
+            if (args.pdl_prefetch && cluster < args.total_tiles) {
                 int g, m, n;
                 tile_coords(args, cluster, g, m, n);
                 const int rot = args.rotate_k ? cluster % args.k_blocks : 0;
@@ -1170,9 +1171,9 @@ static int raster_band(int tile_rows, int64_t k_total) {
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(band, 64)));
 }
 
-// Programmatic dependent launch for a GEMM that follows another kernel of the
-// same library call (GemmDesc::pdl): the attribute lets it start before that
-// kernel ends; its producer then waits (pdl_wait) before loading A.
+// Programmatic dependent launch (GemmDesc::pdl): the attribute lets the GEMM
+// start before the previous kernel of the stream ends; its producer waits
+// (pdl_wait) before loading what that kernel may have written.
 static void set_pdl(cudaLaunchAttribute& at) {
     at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at.val.programmaticStreamSerializationAllowed = 1;
@@ -1389,6 +1390,7 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     a.glu_up_row = static_cast<int>(d.glu_up_row);
     a.act = d.act;
     a.status = d.status;
+    a.pdl_prefetch = d.pdl == 1 ? 1 : 0;
     if (d.M == 0 || d.N == 0) return TP_OK;
     // tile indices are 32-bit in the kernels
     if (static_cast<int64_t>(d.groups) * ((d.M + 127) / 128) * ((d.N + 63) / 64) > INT32_MAX) return TP_ERR_UNSUPPORTED;

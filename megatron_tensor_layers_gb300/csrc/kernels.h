@@ -34,10 +34,12 @@ struct GemmDesc {
     int pair = 0;                        // CTA-pair kernel: -1 never, 0 automatic, 1 always
     int split = 0;                       // split-K kernel (fused reduce, M <= 64): -1 never, 0 automatic, 1 always
     int split_clusters = 0;              // > 0: at most this many split-K clusters resident
-    // 1: the previous launch of the stream is a kernel of the same library call, which
-    // may have written A but writes no B.  The launch may then start before that kernel
-    // ends (programmatic dependent launch); its producer waits for the kernel before
-    // loading A (the split-K kernel loads its first ring of B before that wait).
+    // Programmatic dependent launch: the launch may start before the previous kernel of
+    // the stream ends, and its producer waits for that kernel (griddepcontrol.wait) before
+    // loading.  1: the previous kernel belongs to the same library call and writes no B,
+    // so the split-K kernel may load its first ring of B before the wait; 2: the first
+    // kernel of a call, whose predecessor may have written anything: nothing is loaded
+    // before the wait.
     int pdl = 0;
 };
 

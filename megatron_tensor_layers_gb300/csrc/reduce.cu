@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(256) shard_reduce_kernel(const __grid_constant
     constexpr int VEC = IN_BF16 ? 8 : 4;
     constexpr int EB = IN_BF16 ? 2 : 4;
     pdl_wait();                                       // the partials may be the previous grid's output
+    if (threadIdx.x == 0) pdl_trigger();              // the next kernel of the stream may take freed SMs
     const int slice = blockIdx.y;
     const int64_t lo = a.ring ? min(static_cast<int64_t>(slice) * a.chunk, a.count) : 0;
     const int64_t hi = a.ring ? min(lo + a.chunk, a.count) : a.count;

@@ -8,6 +8,7 @@ deterministic (fixed fold order, no atomics), so repeated results must be
 bit-identical.
 """
 
+import numpy as np
 import pytest
 import torch
 
@@ -77,8 +78,10 @@ def test_mlp_graph_replay_bit_identical_to_eager(mode, t, n, h, f):
 @pytest.mark.parametrize("mode", ["direct", "fused"])
 def test_mlp_back_to_back_calls_share_workspace(mode):
     """Several calls queued without a host sync, one workspace: each call's
-    first kernel keeps ordinary stream order, so it cannot overwrite H or the
-    partials while the previous call's later kernels still read them."""
+    first kernel may start while the previous call's last kernel drains, but
+    it loads nothing before that kernel has finished, and it writes H only
+    after those loads, so it cannot overwrite H or the partials while the
+    previous call's kernels still read them."""
     t, n, h, f = 4, 16, 1024, 4096
     x, wg, wu, wd, wgu, wds = _mlp(t, n, h, f, 320)
     xs = [synth.normal_bf16((n, h), 1.0, 330 + i, device=DEV) for i in range(6)]
@@ -112,3 +115,36 @@ def test_row_linear_chain_then_reduce_in_every_order():
         y2 = tp.tp_shard_reduce(parts, out_dtype=torch.float32, mode=mode)
         torch.cuda.synchronize()
         _same_bits(y, y2)
+
+
+def test_inputs_and_weights_written_just_before_a_call():
+    """Every call's first kernel may start while the previous kernel of the
+    stream drains, so it must not read anything (weights included) before
+    waiting for it.  Here a torch kernel rewrites the input or the weights
+    immediately before each call, with no host sync in between; every result
+    must reflect the data just written."""
+    t, n, k, os_ = 2, 24, 512, 384
+    x = synth.int_valued((n, k), -3, 3, 360, dtype=torch.bfloat16, device=DEV)
+    w = [synth.int_valued((os_, k), -3, 3, 361 + r, dtype=torch.bfloat16, device=DEV) for r in range(t)]
+    xs = [synth.int_valued((n, k), -3, 3, 370 + i, dtype=torch.bfloat16, device=DEV) for i in range(3)]
+    ws = [[synth.int_valued((os_, k), -3, 3, 380 + 10 * i + r, dtype=torch.bfloat16, device=DEV) for r in range(t)]
+          for i in range(3)]
+    outs = []
+    for i in range(3):
+        x.copy_(xs[i])
+        for r in range(t):
+            w[r].copy_(ws[i][r])
+        outs.append([o.clone() for o in tp.tp_linear_col(x, w, y_dtype=torch.float32)])
+        # the fused row GEMM (split-K kernel at this size) as the first kernel of a call
+        x2 = [xi.contiguous() for xi in torch.chunk(x, t, dim=1)]
+        outs[-1].append(tp.tp_linear_row(x2, [wr[:, :k // t].contiguous() for wr in w], mode="fused",
+                                         y_dtype=torch.float32).clone())
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    for i in range(3):
+        xf = f64(xs[i])
+        for r in range(t):
+            assert np.array_equal(f64(outs[i][r]), O.linear(xf, f64(ws[i][r])))
+        ref = O.reduce_direct([O.linear(f64(xs[i][:, r * (k // t):(r + 1) * (k // t)]),
+                                        f64(ws[i][r][:, :k // t])) for r in range(t)])
+        assert np.array_equal(f64(outs[i][t]), ref)
