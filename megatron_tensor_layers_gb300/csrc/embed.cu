@@ -132,6 +132,8 @@ tp_status launch_vocab_embed(const EmbedDesc& d, cudaStream_t stream) {
     }
     const int64_t resident = static_cast<int64_t>(std::max(sms, 1)) * std::max(occ, 1);
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, resident)));
+    // Launched in plain stream order: with programmatic launch, back-to-back lookups of
+    // 4096 ids measured 3.33 us per call instead of 2.97.
     if (d.bf16)
         vocab_embed_kernel<true><<<grid, 256, 0, stream>>>(a);
     else

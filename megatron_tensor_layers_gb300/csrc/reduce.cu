@@ -279,6 +279,8 @@ struct GatherArgs {
 // One thread block per (row, shard) segment: copy the shard's row into its
 // column slice of the output row, 16 bytes at a time when both ends allow.
 __global__ void __launch_bounds__(256) shard_gather_kernel(const __grid_constant__ GatherArgs a) {
+    pdl_wait();                                       // the shards may be the previous kernel's output
+    if (threadIdx.x == 0) pdl_trigger();
     const int64_t nseg = a.rows * a.t;
     for (int64_t seg = blockIdx.x; seg < nseg; seg += gridDim.x) {
         const int r = static_cast<int>(seg % a.t);
@@ -330,8 +332,8 @@ tp_status launch_shard_gather(const GatherDesc& d, cudaStream_t stream) {
     const int sms = std::max(1, sm_count_cached());
     const int64_t nseg = d.rows * d.t;
     const int grid = static_cast<int>(std::min<int64_t>(nseg, static_cast<int64_t>(sms) * 16));
-    shard_gather_kernel<<<grid, 256, 0, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+    const cudaError_t e = launch_pdl(shard_gather_kernel, dim3(grid), dim3(256), 0, stream, a);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ probe

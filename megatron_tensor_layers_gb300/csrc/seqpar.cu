@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(kSeqThreads, 4) seqpar_rmsnorm_kernel(const __
     constexpr int EB = IN_BF16 ? 2 : 4;
     extern __shared__ float xrow[];             // the row in fp32, h floats
     __shared__ float warp_sums[kSeqThreads / 32];
+    pdl_wait();                                 // the partials may be the previous kernel's output
+    if (threadIdx.x == 0) pdl_trigger();
     const int64_t nvec = a.h / VEC;
     for (int64_t row = blockIdx.x; row < a.n; row += gridDim.x) {
         const int owner = static_cast<int>(row / a.rows_per);
@@ -192,8 +194,8 @@ static tp_status launch_seqpar_cfg(const SeqParArgs& a, int64_t n, size_t smem, 
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSeqThreads, smem);
     const int64_t resident = static_cast<int64_t>(std::max(sms, 1)) * std::max(per_sm, 1);
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(n, resident)));
-    kern<<<grid, kSeqThreads, smem, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kSeqThreads), smem, stream, a);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
 tp_status launch_seqpar_rmsnorm(const SeqParDesc& d, cudaStream_t stream) {
