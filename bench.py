@@ -42,10 +42,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the gate_up GEMM at the bench
 # size, from ncu (dram__bytes_read.sum + dram__bytes_write.sum); None until
 # taken for the current kernel.
-TRAFFIC_GLU_FULL = 8617782016 + 468312320
+TRAFFIC_GLU_FULL = 9201524992 + 468526336
 TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the CTA-pair gate_up "
                 "GEMM at the bench size (1-pass capture, profiles/tp_gemm_pair_traffic_t4_n8192.md); "
-                "5.9x the algorithmic bytes: weights streamed once per 64 MB raster band of X rows, "
+                "6.3x the algorithmic bytes: weights streamed once per 64 MB raster band of X rows, "
                 "band rows re-read from DRAM between waves")
 
 
