@@ -30,6 +30,14 @@
  *    Shard counts must be in 1..TP_MAX_SHARDS, else TP_ERR_INVALID_ARG.  Splits that do not divide evenly return
  *    TP_ERR_NOT_DIVISIBLE (the `divide` assertion of the same page, §1).
  *  - GEMM operands (x, w) are bfloat16; accumulation is float32.
+ *  - Stream order is kept as the caller sees it.  The GEMM, shard-reduce,
+ *    gather and reduce-scatter kernels are launched with programmatic stream
+ *    serialization: one may be scheduled while the previous kernel of the
+ *    stream is still draining, but it reads nothing, and so writes nothing,
+ *    before that kernel has finished and its writes are visible.  A caller's
+ *    kernel that follows a library call starts after the call's last kernel
+ *    unless the caller opts into the same mechanism.  Launches of this kind
+ *    are captured into CUDA graphs like any other.
  *  - Nothing here is thread-safe against concurrent calls that share output
  *    buffers; calls on different streams with disjoint buffers are fine.
  */
