@@ -280,10 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                     const uint32_t sb = sa + Cfg::A_BYTES;
                     mbar_arrive_expect_tx(full_bar(stage), args.a_box_rows * 128 + Cfg::B_BYTES);
                     tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);
-                    if (EPI == EPI_GLU) {
-                        tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * (BN / 2));
-                        tma_load_2d(sb + (BN / 2) * 128, &args.mapB[bi], full_bar(stage), kb * BK,
-                                    args.glu_up_row + n * (BN / 2));
+                    if (EPI == EPI_GLU) {   // gate rows and the same rows of up, one 3-D box
+                        tma_load_3d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * (BN / 2), 0);
                     } else {
                         tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * BN);
                     }
@@ -908,9 +906,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
                 bi = args.segs > 1 ? seg : g;
             };
             auto load_b = [&](uint32_t sb, int bi, uint32_t bar, int kb, int n) {
-                if (EPI == EPI_GLU) {
-                    tma_load_2d(sb, &args.mapB[bi], bar, kb * BK, n * (BN / 2));
-                    tma_load_2d(sb + (BN / 2) * 128, &args.mapB[bi], bar, kb * BK, args.glu_up_row + n * (BN / 2));
+                if (EPI == EPI_GLU) {   // gate rows and the same rows of up, one 3-D box
+                    tma_load_3d(sb, &args.mapB[bi], bar, kb * BK, n * (BN / 2), 0);
                 } else {
                     tma_load_2d(sb, &args.mapB[bi], bar, kb * BK, n * BN);
                 }
@@ -1179,6 +1176,22 @@ static void set_pdl(cudaLaunchAttribute& at) {
     at.val.programmaticStreamSerializationAllowed = 1;
 }
 
+// Tensor map of a gated B block [2 * half_rows, cols] (gate rows, then the same
+// rows of up) as a 3-D tensor {cols, half_rows, 2}: one box of box_rows rows of
+// each half lands as the gate tile followed by the up tile, in one TMA load.
+static bool make_map_glu(CUtensorMap* m, const void* ptr, int64_t half_rows, int64_t cols, int64_t ld, int box_rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(half_rows), 2};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(half_rows * ld) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int BN, int STAGES, int EPI, int AROWS = BM>
 static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream) {
     using Cfg = GemmCfg<BN, STAGES, EPI, AROWS>;
@@ -1200,7 +1213,9 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
         if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
     for (int i = 0; i < nB; ++i) {
         const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
-        if (!make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box)) return TP_ERR_CUDA;
+        const bool ok = (EPI == EPI_GLU) ? make_map_glu(&a.mapB[i], d.b[i], d.glu_up_row, d.K, d.ldb, b_box)
+                                         : make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box);
+        if (!ok) return TP_ERR_CUDA;
     }
     auto kern = tp_gemm_kernel<BN, STAGES, EPI, AROWS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
@@ -1295,7 +1310,9 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
         if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
     for (int i = 0; i < nB; ++i) {
         const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
-        if (!make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box)) return TP_ERR_CUDA;
+        const bool ok = (EPI == EPI_GLU) ? make_map_glu(&a.mapB[i], d.b[i], d.glu_up_row, d.K, d.ldb, b_box)
+                                         : make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box);
+        if (!ok) return TP_ERR_CUDA;
     }
     auto kern = tp_gemm_splitk_kernel<BN, STAGES, EPI>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
