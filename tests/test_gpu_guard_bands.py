@@ -118,3 +118,31 @@ def test_reduce_embed_seqpar_stay_inside(dtype, mode):
     assert bool(torch.all(eb[n * h:] == CANARY_BF16).item())
     assert bool(torch.all(rb[n2 * h2:] == CANARY_BF16).item())
     assert bool(torch.all(nb[n2 * h2:] == CANARY_BF16).item())
+
+
+@pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
+def test_split_k_cluster_outputs_stay_inside(ydt):
+    """The split-K cluster kernel (decode-sized rows) writes through its own
+    reduction epilogue: the fused row GEMM, and with the split forced the
+    gated column GEMM and per-shard partials."""
+    t, n, ks, out = 3, 37, 136, 200
+    xs = [ints((n, ks), 50 + r) for r in range(t)]
+    ws = [ints((out, ks), 60 + r) for r in range(t)]
+    yf = guarded(n, out, ydt)
+    tp.tp_linear_row(xs, ws, mode="fused", y=yf[0], y_dtype=ydt)
+    tp.tp_set_gemm_split(1, 0)
+    try:
+        x = ints((n, 256), 70)
+        wgu = [ints((2 * 72, 256), 71 + r) for r in range(t)]
+        hg = [guarded(n, 72, ydt) for _ in range(t)]
+        tp.tp_linear_col(x, wgu, act="silu", y=[o[0] for o in hg], y_dtype=ydt)
+        xp = [ints((n, 264), 80 + r) for r in range(t)]        # 5 K blocks: two CTAs per cluster
+        wp = [ints((out, 264), 90 + r) for r in range(t)]
+        parts = [guarded(n, out, torch.float32) for _ in range(t)]
+        tp.tp_linear_row(xp, wp, reduce_results=False, partials=[p[0] for p in parts], partial_dtype=torch.float32)
+        torch.cuda.synchronize()
+    finally:
+        tp.tp_set_gemm_split(0, 0)
+    assert tp.tp_device_status() == 0
+    for o in [yf] + hg + parts:
+        assert intact(o[1], o[2], o[3])
