@@ -148,3 +148,33 @@ def test_inputs_and_weights_written_just_before_a_call():
         ref = O.reduce_direct([O.linear(f64(xs[i][:, r * (k // t):(r + 1) * (k // t)]),
                                         f64(ws[i][r][:, :k // t])) for r in range(t)])
         assert np.array_equal(f64(outs[i][t]), ref)
+
+
+def test_event_wait_still_orders_a_programmatic_launch():
+    """A call's first kernel may start before the previous kernel of its
+    stream ends, but a cross-stream event wait queued between them still
+    holds it: here the input arrives behind a 1 GiB host-to-device copy on
+    another stream, long after the short GEMM before it has finished, and
+    the GEMM after the event wait must see the new input."""
+    t, n, k, os_ = 2, 16, 256, 128
+    w = [synth.int_valued((os_, k), -3, 3, 390 + r, dtype=torch.bfloat16, device=DEV) for r in range(t)]
+    x_old = synth.int_valued((n, k), -3, 3, 393, dtype=torch.bfloat16, device=DEV)
+    x_new_host = synth.int_valued((n, k), -3, 3, 394, dtype=torch.bfloat16).pin_memory()
+    big_host = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    big_dev = torch.empty(1 << 30, dtype=torch.uint8, device=DEV)
+    x = x_old.clone()
+    copy = torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(copy):
+        big_dev.copy_(big_host, non_blocking=True)           # about a millisecond or more
+        x.copy_(x_new_host, non_blocking=True)
+        ev.record(copy)
+    tp.tp_linear_col(x_old, w, y_dtype=torch.float32)       # short kernel, done long before the copy
+    torch.cuda.current_stream().wait_event(ev)
+    y = tp.tp_linear_col(x, w, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    xf = f64(x_new_host.to(DEV))
+    for r in range(t):
+        assert np.array_equal(f64(y[r]), O.linear(xf, f64(w[r])))
