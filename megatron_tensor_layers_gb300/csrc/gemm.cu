@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
 // the single-CTA kernel.  Both CTAs' loads complete on the even CTA's
 // full barrier; MMA completion is multicast to both CTAs' stage and
 // accumulator barriers; both epilogues report back to the even CTA.
-constexpr int kPairStages = 6;   // 6 x 32 KB ring (7 stages measured slower)
+constexpr int kPairStages = 6;   // 6 x 32 KB ring (7 measured no faster for the gated kernel)
 
 template <int STAGES, int EPI>
 struct PairCfg {
