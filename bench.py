@@ -406,15 +406,26 @@ def _detail_tiny(torch, tp, synth, dev):
     t, n, h, f = 2, 8, 1024, 3072
     x, wgu, wds = make_mlp(torch, synth, t, n, h, f, dev, seed=90)
     y = torch.empty((n, h), dtype=torch.bfloat16, device=dev)
+    wbytes = 3.0 * h * f * 2
+    # Cold: each launch of the graph runs its own copy of the weights (and input), the copies
+    # together twice the L2.  Warm (context only): one copy, L2-resident across launches.
+    sets = cold_set_count(torch, wbytes, 64)
+    copies = [(x, wgu, wds)] + [make_mlp(torch, synth, t, n, h, f, dev, seed=90 + 10 * j) for j in range(1, sets)]
     for mode in ("direct", "ring", "fused"):
         ws = torch.empty(max(256, tp.tp_mlp_workspace_size(t, n, h, f, mode, torch.bfloat16)), dtype=torch.uint8,
                          device=dev)
         fn = lambda: tp.tp_mlp_forward(x, wgu, wds, mode=mode, workspace=ws, y=y)
-        rec = {"us": time_fn(torch, fn, 100) * 1e6, "weight_MB": 3.0 * h * f * 2 / 1e6}
-        gs = graph_time(torch, fn, 100)
+        rec = {"us": time_fn(torch, fn, 100) * 1e6, "weight_MB": wbytes / 1e6}
+        fns = [(lambda c: (lambda: tp.tp_mlp_forward(c[0], c[1], c[2], mode=mode, workspace=ws, y=y)))(c)
+               for c in copies]
+        gs = graph_time_cold(torch, fns, 4)
         if gs:
-            rec["graph_us"] = gs * 1e6
+            rec.update({"graph_us": gs * 1e6, "graph_weight_GBps": wbytes / gs / 1e9, "graph_sets": sets})
+        gw = graph_time(torch, fn, 100)
+        if gw:
+            rec["graph_us_l2_warm"] = gw * 1e6
         out[f"tiny_t2_n8_{mode}"] = rec
+    del copies
     return out
 
 
@@ -425,9 +436,10 @@ def _detail_reduce_sweep(torch, tp, dev, hbm):
         es = 2 if dt == torch.bfloat16 else 4
         for t in (2, 4, 8):
             base = [torch.randn((N_TOK * H,), device=dev).to(dt) for _ in range(t)]
+            o_all = torch.empty((N_TOK * H,), dtype=dt, device=dev)
             for n in (1, 64, 8192):
                 ps = [b[: n * H] for b in base]
-                o = torch.empty((n * H,), dtype=dt, device=dev)
+                o = o_all[: n * H]
                 for mode in ("direct", "ring"):
                     iters = 20 if n == 8192 else 200
                     fn = lambda: tp.tp_shard_reduce(ps, out=o, mode=mode)
@@ -436,12 +448,23 @@ def _detail_reduce_sweep(torch, tp, dev, hbm):
                     rec = {"us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm}
                     if n < 8192:
                         # small messages: eager calls time the host's launch rate; a CUDA-graph
-                        # replay gives the device latency of one reduce (the all-reduce's alpha)
-                        gs = graph_time(torch, fn, 50)
+                        # replay gives the device latency of one reduce (the all-reduce's alpha).
+                        # Cold: each launch reduces its own slices of the buffers, the slices of
+                        # all launches together twice the L2.  Warm: the same slices every launch,
+                        # as when the partials come straight from the GEMM that wrote them.
+                        sets = cold_set_count(torch, byts, N_TOK // n)
+                        fns = [(lambda j: (lambda: tp.tp_shard_reduce(
+                            [b[j * n * H:(j + 1) * n * H] for b in base], out=o_all[j * n * H:(j + 1) * n * H],
+                            mode=mode)))(j) for j in range(sets)]
+                        gs = graph_time_cold(torch, fns)
                         if gs:
-                            rec["graph_us"] = gs * 1e6
+                            rec.update({"graph_us": gs * 1e6, "graph_GBps": byts / gs / 1e9,
+                                        "graph_hbm_frac": byts / gs / 1e9 / hbm, "graph_sets": sets})
+                        gw = graph_time(torch, fn, 50)
+                        if gw:
+                            rec["graph_us_l2_warm"] = gw * 1e6
                     sweep[f"{'bf16' if es == 2 else 'f32'}_t{t}_n{n}_{mode}"] = rec
-            del base
+            del base, o_all
     return sweep
 
 
@@ -481,11 +504,22 @@ def _detail_vocab(torch, tp, synth, dev, hbm, ten, rows):
             s = time_fn(torch, lambda: tp.vocab_parallel_embed(idv, shards, V, out=e), 200 if m == nt else 50)
             byts = m * 4 + 2 * m * hh * 2
             rec = {"us": s * 1e6, "GBps": byts / s / 1e9, "hbm_frac": byts / s / 1e9 / hbm, "bytes": byts}
-            graph_s = graph_time(torch, lambda: tp.vocab_parallel_embed(idv, shards, V, out=e), 100 if m == nt else 20)
+            # Cold: a CUDA graph of lookups, each with its own seeded ids (so its own table rows) and
+            # its own output, the sets together twice the L2.  Warm (context only): the same ids and
+            # output every launch, so rows, ids and output stay in L2.
+            sets = cold_set_count(torch, byts, 64)
+            idss = [idv] + [synth.uniform_ids(m, V, 500 + 7 * j + m, device=dev) for j in range(1, sets)]
+            outs = [e] + [torch.empty((m, hh), dtype=torch.bfloat16, device=dev) for _ in range(1, sets)]
+            fns = [(lambda j: (lambda: tp.vocab_parallel_embed(idss[j], shards, V, out=outs[j])))(j)
+                   for j in range(sets)]
+            graph_s = graph_time_cold(torch, fns, 4 if m == nt else 1)
             if graph_s:
-                rec["graph_us"] = graph_s * 1e6
-                rec["graph_GBps"] = byts / graph_s / 1e9
-                rec["graph_hbm_frac"] = byts / graph_s / 1e9 / hbm
+                rec.update({"graph_us": graph_s * 1e6, "graph_GBps": byts / graph_s / 1e9,
+                            "graph_hbm_frac": byts / graph_s / 1e9 / hbm, "graph_sets": sets})
+            gw = graph_time(torch, lambda: tp.vocab_parallel_embed(idv, shards, V, out=e), 100 if m == nt else 20)
+            if gw:
+                rec["graph_us_l2_warm"] = gw * 1e6
+            del idss, outs, fns
             out[f"embed_t{t}{tag}"] = rec
         if "lm_head" not in rows:
             continue
@@ -526,6 +560,51 @@ def graph_time(torch, fn, reps):
             b.record()
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b) / 1e3 / (5 * reps))
+        return sorted(times)[1]
+    except Exception:
+        return None
+
+
+def l2_bytes(torch):
+    return int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0)) or 126 * 2**20
+
+
+def cold_set_count(torch, set_bytes, cap):
+    """How many disjoint buffer sets a rotation needs so that the sets together
+    hold at least twice the L2: each set is then evicted before its next use."""
+    return max(2, min(cap, -(-2 * l2_bytes(torch) // max(1, int(set_bytes)))))
+
+
+def graph_time_cold(torch, fns, passes=1):
+    """Per-launch time of a CUDA graph that calls fns[0], fns[1], ... in turn
+    (`passes` times), each on its own buffers, with the buffers of all sets
+    together larger than twice the L2: every launch starts with its inputs out
+    of L2, as with an L2 flush between launches but without timing the flush.
+    Median of three timed windows."""
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fns[0]()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(passes):
+                for fn in fns:
+                    fn()
+        g.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(3):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) / 1e3 / (3 * passes * len(fns)))
+        del g
         return sorted(times)[1]
     except Exception:
         return None

@@ -294,7 +294,9 @@ tp_status tp_mlp_forward_static(int t, int64_t n, int64_t h, int64_t f,
  *   partials   NULL, or t device pointers to [n, h] buffers that also
  *              receive each rank's masked lookup (its pre-all-reduce view).
  * Out-of-range ids are not an error.  The result is bit-exact: each output
- * element is one table value plus exact zeros.
+ * element is one table value plus exact zeros.  h * sizeof(dtype) must be a
+ * multiple of 16 (TP_ERR_ALIGNMENT); h <= 2^31 - 1 and n <= 4 (2^31 - 1)
+ * (TP_ERR_INVALID_ARG).
  */
 tp_status vocab_parallel_embed(int t, int64_t vocab, int64_t h, const int32_t* ids, int64_t n,
                                const void* const* table, tp_dtype dtype, void* out,

@@ -344,7 +344,8 @@ tp_status vocab_parallel_embed(int t, int64_t vocab, int64_t h, const int32_t* i
                                const void* const* table, tp_dtype dtype, void* out, void* const* partials,
                                tp_stream stream) {
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
-    TP_CHECK(vocab > 0 && vocab <= INT32_MAX && h > 0 && n >= 0, TP_ERR_INVALID_ARG);
+    TP_CHECK(vocab > 0 && vocab <= INT32_MAX && h > 0 && h <= INT32_MAX && n >= 0, TP_ERR_INVALID_ARG);
+    TP_CHECK(n <= static_cast<int64_t>(INT32_MAX) * 4, TP_ERR_INVALID_ARG);   // one warp per id, four per block
     TP_CHECK(table != nullptr && out != nullptr && (ids != nullptr || n == 0), TP_ERR_INVALID_ARG);
     TP_CHECK(dtype_ok(dtype), TP_ERR_UNSUPPORTED);
     TP_CHECK((h * esize(dtype)) % 16 == 0, TP_ERR_ALIGNMENT);

@@ -7,12 +7,23 @@
 // another rank never leaks), and the t outputs are all-reduced (summed in
 // rank order).  Ranges are disjoint, so for every token at most one rank
 // holds a real row: the kernel reads that one row (one warp per token,
-// 16-byte loads) and forms the rank-order sum of it and t-1 exact zeros in
-// float32, which is x + 0.0 in closed form.  That sum is bit-exact to the
-// lookup, except that -0.0 becomes +0.0 when t > 1, which is what summing
-// the ranks' outputs gives.
+// 16-byte loads) and forms the rank-order sum of it and t-1 exact zeros,
+// which is x + 0.0 in closed form.  That sum is bit-exact to the lookup,
+// except that -0.0 becomes +0.0 (and a NaN becomes the canonical NaN) when
+// t > 1, which is what summing the ranks' outputs gives.
 // Bytes moved per token: h*b read (owner row) + h*b written (+ t*h*b for the
 // optional per-rank outputs) + 4 for the id.
+//
+// A lookup of a few thousand ids moves only a few MB, so its time is mostly
+// latency: launch, the id load, then the row load.  The kernel keeps the
+// path between them short: every shard pointer and range start is read from
+// the parameters before the id arrives, the owner is found by comparisons
+// (no division), one bf16x2 add per 32-bit word forms x + 0.0 (the same bits
+// as the float32 add and round for every bf16 pair pattern), and each warp
+// handles exactly one token (a grid of n/4 four-warp blocks, no grid-stride
+// loop).  Table rows are read and the output written with the streaming
+// cache hint: rows of a random lookup are not reused, and the output is
+// read once by the next layer.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -24,79 +35,89 @@
 namespace tpk {
 
 struct EmbedArgs {
-    const void* table[TP_MAX_SHARDS];
-    void* partials[TP_MAX_SHARDS];
+    // fields read before the id arrives first, so they share constant-cache lines
     const int32_t* ids;
     void* out;
-    int64_t vocab, h, n, per;
+    const void* table[TP_MAX_SHARDS];
+    uint32_t start[TP_MAX_SHARDS];     // first id of each shard (start[r] < vocab for r < t)
+    uint32_t vocab;
     int t;
+    int nvec;                          // 16-byte vectors per row
     int with_partials;
+    int64_t n;
+    void* partials[TP_MAX_SHARDS];
 };
 
+constexpr int kEmbedThreads = 128;     // four tokens per block
+
+// x + 0.0 on two packed bf16 values, rounded to nearest even.
+__device__ __forceinline__ uint32_t add_zero_bf16x2(uint32_t w) {
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0u));
+    return r;
+}
+
+__device__ __forceinline__ uint4 add_zero(uint4 v, bool bf16) {
+    if (bf16)
+        return make_uint4(add_zero_bf16x2(v.x), add_zero_bf16x2(v.y), add_zero_bf16x2(v.z), add_zero_bf16x2(v.w));
+    return make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(v.x), 0.0f)),
+                      __float_as_uint(__fadd_rn(__uint_as_float(v.y), 0.0f)),
+                      __float_as_uint(__fadd_rn(__uint_as_float(v.z), 0.0f)),
+                      __float_as_uint(__fadd_rn(__uint_as_float(v.w), 0.0f)));
+}
+
 template <bool BF16>
-__global__ void __launch_bounds__(256) vocab_embed_kernel(const __grid_constant__ EmbedArgs a) {
-    constexpr int VEC = BF16 ? 8 : 4;             // elements per 16-byte vector
+__global__ void __launch_bounds__(kEmbedThreads) vocab_embed_kernel(const __grid_constant__ EmbedArgs a) {
     const int lane = threadIdx.x & 31;
-    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t nvec = a.h / VEC;
-    for (int64_t tok = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; tok < a.n; tok += warps) {
-        const int32_t id = a.ids[tok];
-        int owner = -1;
-        int64_t local = 0;
-        if (id >= 0 && id < a.vocab) {     // 32-bit arithmetic: ids and vocab sizes are int32
-            const uint32_t u = static_cast<uint32_t>(id), per = static_cast<uint32_t>(a.per);
-            owner = static_cast<int>(u / per);
-            local = static_cast<int64_t>(u - static_cast<uint32_t>(owner) * per);
+    const uint4* tabs[TP_MAX_SHARDS];
+    uint32_t starts[TP_MAX_SHARDS];
+#pragma unroll
+    for (int r = 0; r < TP_MAX_SHARDS; ++r) {
+        tabs[r] = static_cast<const uint4*>(a.table[r]);
+        starts[r] = a.start[r];
+    }
+    const int t = a.t, nvec = a.nvec;
+    const int64_t tok = (static_cast<int64_t>(blockIdx.x) * kEmbedThreads + threadIdx.x) >> 5;
+    if (tok >= a.n) return;
+
+    // Ids are int32: a negative id wraps to 2^31 or more, above every vocab size.
+    const uint32_t u = static_cast<uint32_t>(__ldg(a.ids + tok));
+    const bool hit = u < a.vocab;
+    int owner = 0;
+#pragma unroll
+    for (int r = 1; r < TP_MAX_SHARDS; ++r) owner += (r < t && u >= starts[r]) ? 1 : 0;
+    const uint4* base = tabs[0];
+    uint32_t first = starts[0];
+#pragma unroll
+    for (int r = 1; r < TP_MAX_SHARDS; ++r) {
+        base = owner == r ? tabs[r] : base;
+        first = owner == r ? starts[r] : first;
+    }
+    const uint4* src = base + static_cast<int64_t>(u - first) * nvec;
+    uint4* dst = static_cast<uint4*>(a.out) + tok * nvec;
+
+    // Four row vectors per lane are loaded before any is stored, so a warp has
+    // a 2 KB row (h = 1024 bf16) in flight at once.
+    constexpr int U = 4;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+        uint4 row[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int v = v0 + k * 32;
+            row[k] = (hit && v < nvec) ? __ldcs(src + v) : make_uint4(0, 0, 0, 0);
         }
-        const uint4* src = owner >= 0 ? reinterpret_cast<const uint4*>(a.table[owner]) + local * nvec : nullptr;
-        uint4* dst = reinterpret_cast<uint4*>(a.out) + tok * nvec;
-        // Up to U row vectors per lane are loaded before any is stored, so a
-        // warp has the whole 2 KB row (h = 1024 bf16) in flight at once.
-        constexpr int U = 4;
-        for (int64_t v0 = lane; v0 < nvec; v0 += 32 * U) {
-            uint4 row[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * 32;
-                row[u] = (owner >= 0 && v < nvec) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * 32;
-                if (v >= nvec) break;
-                const uint32_t w[4] = {row[u].x, row[u].y, row[u].z, row[u].w};
-                float x[VEC];
-                if constexpr (BF16) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        x[2 * i] = __uint_as_float(w[i] << 16);
-                        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < VEC; ++i) x[i] = __uint_as_float(w[i]);
-                }
-                // The all-reduce: the rank-order sum of the t masked outputs.  At most one of them
-                // is non-zero, the rest are exact +0.0, so for t > 1 the sum is x + 0.0 in every
-                // order (x itself, except that -0.0 becomes +0.0; NaN and Inf pass), and for t = 1
-                // it is x.  __fadd_rn keeps the addition from being contracted or dropped.
-                float acc[VEC];
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) acc[i] = a.t > 1 ? __fadd_rn(x[i], 0.0f) : x[i];
-                uint4 o;
-                if constexpr (BF16) {
-                    o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-                } else {
-                    o = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
-                                   __float_as_uint(acc[3]));
-                }
-                dst[v] = o;
-                if (a.with_partials) {
-                    for (int r = 0; r < a.t; ++r)
-                        reinterpret_cast<uint4*>(a.partials[r])[tok * nvec + v] =
-                            owner == r ? row[u] : make_uint4(0, 0, 0, 0);
-                }
+        for (int k = 0; k < U; ++k) {
+            const int v = v0 + k * 32;
+            if (v >= nvec) break;
+            // The all-reduce: the rank-order sum of the t masked outputs.  At most one of them is
+            // non-zero and the rest are exact +0.0, so for t > 1 the sum is x + 0.0 in every
+            // order; for t = 1 it is x.
+            __stcs(dst + v, t > 1 ? add_zero(row[k], BF16) : row[k]);
+            if (a.with_partials) {
+                for (int r = 0; r < t; ++r)
+                    static_cast<uint4*>(a.partials[r])[tok * nvec + v] =
+                        (hit && owner == r) ? row[k] : make_uint4(0, 0, 0, 0);
             }
         }
     }
@@ -105,39 +126,28 @@ __global__ void __launch_bounds__(256) vocab_embed_kernel(const __grid_constant_
 tp_status launch_vocab_embed(const EmbedDesc& d, cudaStream_t stream) {
     if (d.n == 0) return TP_OK;
     EmbedArgs a;
+    a.ids = d.ids;
+    a.out = d.out;
     for (int r = 0; r < TP_MAX_SHARDS; ++r) {
         a.table[r] = r < d.t ? d.table[r] : nullptr;
         a.partials[r] = (d.with_partials && r < d.t) ? d.partials[r] : nullptr;
+        // shards past t never match (the kernel compares only r < t); ranges are clipped to V
+        a.start[r] = static_cast<uint32_t>(std::min<int64_t>(static_cast<int64_t>(r) * d.per, d.vocab));
     }
-    a.ids = d.ids;
-    a.out = d.out;
-    a.vocab = d.vocab;
-    a.h = d.h;
-    a.n = d.n;
-    a.per = d.per;
+    a.vocab = static_cast<uint32_t>(d.vocab);
     a.t = d.t;
+    a.nvec = static_cast<int>(d.h * (d.bf16 ? 2 : 4) / 16);
     a.with_partials = d.with_partials;
-    // one warp per token; at most one resident wave of blocks (grid-stride beyond)
-    const int64_t want = (d.n * 32 + 255) / 256;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    static int per_sm[2] = {0, 0};            // a property of the kernel, the same on every GB300
-    int& occ = per_sm[d.bf16 ? 1 : 0];
-    if (occ <= 0) {
-        if (d.bf16)
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, vocab_embed_kernel<true>, 256, 0);
-        else
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, vocab_embed_kernel<false>, 256, 0);
-    }
-    const int64_t resident = static_cast<int64_t>(std::max(sms, 1)) * std::max(occ, 1);
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, resident)));
+    a.n = d.n;
+    // one warp per token, four tokens per block
+    const int64_t blocks = (d.n + kEmbedThreads / 32 - 1) / (kEmbedThreads / 32);
+    if (blocks > INT32_MAX) return TP_ERR_INVALID_ARG;
     // Launched in plain stream order: with programmatic launch, back-to-back lookups of
     // 4096 ids measured 3.33 us per call instead of 2.97.
     if (d.bf16)
-        vocab_embed_kernel<true><<<grid, 256, 0, stream>>>(a);
+        vocab_embed_kernel<true><<<static_cast<unsigned>(blocks), kEmbedThreads, 0, stream>>>(a);
     else
-        vocab_embed_kernel<false><<<grid, 256, 0, stream>>>(a);
+        vocab_embed_kernel<false><<<static_cast<unsigned>(blocks), kEmbedThreads, 0, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 

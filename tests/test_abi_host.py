@@ -95,6 +95,8 @@ def test_reduce_embed_head_gather_reject_on_host(lib):
     assert lib.tp_shard_reduce(2, 100, 0, two, FAKE, 0, 2, 1, 0, None) == 1        # FUSED is not a reduce mode
     assert lib.vocab_parallel_embed(2, 10, 12, FAKE, 4, two, 0, FAKE, None, None) == 3   # 24-byte rows
     assert lib.vocab_parallel_embed(0, 10, 16, FAKE, 4, two, 0, FAKE, None, None) == 1
+    assert lib.vocab_parallel_embed(2, 10, 16, FAKE, 4 * (2 ** 31 - 1) + 1, two, 0, FAKE, None, None) == 1  # grid
+    assert lib.vocab_parallel_embed(2, 10, 2 ** 31, FAKE, 4, two, 0, FAKE, None, None) == 1
     assert lib.lm_head_sharded(2, 4, 12, 10, FAKE, 16, two, FAKE, 16, None, 0, None) == 3
     assert lib.lm_head_sharded(2, 4, 16, 10, FAKE, 16, two, None, 0, None, 0, None) == 1
     cols = (ctypes.c_int64 * 2)(3, -1)

@@ -314,6 +314,49 @@ def test_vocab_embed_edges(t, V):
     exact(f64(out), ref)
 
 
+@pytest.mark.parametrize("t", [1, 2, 3])
+def test_vocab_embed_every_bf16_pattern(t):
+    """The all-reduce of one row and t-1 exact zeros, formed on packed bf16
+    pairs: every one of the 65536 bf16 bit patterns (zeros of both signs,
+    subnormals, infinities, NaNs) as a table value, against the oracle's sum."""
+    V, h = 64, 1024
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(V, h)
+    table = bits.view(torch.bfloat16).to(DEV)
+    ids = torch.tensor(list(range(V - 1, -1, -1)) + [-5, V, 7], dtype=torch.int32, device=DEV)
+    parts = [torch.empty((ids.numel(), h), dtype=torch.bfloat16, device=DEV) for _ in range(t)]
+    out = tp.vocab_parallel_embed(ids, _table_shards(table, t), V, partials=parts)
+    torch.cuda.synchronize()
+    ref, refp = O.vocab_parallel_embedding(ids.cpu().numpy(), f64(table), t)
+    exact(f64(out), ref)
+    for r in range(t):
+        exact(f64(parts[r]), refp[r])
+    if t == 1:       # a single rank's lookup is the row itself, NaN payloads included
+        assert torch.equal(out[:V].view(torch.int16), table[ids[:V].long()].view(torch.int16))
+
+
+@pytest.mark.parametrize("t", [1, 3])
+def test_vocab_embed_f32_table(t):
+    V, h, n = 37, 20, 300
+    table = synth.normal_f32((V, h), 1.0, 8, device=DEV)
+    table[0, :4] = torch.tensor([float("nan"), float("-inf"), -0.0, 1e-41])
+    ids = synth.uniform_ids(n, V + 3, 9, device=DEV) - 1      # includes -1 and ids >= V
+    out = tp.vocab_parallel_embed(ids, _table_shards(table, t), V)
+    torch.cuda.synchronize()
+    ref, _ = O.vocab_parallel_embedding(ids.cpu().numpy(), f64(table), t)
+    exact(f64(out), ref)
+
+
+def test_vocab_embed_many_ids_ragged():
+    """More ids than one wave of warps (one warp per id, n/4 blocks) with a ragged last block."""
+    V, h, n, t = 151936, 1024, 70001, 4
+    table = normal((V, h), 0.02, 6)
+    ids = synth.uniform_ids(n, V, 15, device=DEV)
+    out = tp.vocab_parallel_embed(ids, _table_shards(table, t), V)
+    torch.cuda.synchronize()
+    ref, _ = O.vocab_parallel_embedding(ids.cpu().numpy(), f64(table), t)
+    exact(f64(out), ref)
+
+
 def test_vocab_embed_worked_example_structure():
     # vLLM source analysis 13, section 2.4.1: V=10, ids [[1,6],[3,8]], two ranges of 5 rows
     V, h, t = 10, 8, 2
