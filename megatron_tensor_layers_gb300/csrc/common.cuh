@@ -261,6 +261,15 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Cluster barrier whose arrive orders nothing before it: for a teardown where
+// every access to a peer's shared memory is already known complete (each was
+// observed by its target through an mbarrier, or its value consumed), so that
+// exiting does not wait for this CTA's global stores to become visible.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Address, in the cluster's shared window, of the variable at `addr` in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     uint32_t r;
@@ -272,6 +281,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
+
+// Fence that, followed by relaxed cluster arrives, makes them one release:
+// the arrives are then issued back to back instead of each waiting for the
+// thread's earlier writes to become visible to the cluster.
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // The same arrive without release semantics: it orders nothing but the
 // thread's own program order, so it does not wait for the thread's global

@@ -1043,12 +1043,15 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             }
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));                // the accumulator is free for the next tile
-            // The warp's staged rows are visible to the cluster once lane 0's release arrive is:
-            // the warp barrier orders every lane's writes before it.
+            // The warp's staged rows are visible to the cluster once lane 0's arrives are: the warp
+            // barrier orders every lane's writes before lane 0's fence, and the fence followed by
+            // the relaxed arrives is a release (one fence, not one release per peer).
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0) {
+                fence_acq_rel_cluster();
                 for (int p = 0; p < cs; ++p)
-                    mbar_arrive_cluster(mapa_shared(staged_bar, static_cast<uint32_t>(p)));
+                    mbar_arrive_cluster_relaxed(mapa_shared(staged_bar, static_cast<uint32_t>(p)));
+            }
             if (!mbar_wait_cluster_warp(staged_bar, j & 1u, abort_flag, args.status)) {
                 aborted = true;
                 break;
@@ -1088,9 +1091,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
                 store_quad(out, args.ldo, args.out_f32, static_cast<int64_t>(m) * BM + r, col0, nvalid, v);
             }
             // This warp has read (and consumed) its share of every peer's staging; a relaxed
-            // arrive suffices, since no peer needs this warp's output stores ordered.
+            // arrive suffices, since no peer needs this warp's output stores ordered.  After the
+            // CTA's last tile nobody waits on the drained barriers: no arrive is sent, so that no
+            // remote arrive can still be in flight at teardown.
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0 && tile + nclusters < args.total_tiles)
                 for (int p = 0; p < cs; ++p)
                     mbar_arrive_cluster_relaxed(mapa_shared(drained_bar, static_cast<uint32_t>(p)));
             if (++acc == 2) {
@@ -1103,7 +1108,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
     if (aborted) spin_ns(50000);
     __syncwarp();                                        // reconverge the lane-0 roles (aligned barrier below)
     tc_fence_before();
-    cluster_sync();                                      // peers may still read this CTA's staging until here
+    // Peers may read this CTA's staging until they reach this barrier.  Every such read was
+    // consumed (its value stored) before the reader arrives, every staged arrive was observed
+    // by its target's staged wait, and the last tile sends no drained arrives, so nothing
+    // remote is in flight: the arrive need not wait for this CTA's output stores.
+    cluster_sync_relaxed();
     if (*abort_flag) spin_ns(50000);
     if (warp == 1) {
         __syncwarp();
