@@ -196,9 +196,16 @@ struct GemmCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-template <int BN, int STAGES, int EPI, int AROWS>
+// KSUB: K blocks per ring slot group.  The STAGES stage buffers form STAGES/KSUB groups with
+// one full and one empty barrier each: the producer waits once, arms once and issues KSUB
+// blocks' loads; the MMA thread waits once, issues KSUB blocks' MMAs and commits once.  At
+// decode sizes with short K the MMA thread's per-block wait, fence and commit (about twice
+// the MMAs' own time for a 64-wide tile) otherwise bound the K loop.
+template <int BN, int STAGES, int EPI, int AROWS, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_constant__ GemmArgs args) {
     using Cfg = GemmCfg<BN, STAGES, EPI, AROWS>;
+    static_assert(KSUB >= 1 && STAGES % KSUB == 0, "stage groups of KSUB blocks");
+    constexpr int GROUPS = STAGES / KSUB;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles.
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -252,8 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
             // it was: at decode sizes the producer's issue rate bounds the weight stream, and a
             // variant that loaded the first ring of weights before the wait ran 6 % slower.
             pdl_wait();
-            int stage = 0;
+            int grp = 0;
             uint32_t phase = 0;
+            const uint32_t block_bytes = static_cast<uint32_t>(args.a_box_rows * 128 + Cfg::B_BYTES);
             for (int tile = blockIdx.x; tile < args.total_tiles && !aborted; tile += gridDim.x) {
                 int g, m, n;
                 tile_coords(args, tile, g, m, n);
@@ -263,30 +271,37 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                 const int rot = args.rotate_k ? tile % args.k_blocks : 0;
                 // (segment, block) advanced incrementally: no division in the issue loop
                 int seg = 0, kin = 0;
-                for (int kk = 0; kk < kb_per_tile; ++kk) {
-                    int kb = kin + rot;
-                    if (kb >= args.k_blocks) kb -= args.k_blocks;
-                    const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
-                    const int bi = args.segs > 1 ? seg : g;
-                    if (++kin == args.k_blocks) {
-                        kin = 0;
-                        ++seg;
-                    }
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
+                for (int kk = 0; kk < kb_per_tile; kk += KSUB) {
+                    const int cnt = min(KSUB, kb_per_tile - kk);   // a tile's last group may be short
+                    if (!mbar_wait(empty_bar(grp), phase ^ 1u, abort_flag, args.status)) {
                         aborted = true;
                         break;
                     }
-                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
-                    const uint32_t sb = sa + Cfg::A_BYTES;
-                    mbar_arrive_expect_tx(full_bar(stage), args.a_box_rows * 128 + Cfg::B_BYTES);
-                    tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);
-                    if (EPI == EPI_GLU) {   // gate rows and the same rows of up, one 3-D box
-                        tma_load_3d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * (BN / 2), 0);
-                    } else {
-                        tma_load_2d(sb, &args.mapB[bi], full_bar(stage), kb * BK, n * BN);
+                    const uint32_t bar = full_bar(grp);
+                    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * block_bytes);
+#pragma unroll
+                    for (int i = 0; i < KSUB; ++i) {
+                        if (i < cnt) {
+                            int kb = kin + rot;
+                            if (kb >= args.k_blocks) kb -= args.k_blocks;
+                            const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                            const int bi = args.segs > 1 ? seg : g;
+                            if (++kin == args.k_blocks) {
+                                kin = 0;
+                                ++seg;
+                            }
+                            const uint32_t sa = base + (grp * KSUB + i) * Cfg::STAGE_BYTES;
+                            const uint32_t sb = sa + Cfg::A_BYTES;
+                            tma_load_2d(sa, &args.mapA[ai], bar, kb * BK, m * BM);
+                            if (EPI == EPI_GLU) {   // gate rows and the same rows of up, one 3-D box
+                                tma_load_3d(sb, &args.mapB[bi], bar, kb * BK, n * (BN / 2), 0);
+                            } else {
+                                tma_load_2d(sb, &args.mapB[bi], bar, kb * BK, n * BN);
+                            }
+                        }
                     }
-                    if (++stage == STAGES) {
-                        stage = 0;
+                    if (++grp == GROUPS) {
+                        grp = 0;
                         phase ^= 1u;
                     }
                 }
@@ -296,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t idesc = mma_idesc_bf16(BM, BN);
-            int stage = 0;
+            int grp = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
@@ -307,23 +322,29 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kk = 0; kk < kb_per_tile; ++kk) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.status)) {
+                for (int kk = 0; kk < kb_per_tile; kk += KSUB) {
+                    const int cnt = min(KSUB, kb_per_tile - kk);
+                    if (!mbar_wait(full_bar(grp), phase, abort_flag, args.status)) {
                         aborted = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
-                    const uint64_t adesc = sw128_kmajor_desc(sa);
-                    const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        // advance 16 bf16 = 32 bytes along K inside the swizzle row
-                        tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0 ? 1u : 0u);
+                    for (int i = 0; i < KSUB; ++i) {
+                        if (i < cnt) {
+                            const uint32_t sa = base + (grp * KSUB + i) * Cfg::STAGE_BYTES;
+                            const uint64_t adesc = sw128_kmajor_desc(sa);
+                            const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k) {
+                                // advance 16 bf16 = 32 bytes along K inside the swizzle row
+                                tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, ((kk + i) | k) != 0 ? 1u : 0u);
+                            }
+                        }
                     }
-                    tc_commit(empty_bar(stage));
-                    if (++stage == STAGES) {
-                        stage = 0;
+                    tc_commit(empty_bar(grp));
+                    if (++grp == GROUPS) {
+                        grp = 0;
                         phase ^= 1u;
                     }
                 }
@@ -1201,7 +1222,7 @@ static bool make_map_glu(CUtensorMap* m, const void* ptr, int64_t half_rows, int
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int EPI, int AROWS = BM>
+template <int BN, int STAGES, int EPI, int AROWS = BM, int KSUB = 1>
 static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream) {
     using Cfg = GemmCfg<BN, STAGES, EPI, AROWS>;
     if (AROWS < BM && d.M > AROWS) return TP_ERR_UNSUPPORTED;   // a short A tile holds one m-tile
@@ -1226,7 +1247,7 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
                                          : make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box);
         if (!ok) return TP_ERR_CUDA;
     }
-    auto kern = tp_gemm_kernel<BN, STAGES, EPI, AROWS>;
+    auto kern = tp_gemm_kernel<BN, STAGES, EPI, AROWS, KSUB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return TP_ERR_CUDA;
     const int sms = sm_count();
@@ -1462,12 +1483,12 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     if (d.M <= 64) {   // decode: 64-row A tiles, deeper B rings
         if (glu) {
             if (best == 256) return launch_cfg<256, 5, EPI_GLU, 64>(a, d, stream);
-            if (best == 128) return launch_cfg<128, 8, EPI_GLU, 64>(a, d, stream);
-            return launch_cfg<64, 13, EPI_GLU, 64>(a, d, stream);
+            if (best == 128) return launch_cfg<128, 8, EPI_GLU, 64, 2>(a, d, stream);
+            return launch_cfg<64, 12, EPI_GLU, 64, 4>(a, d, stream);
         }
         if (best == 256) return launch_cfg<256, 5, EPI_STORE, 64>(a, d, stream);
-        if (best == 128) return launch_cfg<128, 9, EPI_STORE, 64>(a, d, stream);
-        return launch_cfg<64, 14, EPI_STORE, 64>(a, d, stream);
+        if (best == 128) return launch_cfg<128, 8, EPI_STORE, 64, 2>(a, d, stream);
+        return launch_cfg<64, 12, EPI_STORE, 64, 4>(a, d, stream);
     }
     if (glu) {
         if (best == 256) return launch_cfg<256, 4, EPI_GLU>(a, d, stream);
