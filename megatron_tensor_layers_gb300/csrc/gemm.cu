@@ -854,9 +854,11 @@ __device__ __forceinline__ void store_quad(void* base, int64_t ldo, int out_f32,
     }
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __grid_constant__ GemmArgs args) {
     using Cfg = SplitCfg<BN, STAGES, EPI>;
+    static_assert(KSUB >= 1 && STAGES % KSUB == 0, "stage groups of KSUB blocks (as in tp_gemm_kernel)");
+    constexpr int GROUPS = STAGES / KSUB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -935,50 +937,61 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
             };
             // B of the first ring fill before waiting for the previous grid of the stream, when
             // that grid is a kernel of the same call (only A can be its output)
-            int pre = 0;
+            const uint32_t block_bytes = static_cast<uint32_t>(args.a_box_rows * 128 + Cfg::B_BYTES);
+            const int nkb = kb_hi - kb_lo;
+            int pre = 0;                                   // blocks of the first tile already armed
             if (args.pdl_prefetch && cluster < args.total_tiles) {
                 int g, m, n;
                 tile_coords(args, cluster, g, m, n);
                 const int rot = args.rotate_k ? cluster % args.k_blocks : 0;
-                pre = min(STAGES, kb_hi - kb_lo);
-                for (int i = 0; i < pre; ++i) {
-                    int kb, ai, bi;
-                    kblock(kb_lo + i, rot, g, kb, ai, bi);
-                    mbar_arrive_expect_tx(full_bar(i), args.a_box_rows * 128 + Cfg::B_BYTES);
-                    load_b(base + i * Cfg::STAGE_BYTES + Cfg::A_BYTES, bi, full_bar(i), kb, n);
+                pre = min(STAGES, nkb);
+                for (int gi = 0; gi * KSUB < pre; ++gi) {
+                    const int cnt = min(KSUB, nkb - gi * KSUB);
+                    mbar_arrive_expect_tx(full_bar(gi), static_cast<uint32_t>(cnt) * block_bytes);
+                    for (int i = 0; i < cnt; ++i) {
+                        int kb, ai, bi;
+                        kblock(kb_lo + gi * KSUB + i, rot, g, kb, ai, bi);
+                        load_b(base + (gi * KSUB + i) * Cfg::STAGE_BYTES + Cfg::A_BYTES, bi, full_bar(gi), kb, n);
+                    }
                 }
             }
             pdl_wait();
-            int stage = 0;
+            int grp = 0;
             uint32_t phase = 0;
             for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
                 int g, m, n;
                 tile_coords(args, tile, g, m, n);
                 const int rot = args.rotate_k ? tile % args.k_blocks : 0;
                 int seg = kb_lo / args.k_blocks, kin = kb_lo - (kb_lo / args.k_blocks) * args.k_blocks;
-                for (int kk = kb_lo; kk < kb_hi; ++kk) {
-                    int kb = kin + rot;                    // (segment, block) advanced without division
-                    if (kb >= args.k_blocks) kb -= args.k_blocks;
-                    const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
-                    const int bi = args.segs > 1 ? seg : g;
-                    if (++kin == args.k_blocks) {
-                        kin = 0;
-                        ++seg;
-                    }
-                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
-                    if (tile == cluster && kk - kb_lo < pre) {
-                        tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);   // armed, B in flight
-                    } else {
-                        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
+                for (int kk = 0; kk < nkb; kk += KSUB) {
+                    const int cnt = min(KSUB, nkb - kk);
+                    const bool armed = tile == cluster && kk < pre;   // B in flight since the prefetch
+                    const uint32_t bar = full_bar(grp);
+                    if (!armed) {
+                        if (!mbar_wait(empty_bar(grp), phase ^ 1u, abort_flag, args.status)) {
                             aborted = true;
                             break;
                         }
-                        mbar_arrive_expect_tx(full_bar(stage), args.a_box_rows * 128 + Cfg::B_BYTES);
-                        tma_load_2d(sa, &args.mapA[ai], full_bar(stage), kb * BK, m * BM);
-                        load_b(sa + Cfg::A_BYTES, bi, full_bar(stage), kb, n);
+                        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * block_bytes);
                     }
-                    if (++stage == STAGES) {
-                        stage = 0;
+#pragma unroll
+                    for (int i = 0; i < KSUB; ++i) {
+                        if (i < cnt) {
+                            int kb = kin + rot;            // (segment, block) advanced without division
+                            if (kb >= args.k_blocks) kb -= args.k_blocks;
+                            const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                            const int bi = args.segs > 1 ? seg : g;
+                            if (++kin == args.k_blocks) {
+                                kin = 0;
+                                ++seg;
+                            }
+                            const uint32_t sa = base + (grp * KSUB + i) * Cfg::STAGE_BYTES;
+                            tma_load_2d(sa, &args.mapA[ai], bar, kb * BK, m * BM);
+                            if (!armed) load_b(sa + Cfg::A_BYTES, bi, bar, kb, n);
+                        }
+                    }
+                    if (++grp == GROUPS) {
+                        grp = 0;
                         phase ^= 1u;
                     }
                 }
@@ -988,10 +1001,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t idesc = mma_idesc_bf16(BM, BN);
-            int stage = 0;
+            int grp = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            const int nkb = kb_hi - kb_lo;
             for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) {
                     aborted = true;
@@ -999,21 +1013,27 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kk = kb_lo; kk < kb_hi; ++kk) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.status)) {
+                for (int kk = 0; kk < nkb; kk += KSUB) {
+                    const int cnt = min(KSUB, nkb - kk);
+                    if (!mbar_wait(full_bar(grp), phase, abort_flag, args.status)) {
                         aborted = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
-                    const uint64_t adesc = sw128_kmajor_desc(sa);
-                    const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk > kb_lo || k > 0) ? 1u : 0u);
-                    tc_commit(empty_bar(stage));
-                    if (++stage == STAGES) {
-                        stage = 0;
+                    for (int i = 0; i < KSUB; ++i) {
+                        if (i < cnt) {
+                            const uint32_t sa = base + (grp * KSUB + i) * Cfg::STAGE_BYTES;
+                            const uint64_t adesc = sw128_kmajor_desc(sa);
+                            const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k)
+                                tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, ((kk + i) | k) != 0 ? 1u : 0u);
+                        }
+                    }
+                    tc_commit(empty_bar(grp));
+                    if (++grp == GROUPS) {
+                        grp = 0;
                         phase ^= 1u;
                     }
                 }
@@ -1320,7 +1340,7 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int KSUB = 1>
 static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream_t stream) {
     using Cfg = SplitCfg<BN, STAGES, EPI>;
     const int kb_all = a.k_blocks * d.segs;
@@ -1344,7 +1364,7 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
                                          : make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box);
         if (!ok) return TP_ERR_CUDA;
     }
-    auto kern = tp_gemm_splitk_kernel<BN, STAGES, EPI>;
+    auto kern = tp_gemm_splitk_kernel<BN, STAGES, EPI, KSUB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return TP_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1475,10 +1495,10 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     if (cs >= 2) {
         if (glu) {
             if (split_bn == 256) return launch_split<256, 4, EPI_GLU>(a, d, cs, stream);
-            return launch_split<128, 8, EPI_GLU>(a, d, cs, stream);
+            return launch_split<128, 8, EPI_GLU, 2>(a, d, cs, stream);
         }
         if (split_bn == 256) return launch_split<256, 4, EPI_STORE>(a, d, cs, stream);
-        return launch_split<128, 8, EPI_STORE>(a, d, cs, stream);
+        return launch_split<128, 8, EPI_STORE, 2>(a, d, cs, stream);
     }
     if (d.M <= 64) {   // decode: 64-row A tiles, deeper B rings
         if (glu) {
