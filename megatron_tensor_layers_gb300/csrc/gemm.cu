@@ -480,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
 // full barrier; MMA completion is multicast to both CTAs' stage and
 // accumulator barriers; both epilogues report back to the even CTA.
 constexpr int kPairStages = 6;   // 6 x 32 KB ring (7 measured no faster for the gated kernel)
+constexpr int kPairKsub = 2;     // K blocks per ring barrier
 
 template <int STAGES, int EPI>
 struct PairCfg {
@@ -501,9 +502,11 @@ struct PairCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-template <int STAGES, int EPI>
+template <int STAGES, int EPI, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_constant__ GemmArgs args) {
     using Cfg = PairCfg<STAGES, EPI>;
+    static_assert(KSUB >= 1 && STAGES % KSUB == 0, "stage groups of KSUB blocks (as in tp_gemm_kernel)");
+    constexpr int GROUPS = STAGES / KSUB;
     constexpr int BN = Cfg::BN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
             pdl_wait();                                // A may be the previous grid's output
-            int stage = 0;
+            int grp = 0;
             uint32_t phase = 0;
             for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
                 int g, m, n;
@@ -566,26 +569,32 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                 const int b_row = (EPI == EPI_GLU) ? (rank == 0 ? n * 128 : args.glu_up_row + n * 128)
                                                    : n * BN + static_cast<int>(rank) * 128;
                 int seg = 0, kb = 0;                   // (segment, block), advanced without division
-                for (int kk = 0; kk < kb_per_tile; ++kk) {
-                    const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
-                    const int bi = args.segs > 1 ? seg : g;
-                    const int kcol = kb * BK;
-                    if (++kb == args.k_blocks) {
-                        kb = 0;
-                        ++seg;
-                    }
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
+                for (int kk = 0; kk < kb_per_tile; kk += KSUB) {
+                    const int cnt = min(KSUB, kb_per_tile - kk);
+                    if (!mbar_wait(empty_bar(grp), phase ^ 1u, abort_flag, args.status)) {
                         aborted = true;
                         break;
                     }
-                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
-                    const uint32_t sb = sa + Cfg::A_BYTES;
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
-                    const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
-                    tma_load_2d_pair(sa, &args.mapA[ai], leader_full, kcol, a_row);
-                    tma_load_2d_pair(sb, &args.mapB[bi], leader_full, kcol, b_row);
-                    if (++stage == STAGES) {
-                        stage = 0;
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(full_bar(grp), static_cast<uint32_t>(cnt) * 2u * Cfg::STAGE_BYTES);
+                    const uint32_t leader_full = mapa_shared(full_bar(grp), 0);
+#pragma unroll
+                    for (int i = 0; i < KSUB; ++i) {
+                        if (i < cnt) {
+                            const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                            const int bi = args.segs > 1 ? seg : g;
+                            const int kcol = kb * BK;
+                            if (++kb == args.k_blocks) {
+                                kb = 0;
+                                ++seg;
+                            }
+                            const uint32_t sa = base + (grp * KSUB + i) * Cfg::STAGE_BYTES;
+                            tma_load_2d_pair(sa, &args.mapA[ai], leader_full, kcol, a_row);
+                            tma_load_2d_pair(sa + Cfg::A_BYTES, &args.mapB[bi], leader_full, kcol, b_row);
+                        }
+                    }
+                    if (++grp == GROUPS) {
+                        grp = 0;
                         phase ^= 1u;
                     }
                 }
@@ -595,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
         if (lane == 0 && rank == 0) {
             // ------------------------------------------------ MMA issuer (even CTA)
             constexpr uint32_t idesc = mma_idesc_bf16(256, BN);
-            int stage = 0;
+            int grp = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
@@ -606,21 +615,28 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kk = 0; kk < kb_per_tile; ++kk) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.status)) {
+                for (int kk = 0; kk < kb_per_tile; kk += KSUB) {
+                    const int cnt = min(KSUB, kb_per_tile - kk);
+                    if (!mbar_wait(full_bar(grp), phase, abort_flag, args.status)) {
                         aborted = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
-                    const uint64_t adesc = sw128_kmajor_desc(sa);
-                    const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        tc_mma_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kk | k) != 0 ? 1u : 0u);
-                    tc_commit_pair(empty_bar(stage), 0x3);
-                    if (++stage == STAGES) {
-                        stage = 0;
+                    for (int i = 0; i < KSUB; ++i) {
+                        if (i < cnt) {
+                            const uint32_t sa = base + (grp * KSUB + i) * Cfg::STAGE_BYTES;
+                            const uint64_t adesc = sw128_kmajor_desc(sa);
+                            const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k)
+                                tc_mma_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                                            ((kk + i) | k) != 0 ? 1u : 0u);
+                        }
+                    }
+                    tc_commit_pair(empty_bar(grp), 0x3);
+                    if (++grp == GROUPS) {
+                        grp = 0;
                         phase ^= 1u;
                     }
                 }
@@ -1286,7 +1302,7 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
-template <int STAGES, int EPI>
+template <int STAGES, int EPI, int KSUB = 1>
 static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream) {
     using Cfg = PairCfg<STAGES, EPI>;
     a.m_tiles = static_cast<int>((d.M + Cfg::TILE_M - 1) / Cfg::TILE_M);
@@ -1304,7 +1320,7 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
         const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
         if (!make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, 128)) return TP_ERR_CUDA;
     }
-    auto kern = tp_gemm_pair_kernel<STAGES, EPI>;
+    auto kern = tp_gemm_pair_kernel<STAGES, EPI, KSUB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
         return TP_ERR_CUDA;
     const int sms = sm_count();
@@ -1487,8 +1503,8 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
         pair = d.pair > 0 || (d.M >= 512 && pair_tiles >= 2LL * (sms / 2) && d.force_bn == 0);
     }
     if (pair) {
-        if (glu) return launch_pair<kPairStages, EPI_GLU>(a, d, stream);
-        return launch_pair<kPairStages, EPI_STORE>(a, d, stream);
+        if (glu) return launch_pair<kPairStages, EPI_GLU, kPairKsub>(a, d, stream);
+        return launch_pair<kPairStages, EPI_STORE, kPairKsub>(a, d, stream);
     }
     int split_bn = 0;
     const int cs = split_plan(d, sms, split_bn);
