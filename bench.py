@@ -42,10 +42,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the gate_up GEMM at the bench
 # size, from ncu (dram__bytes_read.sum + dram__bytes_write.sum); None until
 # taken for the current kernel.
-TRAFFIC_GLU_FULL = 9201524992 + 468526336
+TRAFFIC_GLU_FULL = 8152473088 + 467175680
 TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the CTA-pair gate_up "
                 "GEMM at the bench size (1-pass capture, profiles/tp_gemm_pair_traffic_t4_n8192.md); "
-                "6.3x the algorithmic bytes: weights streamed once per 64 MB raster band of X rows, "
+                "5.6x the algorithmic bytes: weights streamed once per 64 MB raster band of X rows, "
                 "band rows re-read from DRAM between waves")
 
 
@@ -291,6 +291,8 @@ def run_ours(args, rank, world, local_rank):
            "path": (f"pinned host X -> tp_mlp_forward_host (C ABI; {E2E_CHUNKS} row blocks, copies overlapped "
                     "with compute on a second stream) -> pinned host Y"),
            "ms_by_chunks": {str(k): v * 1e3 for k, v in e2e_runs.items()}}
+    if args.no_e2e:                     # profiling runs: no end-to-end number (null, not NaN, in the JSON)
+        e2e.update({"value": None, "ms_per_step": None, "ms_by_chunks": None})
 
     if not args.no_detail:
         rows = tuple(args.detail_rows.split(",")) if args.detail_rows else DETAIL_ROWS
