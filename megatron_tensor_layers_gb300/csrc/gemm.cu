@@ -30,10 +30,15 @@
 // Every barrier wait is bounded (1 s); a wait that expires records
 // TP_ERR_TIMEOUT and the CTA unwinds and exits normally.
 //
-// Inside one library call the second and later GEMMs (and the reduce) are
-// launched with programmatic stream serialization: they may start while the
-// previous kernel of the call drains, and their producer executes
-// griddepcontrol.wait before loading anything that kernel may have written.
+// Every GEMM (and the reduce) is launched with programmatic stream
+// serialization: it may start while the previous kernel of the stream
+// drains.  Its producer executes griddepcontrol.wait before loading anything
+// that kernel may have written: for the first kernel of a library call that
+// is everything, for a later kernel of the call everything but the weights.
+// The stage ring is split into groups of KSUB stages (K blocks) under one
+// full and one empty barrier each, so the producer and MMA threads wait, arm
+// and commit once per group; at short K their per-block barrier work, not
+// the MMAs, would otherwise set the pace.
 // Three kernels share this structure: tp_gemm_kernel (one CTA per tile),
 // tp_gemm_pair_kernel (256 x 256 tiles on a CTA pair, cta_group::2) and
 // tp_gemm_splitk_kernel (the K loop of a decode-sized tile split over a
@@ -798,15 +803,16 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
 // Per tile and CTA: wait for the accumulator; wait until every epilogue warp
 // of the cluster has read this CTA's staging of the previous tile
 // (`drained`); stage; free the accumulator; each warp (lane 0, after a warp
-// barrier) release-arrives on the `staged` barrier of every CTA of the
-// cluster, its own included; acquire-wait on its own `staged`; the 128
-// epilogue threads reduce and store this CTA's chunks, one 4-column group of
-// one row per item with the CS peer loads in flight together; each warp
-// arrives on every CTA's `drained`.  One arrival per warp instead of per
-// thread: with CS = 8 a tile otherwise cost each CTA 1024 remote arrivals
-// on each barrier.  Waits are bounded like every other wait of the library,
-// and a cluster barrier before exit keeps each CTA's shared memory alive
-// while its peers may still read it.
+// barrier, one cluster fence, then relaxed arrives: together one release)
+// arrives on the `staged` barrier of every CTA of the cluster, its own
+// included; acquire-wait on its own `staged`; the 128 epilogue threads reduce
+// and store this CTA's chunks, one 4-column group of one row per item with
+// the CS peer loads in flight together; each warp arrives on every CTA's
+// `drained` (not after the CTA's last tile).  One arrival per warp instead
+// of per thread: with CS = 8 a tile otherwise cost each CTA 1024 remote
+// arrivals on each barrier.  Waits are bounded like every other wait of the
+// library, and a relaxed cluster barrier before exit keeps each CTA's shared
+// memory alive while its peers may still read it.
 template <int BN, int STAGES, int EPI>
 struct SplitCfg {
     static constexpr int ROWS = 64;                          // staged rows (M <= 64)
