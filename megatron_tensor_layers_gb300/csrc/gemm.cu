@@ -34,7 +34,9 @@
 // serialization: it may start while the previous kernel of the stream
 // drains.  Its producer executes griddepcontrol.wait before loading anything
 // that kernel may have written: for the first kernel of a library call that
-// is everything, for a later kernel of the call everything but the weights.
+// is everything; only the split-K kernel, when it is a later kernel of the
+// same call (whose predecessor writes no weights), loads its first ring of
+// weights before the wait.
 // The stage ring is split into groups of KSUB stages (K blocks) under one
 // full and one empty barrier each, so the producer and MMA threads wait, arm
 // and commit once per group; at short K their per-block barrier work, not
