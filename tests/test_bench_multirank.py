@@ -53,3 +53,28 @@ def test_two_gloo_ranks_max_and_whole_job_value():
             assert m == 0.5                        # both ranks see the slowest rank's time
             assert v == pytest.approx(100.0 * 2 / 0.5)
         assert out[11] is None                     # the reference arm does no work off rank 0
+
+
+def test_cold_set_count_covers_twice_the_l2():
+    """The cold-L2 timings rotate through buffer sets that together hold at
+    least twice the L2 (unless the rows cap the count), and never fewer than
+    two sets."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class _Props:
+        L2_cache_size = 126 * 2 ** 20
+
+    class _Cuda:
+        @staticmethod
+        def get_device_properties(_):
+            return _Props()
+
+    fake_torch = type("T", (), {"cuda": _Cuda})
+    l2 = _Props.L2_cache_size
+    for set_bytes in (16 << 10, 48 << 10, 3 << 20, 16 << 20, 18_874_368, 300 << 20, 2 << 30):
+        n = bench.cold_set_count(fake_torch, set_bytes, 1 << 20)
+        assert n >= 2
+        assert n * set_bytes >= 2 * l2
+        assert (n - 1) * set_bytes < 2 * l2 or n == 2
+    assert bench.cold_set_count(fake_torch, 16 << 10, 64) == 64          # capped by the rows available
