@@ -124,6 +124,69 @@ def _dt(dtype) -> int:
     return DTYPES[dtype]
 
 
+# ----------------------------------------------------------------- argument checks
+#
+# The C ABI takes raw device pointers with one row stride per list of shards,
+# so it cannot see a tensor's size, device or layout.  The binding checks them
+# before any call: shapes, dtypes and strides first, then that every tensor is
+# on the GPU (a host pointer handed to a kernel would be an illegal address).
+
+
+def _tensor(name: str, t, shape=None, dtypes=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {list(dtypes)}")
+    return t
+
+
+def _matrix(name: str, t, shape=None, dtypes=None) -> torch.Tensor:
+    """A row-major 2-D tensor (unit column stride, any row stride)."""
+    _tensor(name, t, shape, dtypes)
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1) or t.stride(0) < t.shape[1]:
+        raise ValueError(f"{name} must be a row-major matrix with unit column stride")
+    return t
+
+
+def _dense(name: str, t, shape=None, dtypes=None) -> torch.Tensor:
+    _tensor(name, t, shape, dtypes)
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _same_ld(name: str, ts: Sequence[torch.Tensor]) -> None:
+    lds = {t.stride(0) for t in ts}
+    if len(lds) > 1:
+        raise ValueError(f"every {name}[r] must have the same row stride (got {sorted(lds)})")
+
+
+def _shard_count(name: str, ts) -> int:
+    if ts is None or len(ts) < 1 or len(ts) > MAX_SHARDS:
+        raise ValueError(f"{name} must hold 1..{MAX_SHARDS} shards")
+    return len(ts)
+
+
+def _on_gpu(*groups) -> None:
+    """Every tensor (or list of tensors; None entries skipped) is a CUDA tensor of one device."""
+    devs = set()
+    for g in groups:
+        for t in (g if isinstance(g, (list, tuple)) else [g]):
+            if t is None:
+                continue
+            if not t.is_cuda:
+                raise ValueError("every tensor argument must be a CUDA tensor (the library has no CPU path)")
+            devs.add(t.device)
+    if len(devs) > 1:
+        raise ValueError(f"tensor arguments span devices {sorted(str(d) for d in devs)}")
+
+
+BF16 = (torch.bfloat16,)
+BF16_F32 = (torch.bfloat16, torch.float32)
+
+
 # ----------------------------------------------------------------- entry points
 
 def tp_abi_version() -> int:
@@ -136,16 +199,38 @@ def tp_linear_col(x: torch.Tensor, w: Sequence[torch.Tensor], *, act: str = "non
     """ColumnParallelLinear over t shards.  w[r] is [out/t, in] (act="none") or
     rank r's merged [gate; up] block [2*out/t, in].  Returns the list of
     per-shard outputs, or the gathered [n, out] tensor if gather_output."""
-    t = len(w)
-    n, k = x.shape
-    os_ = w[0].shape[0] // (2 if act != "none" else 1)
+    t = _shard_count("w", w)
+    n, k = _matrix("x", x, dtypes=BF16).shape
+    if act not in ACTS:
+        raise ValueError(f"act must be one of {list(ACTS)}")
+    rows = w[0].shape[0] if w[0].dim() == 2 else -1
+    for r in range(t):
+        _matrix(f"w[{r}]", w[r], (rows, k), BF16)
+    _same_ld("w", w)
+    gated = act != "none"
+    if gated and rows % 2:
+        raise ValueError("a gated weight block holds gate rows then as many up rows: its row count must be even")
+    os_ = rows // (2 if gated else 1)
     out_full = os_ * t
+    if bias is not None:
+        if len(bias) != t:
+            raise ValueError("bias must hold one vector per shard")
+        for r in range(t):
+            _dense(f"bias[{r}]", bias[r], (os_,), BF16)
     if y is None:
         if gather_output:
             y = torch.empty((n, out_full), dtype=y_dtype, device=x.device)
         else:
             y = [torch.empty((n, os_), dtype=y_dtype, device=x.device) for _ in range(t)]
     ys = [y] if gather_output else list(y)
+    if len(ys) != (1 if gather_output else t):
+        raise ValueError("y must be one tensor with gather_output, else one per shard")
+    for i, yi in enumerate(ys):
+        _matrix(f"y[{i}]", yi, (n, out_full if gather_output else os_), BF16_F32)
+    if len({yi.dtype for yi in ys}) > 1:
+        raise TypeError("every y[r] must have the same dtype")
+    _same_ld("y", ys)
+    _on_gpu(x, list(w), list(bias) if bias is not None else None, ys)
     ldy = _ld(ys[0])
     code = load().tp_linear_col(t, n, k, out_full, _ptr(x), _ld(x), _ptrs(w), _ld(w[0]), _ptrs(bias),
                                 ACTS[act], int(gather_output), _ptrs(ys), ldy, _dt(ys[0].dtype), _stream(stream))
@@ -159,14 +244,34 @@ def tp_linear_row(x: Sequence[torch.Tensor], w: Sequence[torch.Tensor], *, bias:
                   y_dtype=torch.bfloat16, stream=None):
     """RowParallelLinear: x[r] [n, in/t], w[r] [out, in/t].  Returns y (the
     all-reduced sum) when reduce_results, else the list of partials."""
-    t = len(w)
-    n, ks = x[0].shape
-    out = w[0].shape[0]
+    t = _shard_count("w", w)
+    if len(x) != t:
+        raise ValueError("x and w must hold the same number of shards")
+    n, ks = _matrix("x[0]", x[0], dtypes=BF16).shape
+    out = _matrix("w[0]", w[0], dtypes=BF16).shape[0]
+    for r in range(t):
+        _matrix(f"x[{r}]", x[r], (n, ks), BF16)
+        _matrix(f"w[{r}]", w[r], (out, ks), BF16)
+    _same_ld("x", x)
+    _same_ld("w", w)
+    if mode not in MODES:
+        raise ValueError(f"mode must be one of {list(MODES)}")
+    if bias is not None:
+        _dense("bias", bias, (out,), BF16)
     dev = x[0].device
     if mode != "fused" and partials is None:
         partials = [torch.empty((n, out), dtype=partial_dtype, device=dev) for _ in range(t)]
     if reduce_results and y is None:
         y = torch.empty((n, out), dtype=y_dtype, device=dev)
+    if partials is not None:
+        if len(partials) != t:
+            raise ValueError("partials must hold one buffer per shard")
+        for r in range(t):
+            _matrix(f"partials[{r}]", partials[r], (n, out), (partials[0].dtype,) if r else BF16_F32)
+        _same_ld("partials", partials)
+    if y is not None:
+        _matrix("y", y, (n, out), BF16_F32)
+    _on_gpu(list(x), list(w), bias, partials, y)
     ldp = _ld(partials[0]) if partials is not None else out
     pdt = partials[0].dtype if partials is not None else partial_dtype
     code = load().tp_linear_row(t, n, ks * t, out, _ptrs(x), _ld(x[0]), _ptrs(w), _ld(w[0]), _ptr(bias),
@@ -181,15 +286,47 @@ def tp_shard_reduce(partials: Sequence[torch.Tensor], *, out: Optional[torch.Ten
                     mode: str = "direct", hop_dtype=torch.float32, replicate: bool = False,
                     alloc_out: bool = True, stream=None):
     """All-reduce (sum) of t equally shaped partial buffers."""
-    t = len(partials)
-    p0 = partials[0]
+    t = _shard_count("partials", partials)
+    p0 = _dense("partials[0]", partials[0], dtypes=BF16_F32)
+    for r in range(t):
+        _dense(f"partials[{r}]", partials[r], tuple(p0.shape), (p0.dtype,))
+    if mode not in ("direct", "ring"):
+        raise ValueError("mode must be 'direct' or 'ring'")
     if out is None and alloc_out and not replicate:
         out = torch.empty(p0.shape, dtype=out_dtype or p0.dtype, device=p0.device)
+    if out is not None:
+        _dense("out", out, dtypes=BF16_F32)
+        if out.numel() != p0.numel():
+            raise ValueError(f"out holds {out.numel()} elements, the partials {p0.numel()}")
+    _on_gpu(list(partials), out)
     code = load().tp_shard_reduce(t, p0.numel(), _dt(p0.dtype), _ptrs(partials), _ptr(out),
                                   _dt(out.dtype) if out is not None else 0, MODES[mode], _dt(hop_dtype),
                                   int(replicate), _stream(stream))
     _check("tp_shard_reduce", code)
     return out
+
+
+def _mlp_args(x, w_gate_up, w_down, bias_down, act, mode):
+    """Shapes of the MLP entry points: returns (t, n, h, f)."""
+    t = _shard_count("w_gate_up", w_gate_up)
+    if len(w_down) != t:
+        raise ValueError("w_gate_up and w_down must hold the same number of shards")
+    if act not in ACTS or act == "none":
+        raise ValueError("act must be 'silu' or 'gelu_tanh' (the MLP is gated)")
+    if mode not in MODES:
+        raise ValueError(f"mode must be one of {list(MODES)}")
+    n, h = _matrix("x", x, dtypes=BF16).shape
+    rows = w_gate_up[0].shape[0] if w_gate_up[0].dim() == 2 else -1
+    if rows % 2:
+        raise ValueError("w_gate_up[r] holds gate rows then as many up rows: its row count must be even")
+    fs = rows // 2
+    for r in range(t):
+        _dense(f"w_gate_up[{r}]", w_gate_up[r], (2 * fs, h), BF16)
+        _matrix(f"w_down[{r}]", w_down[r], (h, fs), BF16)
+    _same_ld("w_down", w_down)
+    if bias_down is not None:
+        _dense("bias_down", bias_down, (h,), BF16)
+    return t, n, h, fs * t
 
 
 def tp_mlp_workspace_size(t: int, n: int, h: int, f: int, mode: str = "direct", partial_dtype=torch.bfloat16) -> int:
@@ -202,14 +339,15 @@ def tp_mlp_forward(x: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_down: S
                    y: Optional[torch.Tensor] = None, y_dtype=torch.bfloat16, stream=None):
     """Tensor-parallel MLP block Y = sum_r act(X A_r) B_r.  w_gate_up[r] is
     [2f/t, h] (gate rows then up rows), w_down[r] is [h, f/t]."""
-    t = len(w_gate_up)
-    n, h = x.shape
-    f = w_gate_up[0].shape[0] // 2 * t
-    need = tp_mlp_workspace_size(t, n, h, f, mode, partial_dtype)
+    t, n, h, f = _mlp_args(x, w_gate_up, w_down, bias_down, act, mode)
     if workspace is None:
+        need = tp_mlp_workspace_size(t, n, h, f, mode, partial_dtype)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
     if y is None:
         y = torch.empty((n, h), dtype=y_dtype, device=x.device)
+    _dense("workspace", workspace)
+    _dense("y", y, (n, h), BF16_F32)
+    _on_gpu(x, list(w_gate_up), list(w_down), bias_down, workspace, y)
     code = load().tp_mlp_forward(t, n, h, f, _ptr(x), _ld(x), _ptrs(w_gate_up), _ptrs(w_down), _ld(w_down[0]),
                                  _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _ptr(y), _dt(y.dtype), _stream(stream))
@@ -221,12 +359,32 @@ def vocab_parallel_embed(ids: torch.Tensor, table: Sequence[Optional[torch.Tenso
                          out: Optional[torch.Tensor] = None, partials: Optional[List[torch.Tensor]] = None,
                          stream=None):
     """Vocab-parallel embedding: table[r] holds rank r's rows (ceil rule)."""
-    t = len(table)
-    ref = next(tb for tb in table if tb is not None)
-    h = ref.shape[1]
+    t = _shard_count("table", table)
+    _dense("ids", ids, dtypes=(torch.int32,))
+    if ids.dim() != 1:
+        raise ValueError("ids must be a 1-D int32 tensor")
+    ref = next((tb for tb in table if tb is not None), None)
+    if ref is None:
+        raise ValueError("table holds no shard")
+    h = _dense("table shard", ref, dtypes=BF16_F32).shape[1] if ref.dim() == 2 else -1
+    per = (vocab + t - 1) // t
+    for r in range(t):
+        rows_r = max(0, min((r + 1) * per, vocab) - min(r * per, vocab))
+        if table[r] is None:
+            if rows_r:
+                raise ValueError(f"table[{r}] is None but rank {r} owns {rows_r} ids")
+            continue
+        _dense(f"table[{r}]", table[r], (rows_r, h), (ref.dtype,))
     n = ids.numel()
     if out is None:
         out = torch.empty((n, h), dtype=ref.dtype, device=ids.device)
+    _dense("out", out, (n, h), (ref.dtype,))
+    if partials is not None:
+        if len(partials) != t:
+            raise ValueError("partials must hold one buffer per shard")
+        for r in range(t):
+            _dense(f"partials[{r}]", partials[r], (n, h), (ref.dtype,))
+    _on_gpu(ids, list(table), out, partials)
     code = load().vocab_parallel_embed(t, vocab, h, _ptr(ids), n, _ptrs(table), _dt(ref.dtype), _ptr(out),
                                        _ptrs(partials), _stream(stream))
     _check("vocab_parallel_embed", code)
@@ -238,19 +396,32 @@ def lm_head_sharded(x: torch.Tensor, table: Sequence[Optional[torch.Tensor]], vo
                     shard_logits: Optional[List[torch.Tensor]] = None, out_dtype=torch.bfloat16, stream=None):
     """Vocab-sharded LM head.  Returns the concatenated [n, vocab] logits, or
     the per-shard logits when per_shard=True."""
-    t = len(table)
-    n, h = x.shape
+    t = _shard_count("table", table)
+    n, h = _matrix("x", x, dtypes=BF16).shape
+    per = (vocab + t - 1) // t
+    widths = [max(0, min((r + 1) * per, vocab) - min(r * per, vocab)) for r in range(t)]
+    for r in range(t):
+        if table[r] is None:
+            if widths[r]:
+                raise ValueError(f"table[{r}] is None but rank {r} owns {widths[r]} ids")
+            continue
+        _dense(f"table[{r}]", table[r], (widths[r], h), BF16)
     if per_shard:
         if shard_logits is None:
-            per = (vocab + t - 1) // t
-            widths = [max(0, min((r + 1) * per, vocab) - min(r * per, vocab)) for r in range(t)]
             shard_logits = [torch.empty((n, wd), dtype=out_dtype, device=x.device) for wd in widths]
+        if len(shard_logits) != t:
+            raise ValueError("shard_logits must hold one buffer per shard")
+        for r in range(t):
+            _dense(f"shard_logits[{r}]", shard_logits[r], (n, widths[r]), (shard_logits[0].dtype,) if r else BF16_F32)
+        _on_gpu(x, list(table), list(shard_logits))
         code = load().lm_head_sharded(t, n, h, vocab, _ptr(x), _ld(x), _ptrs(table), None, 0,
                                       _ptrs(shard_logits), _dt(shard_logits[0].dtype), _stream(stream))
         _check("lm_head_sharded", code)
         return shard_logits
     if logits is None:
         logits = torch.empty((n, vocab), dtype=out_dtype, device=x.device)
+    _matrix("logits", logits, (n, vocab), BF16_F32)
+    _on_gpu(x, list(table), logits)
     code = load().lm_head_sharded(t, n, h, vocab, _ptr(x), _ld(x), _ptrs(table), _ptr(logits), _ld(logits),
                                   None, _dt(logits.dtype), _stream(stream))
     _check("lm_head_sharded", code)
@@ -259,11 +430,20 @@ def lm_head_sharded(x: torch.Tensor, table: Sequence[Optional[torch.Tensor]], vo
 
 def tp_shard_gather(shards: Sequence[torch.Tensor], *, out: Optional[torch.Tensor] = None, stream=None):
     """Concatenate t [rows, cols_r] shards along the last dimension."""
-    t = len(shards)
-    rows = shards[0].shape[0]
+    t = _shard_count("shards", shards)
+    s0 = _dense("shards[0]", shards[0], dtypes=BF16_F32)
+    if s0.dim() != 2:
+        raise ValueError("shards must be 2-D")
+    rows = s0.shape[0]
+    for r in range(t):
+        _dense(f"shards[{r}]", shards[r], dtypes=(s0.dtype,))
+        if shards[r].dim() != 2 or shards[r].shape[0] != rows:
+            raise ValueError(f"shards[{r}] must be [{rows}, cols_r]")
     cols = (ctypes.c_int64 * t)(*[s.shape[1] for s in shards])
     if out is None:
         out = torch.empty((rows, sum(s.shape[1] for s in shards)), dtype=shards[0].dtype, device=shards[0].device)
+    _dense("out", out, (rows, sum(s.shape[1] for s in shards)), (s0.dtype,))
+    _on_gpu(list(shards), out)
     code = load().tp_shard_gather(t, rows, cols, _dt(shards[0].dtype), _ptrs(shards), _ptr(out), _stream(stream))
     _check("tp_shard_gather", code)
     return out
@@ -311,11 +491,11 @@ def tp_mlp_forward_static(x: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_
     device array (see include/tp.h).  Pass `y` to keep this call free of
     allocations as well; requests larger than the array raise TPError
     (TP_ERR_WORKSPACE)."""
-    t = len(w_gate_up)
-    n, h = x.shape
-    f = w_gate_up[0].shape[0] // 2 * t
+    t, n, h, f = _mlp_args(x, w_gate_up, w_down, bias_down, act, mode)
     if y is None:
         y = torch.empty((n, h), dtype=y_dtype, device=x.device)
+    _dense("y", y, (n, h), BF16_F32)
+    _on_gpu(x, list(w_gate_up), list(w_down), bias_down, y)
     code = load().tp_mlp_forward_static(t, n, h, f, _ptr(x), _ld(x), _ptrs(w_gate_up), _ptrs(w_down),
                                         _ld(w_down[0]), _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype),
                                         _ptr(y), _dt(y.dtype), _stream(stream))
@@ -330,10 +510,16 @@ def tp_mlp_forward_host(x_host: torch.Tensor, w_gate_up: Sequence[torch.Tensor],
     """tp_mlp_forward on pinned host activations with chunked, overlapped
     copies (see include/tp.h).  Returns y_host; the work is complete when
     `stream` is."""
-    assert x_host.is_pinned() and y_host.is_pinned(), "host buffers must be page-locked"
-    t = len(w_gate_up)
-    n, h = x_host.shape
-    f = w_gate_up[0].shape[0] // 2 * t
+    if not (isinstance(x_host, torch.Tensor) and isinstance(y_host, torch.Tensor)
+            and x_host.is_pinned() and y_host.is_pinned()):
+        raise ValueError("x_host and y_host must be page-locked host tensors")
+    t, n, h, f = _mlp_args(x_dev, w_gate_up, w_down, bias_down, act, mode)
+    _dense("x_host", x_host, (n, h), BF16)
+    _dense("x_dev", x_dev, (n, h), BF16)
+    _dense("y_host", y_host, (n, h), BF16_F32)
+    _dense("y_dev", y_dev, (n, h), (y_host.dtype,))
+    _dense("workspace", workspace)
+    _on_gpu(x_dev, list(w_gate_up), list(w_down), bias_down, y_dev, workspace)
     if copy_stream is None:
         copy_stream = torch.cuda.Stream(device=x_dev.device)
     code = load().tp_mlp_forward_host(t, n, h, f, _ptr(x_host), _ptrs(w_gate_up), _ptrs(w_down), _ld(w_down[0]),
@@ -350,10 +536,24 @@ def tp_reduce_scatter_rmsnorm(partials: Sequence[torch.Tensor], weight: torch.Te
                               stream=None):
     """Sequence-parallel reduce-scatter + residual add + RMSNorm (all-gather
     in place).  Returns (residual_out or None, out)."""
-    t = len(partials)
-    n, h = partials[0].shape
+    t = _shard_count("partials", partials)
+    p0 = _dense("partials[0]", partials[0], dtypes=BF16_F32)
+    if p0.dim() != 2:
+        raise ValueError("partials must be [n, h]")
+    n, h = p0.shape
+    for r in range(t):
+        _dense(f"partials[{r}]", partials[r], (n, h), (p0.dtype,))
+    if mode not in ("direct", "ring"):
+        raise ValueError("mode must be 'direct' or 'ring'")
+    _dense("weight", weight, (h,), BF16)
+    if residual is not None:
+        _dense("residual", residual, (n, h), BF16)
+    if residual_out is not None:
+        _dense("residual_out", residual_out, (n, h), BF16)
     if out is None:
         out = torch.empty((n, h), dtype=torch.bfloat16, device=partials[0].device)
+    _dense("out", out, (n, h), BF16)
+    _on_gpu(list(partials), weight, residual, residual_out, out)
     code = load().tp_reduce_scatter_rmsnorm(t, n, h, _dt(partials[0].dtype), _ptrs(partials), _ptr(residual),
                                             _ptr(weight), eps, MODES[mode], _ptr(residual_out), _ptr(out),
                                             _stream(stream))

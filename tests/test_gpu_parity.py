@@ -127,7 +127,8 @@ def test_row_worked_example_from_page():
     x[0, 8:10] = 1
     b = torch.tensor([10, 20], dtype=torch.bfloat16, device=DEV)
     parts = tp.tp_linear_row([x[:, :8], x[:, 8:]], [W[:, :8], W[:, 8:]], bias=b, reduce_results=False,
-                             partial_dtype=torch.float32, partials=[torch.empty((1, 4), device=DEV) for _ in range(2)])
+                             partial_dtype=torch.float32,
+                             partials=[torch.empty((1, 4), device=DEV)[:, :2] for _ in range(2)])   # row stride 4
     torch.cuda.synchronize()
     assert parts[0][:, :2].tolist() == [[13.0, 31.0]] and parts[1][:, :2].tolist() == [[7.0, 15.0]]
 
