@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401
     tp_linear_row,
     tp_mlp_forward,
     tp_mlp_forward_host,
+    tp_mlp_forward_static,
     tp_mlp_workspace_size,
     tp_reduce_scatter_rmsnorm,
     tp_reset_collective_count,
