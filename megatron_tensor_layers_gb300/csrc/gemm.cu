@@ -1502,13 +1502,18 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
         }
     }
     if (d.force_bn) best = d.force_bn;
-    // CTA pairs for problems with at least two full waves of 256-row tiles.
+    // CTA pairs whenever they need no more waves than single CTAs with the same tile width
+    // (a pair tile holds 256 rows on two SMs, a single-CTA tile 128 rows on one; per wave the
+    // pair kernel does the same work per SM at a higher tensor-pipe rate).  Measured on the 70B
+    // MLP: pairs win at n = 256 (3 waves either way) and 512, lose at n = 128 and for the down
+    // GEMM at n = 384, where they would add a wave.
     bool pair = false;
     if (d.pair >= 0 && sms >= 2) {
         const int out_cols = glu ? 128 : 256;
-        const long long pair_tiles = static_cast<long long>(d.groups) * ((d.M + 255) / 256) *
-                                     ((d.N + out_cols - 1) / out_cols);
-        pair = d.pair > 0 || (d.M >= 512 && pair_tiles >= 2LL * (sms / 2) && d.force_bn == 0);
+        const long long col_tiles = static_cast<long long>(d.groups) * ((d.N + out_cols - 1) / out_cols);
+        const long long pair_waves = (col_tiles * ((d.M + 255) / 256) + sms / 2 - 1) / (sms / 2);
+        const long long single_waves = (col_tiles * ((d.M + 127) / 128) + sms - 1) / sms;
+        pair = d.pair > 0 || (d.M > 128 && d.force_bn == 0 && pair_waves <= single_waves);
     }
     if (pair) {
         if (glu) return launch_pair<kPairStages, EPI_GLU, kPairKsub>(a, d, stream);
