@@ -109,6 +109,23 @@ def test_decode_all_rows(mlp70b, n, mode):
     gemm_gate(f64(y), ref, bf16_out=False, extra=extra)
 
 
+@pytest.mark.parametrize("n", [200, 256, 300])
+def test_mid_size_all_rows(mlp70b, n):
+    """Chunked-prefill sizes between decode and the bench's 8192 tokens, where the
+    kernel choice switches between CTA pairs (200, 256: one ragged or full 256-row
+    tile) and single CTAs (300)."""
+    d = mlp70b
+    t = 4
+    wgu, wds = _shards(d, t)
+    x = d["x"][:n].contiguous()
+    y = tp.tp_mlp_forward(x, wgu, wds, mode="direct", partial_dtype=torch.float32, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    rows = [0, 127, 128, n - 1]
+    ref, extra = _reference(f64(x[rows]), d["host"], t, partial_bf16=False)
+    gemm_gate(f64(y[rows]), ref, bf16_out=False, extra=extra)
+
+
 @pytest.mark.parametrize("t", [2, 4, 8])
 def test_shard_reduce_largest_windows(t):
     count = NTOK * H
