@@ -1,4 +1,4 @@
-"""Randomized parity sweep over the GEMM entry points.
+"""Randomized parity sweep over the GEMM, embedding, LM-head and gather entry points.
 
 Seeded random shapes (shard count, tokens, K, output width, all ragged
 against the tiles), output dtypes, gather/bias options, reduce orders and the
@@ -6,7 +6,10 @@ kernel-selection knobs (CTA pairs, split-K clusters, tile width) drive the
 column and row linears through every GEMM kernel and epilogue.  Inputs are
 small integers, so every fp32 result is exact and a bf16 result is the exact
 value rounded once: both are compared bit for bit with the CPU oracle.  The
-gated column GEMM (SiLU is transcendental) uses the float gate.
+gated column GEMM (SiLU is transcendental) uses the float gate.  The
+embedding (bf16 and fp32 tables, ids out of range, t > V) and the LM head
+with its gather (ragged vocab, so shards start mid-line in the logits) are
+swept the same way, bit-exact.
 """
 
 import random
@@ -137,3 +140,52 @@ def test_gated_column_random(i):
         wf = f64(wgu[r])
         ref = O.glu(O.linear(xf, wf[:os_]), O.linear(xf, wf[os_:]), act)
         gemm_gate(f64(hs[r]), ref, bf16_out=True)
+
+
+def _vocab_case(i):
+    rnd = random.Random(5000 + i)
+    t = rnd.choice([1, 2, 3, 4, 5, 8])
+    vocab = rnd.choice([1, 2, 3, 7, 50, 101, 1000, 4097])
+    h = 8 * rnd.randint(1, 40)
+    n = rnd.choice([1, 5, 64, 300, 1025])
+    return t, vocab, h, n, 6000 + 20 * i
+
+
+def _vocab_shards(table, vocab, t):
+    out = []
+    for r in range(t):
+        s, e = O.vocab_range(vocab, t, r)
+        out.append(table[s:e].contiguous() if e > s else None)
+    return out
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_vocab_embed_random(i):
+    t, vocab, h, n, s = _vocab_case(i)
+    dtype = torch.bfloat16 if i % 2 == 0 else torch.float32
+    table = synth.normal_f32((vocab, h), 1.0, s, device=DEV).to(dtype)
+    ids = (synth.uniform_ids(n, vocab + 6, s + 1, device=DEV) - 3).to(torch.int32)   # some ids out of range
+    parts = [torch.empty((n, h), dtype=dtype, device=DEV) for _ in range(t)]
+    out = tp.vocab_parallel_embed(ids, _vocab_shards(table, vocab, t), vocab, partials=parts)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    ref, refp = O.vocab_parallel_embedding(ids.cpu().numpy(), f64(table), t)
+    assert np.array_equal(f64(out), ref), (t, vocab, h, n)
+    for r in range(t):
+        assert np.array_equal(f64(parts[r]), refp[r]), (t, vocab, h, n, r)
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_lm_head_and_gather_random(i):
+    t, vocab, h, n, s = _vocab_case(100 + i)   # ragged vocab: shards start mid-line in the logits
+    x = ints((n, h), s)
+    table = ints((vocab, h), s + 1)
+    shards = _vocab_shards(table, vocab, t)
+    logits = tp.lm_head_sharded(x, shards, vocab, out_dtype=torch.float32)
+    per_shard = tp.lm_head_sharded(x, shards, vocab, per_shard=True, out_dtype=torch.float32)
+    gathered = tp.tp_shard_gather([p for p in per_shard if p.shape[1] > 0])
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    ref = O.linear(f64(x), f64(table))
+    assert np.array_equal(f64(logits), ref), (t, vocab, h, n)
+    assert np.array_equal(f64(gathered), ref), (t, vocab, h, n)
