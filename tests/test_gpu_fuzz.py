@@ -9,7 +9,9 @@ value rounded once: both are compared bit for bit with the CPU oracle.  The
 gated column GEMM (SiLU is transcendental) uses the float gate.  The
 embedding (bf16 and fp32 tables, ids out of range, t > V) and the LM head
 with its gather (ragged vocab, so shards start mid-line in the logits) are
-swept the same way, bit-exact.
+swept the same way, bit-exact, and so is the shard reduce (odd counts, any t,
+both orders, bf16 or fp32 wire, replication) against the oracle's emulation of
+the same fold order.
 """
 
 import random
@@ -189,3 +191,36 @@ def test_lm_head_and_gather_random(i):
     ref = O.linear(f64(x), f64(table))
     assert np.array_equal(f64(logits), ref), (t, vocab, h, n)
     assert np.array_equal(f64(gathered), ref), (t, vocab, h, n)
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_shard_reduce_random(i):
+    """Random counts (odd, below one vector, across ring-chunk boundaries), shard counts,
+    dtypes, orders, wire dtypes and replication, against the oracle's emulation of the
+    same fold order (message-passing ring for RING)."""
+    rnd = random.Random(7000 + i)
+    t = rnd.choice([1, 2, 3, 4, 5, 7, 8])
+    count = rnd.choice([1, 3, 7, 8, 9, 63, 1000, 4099, 65537, 200003])
+    dtype = rnd.choice([torch.bfloat16, torch.float32])
+    mode = rnd.choice(["direct", "ring"])
+    hop = torch.bfloat16 if (mode == "ring" and dtype == torch.bfloat16 and rnd.random() < 0.5) else torch.float32
+    replicate = rnd.random() < 0.3
+    out_dtype = torch.float32 if rnd.random() < 0.5 else dtype
+    parts = [synth.normal_f32((count,), 1.0, 7100 + 10 * i + r, device=DEV).to(dtype) for r in range(t)]
+    pf = [f64(p) for p in parts]
+    out = tp.tp_shard_reduce(parts, mode=mode, hop_dtype=hop, replicate=replicate, out_dtype=out_dtype,
+                             alloc_out=not replicate)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    if mode == "direct":
+        ref = O.reduce_direct_f32(pf)
+    else:
+        ref = O.ring_allreduce(pf, hop="bf16" if hop == torch.bfloat16 else "f32")[0][0]
+    case = (t, count, dtype, mode, hop, replicate, out_dtype)
+    if out is not None:
+        want = O.round_to_bf16(ref) if out_dtype == torch.bfloat16 else ref
+        assert np.array_equal(f64(out), want), case
+    if replicate:
+        want = O.round_to_bf16(ref) if dtype == torch.bfloat16 else ref
+        for r in range(t):
+            assert np.array_equal(f64(parts[r]), want), (case, r)
