@@ -410,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                     __syncwarp();
                     const int col = n * (BN / 2) + c * 32 + lane;
                     if (col < ncols) {
-#pragma unroll 1
+                        // rows are independent: unrolled, their activation chains overlap
+#pragma unroll 4
                         for (int r = 0; r < live; ++r)
                             store_one(out, args.ldo, args.out_f32, row0 + r, col,
                                       act_fn(st[r * Cfg::STG_ROW + lane], args.act) * st[r * Cfg::STG_ROW + 32 + lane]);
