@@ -7,7 +7,8 @@ sides of a 128-row tile boundary included) in fp64 from the same bits.
 Output rows depend only on their own input row, so a sample is a complete
 check of those rows.  The shard reduce at its largest size is compared bit
 for bit with the oracle's emulation on windows around every ring-chunk
-boundary, and the LM head at its configured size on sampled rows.
+boundary, the LM head at its configured size on sampled rows, and the
+attention block's QKV and o_proj projections at the same model's shapes.
 """
 
 import numpy as np
@@ -192,3 +193,38 @@ def test_reduce_scatter_rmsnorm_bench_size(order):
     normed = O.rmsnorm(xr, f64(w), 1e-6)
     assert np.all(np.abs(f64(out[rows]) - normed) <= half_ulp_bf16(normed) + 1e-4 * np.abs(normed) + 1e-6)
     assert np.all(np.abs(f64(res_out[rows]) - xr) <= half_ulp_bf16(xr) + 1e-5 * np.abs(xr))
+
+
+@pytest.mark.parametrize("n", [1, 64, 1024])
+def test_attention_projections_70b_t8(n):
+    """The attention block's tensor-parallel projections at Llama-3.1-70B shapes (64 query
+    heads, 8 KV heads, head size 128, h = 8192) over t = 8: the head-aligned QKV
+    column GEMM (each rank: 8 query heads, 1 KV head) and the o_proj row GEMM over the
+    ranks' attention outputs with the reduce, on sampled rows.  The attention itself is
+    not part of the path: the o_proj input is a seeded stand-in for it."""
+    build()
+    tp.load()
+    t, nh, nkv, hd, h = 8, 64, 8, 128, 8192
+    x = synth.normal_bf16((n, h), 1.0, 800, device=DEV)
+    wq = synth.normal_bf16((nh * hd, h), 0.02, 801, device=DEV)
+    wk = synth.normal_bf16((nkv * hd, h), 0.02, 802, device=DEV)
+    wv = synth.normal_bf16((nkv * hd, h), 0.02, 803, device=DEV)
+    wo = synth.normal_bf16((h, nh * hd), 0.02, 804, device=DEV)
+    qh = nh // t * hd
+    blocks = [torch.cat([wq[r * qh:(r + 1) * qh], wk[r * hd:(r + 1) * hd], wv[r * hd:(r + 1) * hd]]).contiguous()
+              for r in range(t)]
+    qkv = tp.tp_linear_col(x, blocks, y_dtype=torch.float32)
+    attn = [synth.normal_bf16((n, qh), 1.0, 810 + r, device=DEV) for r in range(t)]
+    wos = [wo[:, r * qh:(r + 1) * qh].contiguous() for r in range(t)]
+    y = tp.tp_linear_row(attn, wos, mode="direct", partial_dtype=torch.float32, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    rows = sorted(set([0, n // 2, n - 1]))
+    xf = f64(x[rows])
+    wqf, wkf, wvf = f64(wq), f64(wk), f64(wv)
+    for r in range(t):
+        blk = O.qkv_shard(wqf, wkf, wvf, nh, nkv, hd, t, r)
+        gemm_gate(f64(qkv[r][rows]), O.linear(xf, blk), bf16_out=False)
+    wof = f64(wo)
+    parts = [O.linear(f64(attn[r][rows]), O.row_shard(wof, t, r)) for r in range(t)]
+    gemm_gate(f64(y[rows]), O.reduce_direct(parts), bf16_out=False)
