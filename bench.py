@@ -321,7 +321,7 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
-DETAIL_ROWS = ("prefill", "decode", "prefill_t8", "reduce_sweep", "seqpar", "embed", "lm_head", "tiny")
+DETAIL_ROWS = ("prefill", "decode", "prefill_t8", "reduce_sweep", "seqpar", "embed", "lm_head", "tiny", "attn")
 
 
 def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
@@ -346,6 +346,55 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
         out.update(_detail_vocab(torch, tp, synth, dev, hbm, ten, rows))
     if "tiny" in rows:
         out.update(_detail_tiny(torch, tp, synth, dev))
+    if "attn" in rows:
+        out.update(_detail_attn(torch, tp, synth, dev, hbm, ten))
+    return out
+
+
+def _detail_attn(torch, tp, synth, dev, hbm, ten):
+    """The attention block's tensor-parallel projections at Llama-3.1-70B shapes, t=8
+    (64 query heads, 8 KV heads, head size 128, h=8192): the head-aligned QKV column GEMM
+    (rank r: 8 query heads and 1 KV head, [1280, 8192]) and the o_proj row GEMM ([8192,
+    1024] per rank) into bf16 partials with the direct reduce.  The attention between them
+    is not part of the path; o_proj reads a seeded stand-in.  Decode (n=1, 64) is weight
+    streaming, timed as CUDA graphs over two weight copies (2 x 302 MB, beyond the L2);
+    prefill (n=8192) is compared with the tensor peak."""
+    out = {}
+    t, nh, nkv, hd, h = 8, 64, 8, 128, 8192
+    qh = nh // t * hd
+    wbytes = (t * (qh + 2 * hd) * h + h * nh * hd) * 2
+
+    def weights(seed):
+        blocks = [synth.normal_bf16((qh + 2 * hd, h), 0.02, seed + r, device=dev) for r in range(t)]
+        wos = [synth.normal_bf16((h, qh), 0.02, seed + 20 + r, device=dev) for r in range(t)]
+        return blocks, wos
+
+    copies = [weights(900), weights(950)]
+    for n in (1, 64, 8192):
+        x = synth.normal_bf16((n, h), 1.0, 990, device=dev)
+        attn = [synth.normal_bf16((n, qh), 1.0, 991 + r, device=dev) for r in range(t)]
+        qkv = [torch.empty((n, qh + 2 * hd), dtype=torch.bfloat16, device=dev) for _ in range(t)]
+        parts = [torch.empty((n, h), dtype=torch.bfloat16, device=dev) for _ in range(t)]
+        y = torch.empty((n, h), dtype=torch.bfloat16, device=dev)
+
+        def proj(c):
+            def run():
+                tp.tp_linear_col(x, c[0], y=qkv)
+                tp.tp_linear_row(attn, c[1], partials=parts, y=y)
+            return run
+
+        if n < 8192:
+            gs = graph_time_cold(torch, [proj(c) for c in copies], 5)
+            if gs:
+                out[f"attn_proj_t8_n{n}"] = {"graph_us": gs * 1e6, "weight_GBps": wbytes / gs / 1e9,
+                                             "graph_hbm_frac": wbytes / gs / 1e9 / hbm}
+        else:
+            s = time_fn(torch, proj(copies[0]), 10)
+            fl = 2.0 * n * h * (t * (qh + 2 * hd)) + 2.0 * n * h * (nh * hd)
+            out[f"attn_proj_t8_n{n}"] = {"ms": s * 1e3, "tflops": fl / s / 1e12, "frac": fl / s / 1e12 / ten}
+        del x, attn, qkv, parts, y
+    del copies
+    torch.cuda.empty_cache()
     return out
 
 
