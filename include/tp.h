@@ -377,10 +377,11 @@ uint64_t tp_collective_count(void);
 void tp_reset_collective_count(void);
 
 /*
- * Width of the GEMM output tile (the tcgen05 MMA N: 64, 128 or 256) used by
- * every later GEMM launch of this process; 0 restores the automatic choice
- * (a cost model over whole waves of tiles).  For tests and tuning.  Returns
- * TP_ERR_INVALID_ARG for any other value.
+ * Width of the GEMM output tile (the tcgen05 MMA N: 64, 96, 128 or 256) used
+ * by every later GEMM launch of this process; 0 restores the automatic choice
+ * (a cost model over whole waves of tiles).  96 applies to GEMMs without the
+ * gated epilogue (a gated GEMM given 96 uses 128).  For tests and tuning.
+ * Returns TP_ERR_INVALID_ARG for any other value.
  */
 tp_status tp_set_gemm_tile_n(int n);
 

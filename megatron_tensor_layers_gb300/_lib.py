@@ -478,7 +478,7 @@ def tp_set_gemm_split(mode: int, max_clusters: int = 0) -> None:
 
 
 def tp_set_gemm_tile_n(n: int) -> None:
-    """Force the GEMM tile width (64/128/256) for later launches; 0 = automatic."""
+    """Force the GEMM tile width (64/96/128/256) for later launches; 0 = automatic."""
     _check("tp_set_gemm_tile_n", load().tp_set_gemm_tile_n(n))
 
 

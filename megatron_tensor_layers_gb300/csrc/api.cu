@@ -525,7 +525,7 @@ tp_status tp_device_status(tp_stream stream) {
 }
 
 tp_status tp_set_gemm_tile_n(int n) {
-    if (n != 0 && n != 64 && n != 128 && n != 256) return TP_ERR_INVALID_ARG;
+    if (n != 0 && n != 64 && n != 96 && n != 128 && n != 256) return TP_ERR_INVALID_ARG;
     g_tile_n.store(n);
     return TP_OK;
 }

@@ -189,14 +189,14 @@ struct GemmCfg {
     static constexpr int A_BYTES = AROWS * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int TMEM_COLS = 2 * BN;                 // two accumulators
+    static constexpr int TMEM_COLS = 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;   // two accumulators
     static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
     static constexpr int STG_ROW = 65;
     static constexpr int STG_BYTES = (EPI == EPI_GLU && AROWS < BM) ? 2 * 32 * STG_ROW * 4 : 0;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES;
     static constexpr int OUT_COLS = (EPI == EPI_GLU) ? BN / 2 : BN;   // output columns per tile
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
-    static_assert(BN % 16 == 0 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
+    static_assert(BN % 32 == 0 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256; epilogue chunks of 32");
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(AROWS == BM || (AROWS == 64 && B_BYTES >= 64 * BK * 2),
                   "a 64-row A tile needs at least 64 rows of B behind it in the stage");
@@ -1489,11 +1489,15 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
 
     const int sms = std::max(1, sm_count());
     const bool glu = d.glu != 0;
-    // Candidate MMA widths, largest first; pick the one with the lowest cost.
-    const int cands[3] = {256, 128, 64};
+    // Candidate MMA widths, largest first; pick the one with the lowest cost.  96 (store
+    // epilogue only: a gated tile splits into gate and up halves of whole 32-column chunks)
+    // spreads a narrow weight over more SMs, e.g. 112 tiles instead of 80 for the 1280-row
+    // QKV blocks of 8 ranks.
+    const int cands[4] = {256, 128, 96, 64};
     int best = 256;
     long long best_cost = -1;
     for (int bn : cands) {
+        if (glu && bn == 96) continue;
         const int out_cols = glu ? bn / 2 : bn;
         const int tiles = d.groups * a.m_tiles * static_cast<int>((d.N + out_cols - 1) / out_cols);
         const long long c = plan_cost(tiles, bn, sms);
@@ -1502,7 +1506,7 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
             best = bn;
         }
     }
-    if (d.force_bn) best = d.force_bn;
+    if (d.force_bn) best = (glu && d.force_bn == 96) ? 128 : d.force_bn;
     // CTA pairs whenever they need no more waves than single CTAs with the same tile width
     // (a pair tile holds 256 rows on two SMs, a single-CTA tile 128 rows on one; per wave the
     // pair kernel does the same work per SM at a higher tensor-pipe rate).  Measured on the 70B
@@ -1538,6 +1542,7 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
         }
         if (best == 256) return launch_cfg<256, 5, EPI_STORE, 64>(a, d, stream);
         if (best == 128) return launch_cfg<128, 8, EPI_STORE, 64, 2>(a, d, stream);
+        if (best == 96) return launch_cfg<96, 10, EPI_STORE, 64, 2>(a, d, stream);
         return launch_cfg<64, 12, EPI_STORE, 64, 4>(a, d, stream);
     }
     if (glu) {
@@ -1547,6 +1552,7 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     }
     if (best == 256) return launch_cfg<256, 4, EPI_STORE>(a, d, stream);
     if (best == 128) return launch_cfg<128, 6, EPI_STORE>(a, d, stream);
+    if (best == 96) return launch_cfg<96, 8, EPI_STORE>(a, d, stream);
     return launch_cfg<64, 8, EPI_STORE>(a, d, stream);
 }
 

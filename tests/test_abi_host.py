@@ -107,14 +107,14 @@ def test_tuning_knobs_through_the_binding(lib):
     from megatron_tensor_layers_gb300 import TPError, tp_set_gemm_cta_pair, tp_set_gemm_split, tp_set_gemm_tile_n
     for mode in (1, -1, 0):
         tp_set_gemm_cta_pair(mode)
-    for n in (64, 128, 256, 0):
+    for n in (64, 96, 128, 256, 0):
         tp_set_gemm_tile_n(n)
     for mode, cap in ((1, 3), (-1, 0), (0, 0)):
         tp_set_gemm_split(mode, cap)
     with pytest.raises(TPError):
         tp_set_gemm_cta_pair(2)
     with pytest.raises(TPError):
-        tp_set_gemm_tile_n(96)
+        tp_set_gemm_tile_n(80)
     with pytest.raises(TPError):
         tp_set_gemm_split(2)
     with pytest.raises(TPError):

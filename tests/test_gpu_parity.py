@@ -446,7 +446,7 @@ def tile_n(request):
     tp.tp_set_gemm_tile_n(0)
 
 
-@pytest.mark.parametrize("tile_n", [64, 128, 256], indirect=True)
+@pytest.mark.parametrize("tile_n", [64, 96, 128, 256], indirect=True)
 def test_every_tile_width_integer_exact(tile_n):
     # plain column GEMM: ragged M (300), N (200 per shard), K (8 blocks + 24)
     t, n, k, os_ = 2, 300, 536, 200
@@ -466,7 +466,7 @@ def test_every_tile_width_integer_exact(tile_n):
     exact(f64(yd), ref)
 
 
-@pytest.mark.parametrize("tile_n", [64, 128, 256], indirect=True)
+@pytest.mark.parametrize("tile_n", [64, 96, 128, 256], indirect=True)
 def test_every_tile_width_gated(tile_n):
     t, n, h, fs = 2, 260, 320, 200
     x = normal((n, h), 1.0, 120)
