@@ -416,6 +416,19 @@ tp_status tp_set_gemm_split(int mode, int max_clusters);
  */
 tp_status tp_debug_expire_wait(uint64_t limit_ns, tp_stream stream);
 
+/*
+ * Test hook for the host-side kernel choice (no CUDA call): the GEMM kernel
+ * the library would launch, with the automatic settings, for M rows, an
+ * output of N columns per group (per shard), K per segment, `groups`
+ * independent outputs or `segs` K segments summed into one (the fused
+ * reduce; not both), a gated epilogue or not, on a GPU with `sms` SMs.
+ * Writes kind (0: single-CTA tiles, 1: CTA pairs, 2: split-K clusters), the
+ * output tile width (the MMA N) and the cluster size (split-K only, else 0).
+ * TP_ERR_INVALID_ARG for sizes or counts out of range or null outputs.
+ */
+tp_status tp_debug_gemm_plan(int64_t m, int64_t n, int64_t k, int groups, int segs, int gated, int sms,
+                             int* kind, int* tile_n, int* cluster);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,7 +33,7 @@ EXPORTED = [
     "tp_mlp_workspace_size", "tp_mlp_forward", "vocab_parallel_embed", "lm_head_sharded",
     "tp_shard_gather", "tp_device_status", "tp_collective_count", "tp_reset_collective_count",
     "tp_debug_expire_wait", "tp_set_gemm_tile_n", "tp_mlp_forward_static", "tp_set_gemm_cta_pair", "tp_mlp_forward_host",
-    "tp_reduce_scatter_rmsnorm", "tp_set_gemm_split",
+    "tp_reduce_scatter_rmsnorm", "tp_set_gemm_split", "tp_debug_gemm_plan",
 ]
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -73,6 +73,7 @@ def load() -> ctypes.CDLL:
         "tp_collective_count": (ctypes.c_uint64, []),
         "tp_reset_collective_count": (None, []),
         "tp_debug_expire_wait": (I32, [ctypes.c_uint64, P]),
+        "tp_debug_gemm_plan": (I32, [I64, I64, I64, I32, I32, I32, I32, P, P, P]),
         "tp_set_gemm_tile_n": (I32, [I32]),
         "tp_set_gemm_cta_pair": (I32, [I32]),
         "tp_set_gemm_split": (I32, [I32, I32]),
@@ -459,6 +460,16 @@ def tp_collective_count() -> int:
 
 def tp_reset_collective_count() -> None:
     load().tp_reset_collective_count()
+
+
+def tp_debug_gemm_plan(m: int, n: int, k: int, *, groups: int = 1, segs: int = 1, gated: bool = False,
+                       sms: int = 152):
+    """The GEMM kernel the library would choose (host logic only): returns
+    (kind, tile_n, cluster) with kind "single", "pair" or "split"."""
+    kind, bn, cs = I32(), I32(), I32()
+    _check("tp_debug_gemm_plan", load().tp_debug_gemm_plan(m, n, k, groups, segs, int(gated), sms, ctypes.byref(kind),
+                                                           ctypes.byref(bn), ctypes.byref(cs)))
+    return ("single", "pair", "split")[kind.value], bn.value, cs.value
 
 
 def tp_debug_expire_wait(limit_ns: int, stream=None) -> None:

@@ -543,6 +543,26 @@ tp_status tp_set_gemm_split(int mode, int max_clusters) {
     return TP_OK;
 }
 
+tp_status tp_debug_gemm_plan(int64_t m, int64_t n, int64_t k, int groups, int segs, int gated, int sms, int* kind,
+                             int* tile_n, int* cluster) {
+    TP_CHECK(m > 0 && n > 0 && k > 0 && sms >= 1, TP_ERR_INVALID_ARG);
+    TP_CHECK(groups >= 1 && groups <= TP_MAX_SHARDS && segs >= 1 && segs <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
+    TP_CHECK(groups == 1 || segs == 1, TP_ERR_INVALID_ARG);
+    TP_CHECK(kind != nullptr && tile_n != nullptr && cluster != nullptr, TP_ERR_INVALID_ARG);
+    tpk::GemmDesc d;
+    d.M = m;
+    d.N = n;
+    d.K = k;
+    d.groups = groups;
+    d.segs = segs;
+    d.glu = gated ? 1 : 0;
+    const tpk::GemmPlan p = tpk::plan_gemm(d, sms);
+    *kind = p.kind;
+    *tile_n = p.bn;
+    *cluster = p.cs;
+    return TP_OK;
+}
+
 tp_status tp_debug_expire_wait(uint64_t limit_ns, tp_stream stream) {
     if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
     int* p = status_ptr();

@@ -1462,6 +1462,59 @@ static long long plan_cost(int tiles, int bn, int sms) {
     return waves * (bn + 32);
 }
 
+// Kernel, tile width and split-K cluster size for a GEMM on `sms` SMs (pure host
+// logic: the launch below follows it, and tp_debug_gemm_plan exposes it to tests).
+GemmPlan plan_gemm(const GemmDesc& d, int sms) {
+    const int m_tiles = static_cast<int>((d.M + BM - 1) / BM);
+    const bool glu = d.glu != 0;
+    // Candidate MMA widths, largest first; pick the one with the lowest cost.  96 (store
+    // epilogue only: a gated tile splits into gate and up halves of whole 32-column chunks)
+    // spreads a narrow weight over more SMs, e.g. 112 tiles instead of 80 for the 1280-row
+    // QKV blocks of 8 ranks.
+    const int cands[4] = {256, 128, 96, 64};
+    int best = 256;
+    long long best_cost = -1;
+    for (int bn : cands) {
+        if (glu && bn == 96) continue;
+        const int out_cols = glu ? bn / 2 : bn;
+        const int tiles = d.groups * m_tiles * static_cast<int>((d.N + out_cols - 1) / out_cols);
+        const long long c = plan_cost(tiles, bn, sms);
+        if (best_cost < 0 || c < best_cost) {
+            best_cost = c;
+            best = bn;
+        }
+    }
+    if (d.force_bn) best = (glu && d.force_bn == 96) ? 128 : d.force_bn;
+    // CTA pairs whenever they need no more waves than single CTAs with the same tile width
+    // (a pair tile holds 256 rows on two SMs, a single-CTA tile 128 rows on one; per wave the
+    // pair kernel does the same work per SM at a higher tensor-pipe rate).  Measured on the 70B
+    // MLP: pairs win at n = 256 (3 waves either way) and 512, lose at n = 128 and for the down
+    // GEMM at n = 384, where they would add a wave.
+    bool pair = false;
+    if (d.pair >= 0 && sms >= 2) {
+        const int out_cols = glu ? 128 : 256;
+        const long long col_tiles = static_cast<long long>(d.groups) * ((d.N + out_cols - 1) / out_cols);
+        const long long pair_waves = (col_tiles * ((d.M + 255) / 256) + sms / 2 - 1) / (sms / 2);
+        const long long single_waves = (col_tiles * ((d.M + 127) / 128) + sms - 1) / sms;
+        pair = d.pair > 0 || (d.M > 128 && d.force_bn == 0 && pair_waves <= single_waves);
+    }
+    GemmPlan p;
+    p.bn = best;
+    if (pair) {
+        p.kind = 1;
+        p.bn = 256;
+        return p;
+    }
+    int split_bn = 0;
+    const int cs = split_plan(d, sms, split_bn);
+    if (cs >= 2) {
+        p.kind = 2;
+        p.bn = split_bn;
+        p.cs = cs;
+    }
+    return p;
+}
+
 tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -1487,51 +1540,20 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     // tile indices are 32-bit in the kernels
     if (static_cast<int64_t>(d.groups) * ((d.M + 127) / 128) * ((d.N + 63) / 64) > INT32_MAX) return TP_ERR_UNSUPPORTED;
 
-    const int sms = std::max(1, sm_count());
+    const GemmPlan plan = plan_gemm(d, std::max(1, sm_count()));
     const bool glu = d.glu != 0;
-    // Candidate MMA widths, largest first; pick the one with the lowest cost.  96 (store
-    // epilogue only: a gated tile splits into gate and up halves of whole 32-column chunks)
-    // spreads a narrow weight over more SMs, e.g. 112 tiles instead of 80 for the 1280-row
-    // QKV blocks of 8 ranks.
-    const int cands[4] = {256, 128, 96, 64};
-    int best = 256;
-    long long best_cost = -1;
-    for (int bn : cands) {
-        if (glu && bn == 96) continue;
-        const int out_cols = glu ? bn / 2 : bn;
-        const int tiles = d.groups * a.m_tiles * static_cast<int>((d.N + out_cols - 1) / out_cols);
-        const long long c = plan_cost(tiles, bn, sms);
-        if (best_cost < 0 || c < best_cost) {
-            best_cost = c;
-            best = bn;
-        }
-    }
-    if (d.force_bn) best = (glu && d.force_bn == 96) ? 128 : d.force_bn;
-    // CTA pairs whenever they need no more waves than single CTAs with the same tile width
-    // (a pair tile holds 256 rows on two SMs, a single-CTA tile 128 rows on one; per wave the
-    // pair kernel does the same work per SM at a higher tensor-pipe rate).  Measured on the 70B
-    // MLP: pairs win at n = 256 (3 waves either way) and 512, lose at n = 128 and for the down
-    // GEMM at n = 384, where they would add a wave.
-    bool pair = false;
-    if (d.pair >= 0 && sms >= 2) {
-        const int out_cols = glu ? 128 : 256;
-        const long long col_tiles = static_cast<long long>(d.groups) * ((d.N + out_cols - 1) / out_cols);
-        const long long pair_waves = (col_tiles * ((d.M + 255) / 256) + sms / 2 - 1) / (sms / 2);
-        const long long single_waves = (col_tiles * ((d.M + 127) / 128) + sms - 1) / sms;
-        pair = d.pair > 0 || (d.M > 128 && d.force_bn == 0 && pair_waves <= single_waves);
-    }
-    if (pair) {
+    const int best = plan.bn;
+    if (plan.kind == 1) {
         if (glu) return launch_pair<kPairStages, EPI_GLU, kPairKsub>(a, d, stream);
         return launch_pair<kPairStages, EPI_STORE, kPairKsub>(a, d, stream);
     }
-    int split_bn = 0;
-    const int cs = split_plan(d, sms, split_bn);
-    if (cs >= 2) {
+    if (plan.kind == 2) {
+        const int cs = plan.cs;
         if (glu) {
-            if (split_bn == 256) return launch_split<256, 4, EPI_GLU>(a, d, cs, stream);
+            if (plan.bn == 256) return launch_split<256, 4, EPI_GLU>(a, d, cs, stream);
             return launch_split<128, 8, EPI_GLU, 2>(a, d, cs, stream);
         }
-        if (split_bn == 256) return launch_split<256, 4, EPI_STORE>(a, d, cs, stream);
+        if (plan.bn == 256) return launch_split<256, 4, EPI_STORE>(a, d, cs, stream);
         return launch_split<128, 8, EPI_STORE, 2>(a, d, cs, stream);
     }
     if (d.M <= 64) {   // decode: 64-row A tiles, deeper B rings

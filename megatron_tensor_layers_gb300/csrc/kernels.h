@@ -45,6 +45,16 @@ struct GemmDesc {
 
 tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream);
 
+// The kernel launch_gemm picks for `d` on `sms` SMs: kind 0 = single-CTA tiles of
+// width bn, 1 = CTA pairs (256 x 256 tiles), 2 = split-K clusters of cs CTAs on
+// tiles of width bn.
+struct GemmPlan {
+    int kind = 0;
+    int bn = 256;
+    int cs = 0;
+};
+GemmPlan plan_gemm(const GemmDesc& d, int sms);
+
 // Shard reduce.
 struct ReduceDesc {
     int t = 0;

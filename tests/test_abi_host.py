@@ -131,3 +131,39 @@ def test_host_pipeline_rejects_on_host(lib):
     # a workspace smaller than one row block
     assert lib.tp_mlp_forward_host(2, 8, 64, 128, FAKE, two, two, 64, None, 1, 0, 0, FAKE, FAKE, 16, FAKE,
                                    FAKE, 0, 2, None, None) == 7
+
+
+def test_gemm_kernel_choice(lib):
+    """The host-side plan (no CUDA call) for the shapes whose kernel choice was measured on
+    GB300 (152 SMs): the bench prefill, decode, chunked prefill, the tiny MLP, the LM head
+    and the 70B attention projections."""
+    from megatron_tensor_layers_gb300 import _lib as tp
+    plan = tp.tp_debug_gemm_plan
+    h, f = 8192, 28672
+    # prefill t=4, n=8192: gate_up (gated, 4 shards of 7168 H columns) and down on CTA pairs
+    assert plan(8192, f // 4, h, groups=4, gated=True) == ("pair", 256, 0)
+    assert plan(8192, h, f // 4, groups=4) == ("pair", 256, 0)
+    # fused down at prefill: one output, t K-segments, still pairs
+    assert plan(8192, h, f // 4, segs=4) == ("pair", 256, 0)
+    # decode t=4: gate_up 128-wide gated tiles (448 tiles), down 256-wide (128 tiles)
+    for n in (1, 16, 64):
+        assert plan(n, f // 4, h, groups=4, gated=True) == ("single", 128, 0)
+        assert plan(n, h, f // 4, groups=4) == ("single", 256, 0)
+        # fused reduce at decode: split-K clusters of 4 over 32 tiles of 256
+        assert plan(n, h, f // 4, segs=4) == ("split", 256, 4)
+    # chunked prefill: pairs from 200 to 256 rows, single CTAs at 128 rows
+    assert plan(256, f // 4, h, groups=4, gated=True)[0] == "pair"
+    assert plan(200, f // 4, h, groups=4, gated=True)[0] == "pair"
+    assert plan(128, f // 4, h, groups=4, gated=True)[0] == "single"
+    assert plan(384, h, f // 4, groups=4)[0] == "single"           # pairs would add a wave
+    # tiny MLP t=2, n=8: 64-wide gated tiles (96 CTAs), fused down on split-K clusters
+    assert plan(8, 1536, 1024, groups=2, gated=True) == ("single", 64, 0)
+    assert plan(8, 1024, 1536, segs=2)[0] == "split"
+    # 70B attention, t=8 at decode: 96-wide QKV tiles (112 tiles instead of 80 of 128)
+    assert plan(1, 1280, h, groups=8) == ("single", 96, 0)
+    # LM head t=2, 4096 x 1024 x 151936: pairs
+    assert plan(4096, 75968, 1024, groups=2) == ("pair", 256, 0)
+    # a gated GEMM never takes the 96-wide tile
+    for n in (1, 8, 64):
+        assert plan(n, 640, h, groups=8, gated=True)[1] != 96
+    assert lib.tp_debug_gemm_plan(0, 1, 1, 1, 1, 0, 152, None, None, None) == 1
