@@ -35,7 +35,7 @@ __all__ = [
     "bf16_bits_to_f64", "f32_bits_to_f64", "round_to_bf16", "bf16_from_f64_bits",
     "divide", "column_shard", "row_shard", "merged_column_shard", "qkv_shard", "qkv_shard_gqa", "kv_head_of_rank",
     "vocab_range", "linear", "silu", "gelu_tanh", "glu",
-    "mlp_unsharded", "mlp_shard_partials", "mlp_sharded",
+    "mlp_unsharded", "mlp_shard_partials", "mlp_sharded", "round_to_f32", "mlp_sharded_rounded",
     "reduce_direct", "reduce_direct_f32", "ring_chunks", "ring_schedule",
     "ring_allreduce", "ring_fold_order",
     "vocab_parallel_embedding", "lm_head_sharded", "lm_head_unsharded", "shard_gather",
@@ -311,6 +311,61 @@ def mlp_sharded(x, w_gate, w_up, w_down, t, bias=None, act="silu", order="direct
         bufs, _ = ring_allreduce(parts, hop="f64")
         return bufs[0]
     raise ValueError(order)
+
+
+def round_to_f32(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest IEEE binary32 value, ties to even
+    (numpy's float64 -> float32 conversion), returned as float64."""
+    return np.asarray(x, np.float64).astype(np.float32).astype(np.float64)
+
+
+def mlp_sharded_rounded(x, w_gate, w_up, w_down, t, bias=None, act="silu", partial_dtype="bf16",
+                        order="direct") -> Dict[str, object]:
+    """The tensor-parallel MLP with the intermediate results stored in the
+    number formats a rank keeps them in.
+
+    6.2 Tensor-parallel inference, §1: rank i computes act(X A_i) B_i; the
+    ranks exchange their partials as 2-byte values ("Tensor parallelism from
+    scratch", the cost of communication: 2 bytes per element on the wire).
+    Reading taken where the pages are silent: every product is exact (fp64
+    here), the activation output H_i = act(G_i) * U_i is rounded once to
+    bfloat16 (the dtype of the next GEMM's input), each partial
+    P_i = H_i B_i^T (+ bias on rank 0, before rounding) is rounded once to
+    ``partial_dtype`` ("bf16" or "f32"), and the partials are summed:
+
+    * order "direct": in rank order, exactly (fp64);
+    * order "ring": the ring all-reduce of :func:`ring_allreduce`, every hop
+      rounded to the partial dtype (a ring over a bf16 wire rounds at each
+      hop);
+    * partial_dtype None ("fused"): no partial exists; Y = sum_i H_i B_i^T
+      (+ bias once), exact.
+
+    Returns a dict: ``y`` [n, h]; ``h`` / ``h_exact`` the t rounded and
+    unrounded H_i; ``p`` the t rounded partials (empty when fused) and
+    ``p_exact`` the t products H_i B_i^T (+ bias on rank 0) before rounding.
+    """
+    f = w_gate.shape[0]
+    fs = divide(f, t)
+    hs, hs_exact, ps, ps_exact = [], [], [], []
+    for i in range(t):
+        gu = merged_column_shard([w_gate, w_up], t, i)
+        h_exact = glu(linear(x, gu[:fs]), linear(x, gu[fs:]), act)
+        h_i = round_to_bf16(h_exact)
+        hs_exact.append(h_exact)
+        hs.append(h_i)
+        ps_exact.append(linear(h_i, row_shard(w_down, t, i), bias if i == 0 else None))
+    if partial_dtype is None:
+        return {"y": reduce_direct(ps_exact), "h": hs, "h_exact": hs_exact, "p": [], "p_exact": ps_exact}
+    rnd = {"bf16": round_to_bf16, "f32": round_to_f32}[partial_dtype]
+    ps = [rnd(p) for p in ps_exact]
+    if order == "direct":
+        y = reduce_direct(ps)
+    elif order == "ring":
+        bufs, _ = ring_allreduce(ps, hop=partial_dtype)
+        y = bufs[0]
+    else:
+        raise ValueError(order)
+    return {"y": y, "h": hs, "h_exact": hs_exact, "p": ps, "p_exact": ps_exact}
 
 
 # ---------------------------------------------------------------------------

@@ -226,6 +226,83 @@ def test_sharded_mlp_equals_unsharded_float():
     assert np.abs(ref).max() > 0.1
 
 
+# The MLP with H rounded to bf16 and the partials rounded to their dtype, on a
+# case worked by hand.  t = 2, one token, h = 1, f = 2: x = 1, gate rows
+# (1.5, -1), up rows (3, 7), down row (1.1875, 0.5).
+#   rank 0: H = silu(1.5) * 3 = 3.679085...   -> bf16 3.671875 (spacing 2^-6 in [2, 4));
+#           rounding silu(1.5) first would give 3.6875.
+#           P = 3.671875 * 1.1875 = 4.3603515625 (exact in fp32) -> bf16 4.375 (spacing 2^-5)
+#   rank 1: H = silu(-1) * 7 = -1.882589...   -> bf16 -1.8828125 (spacing 2^-7);
+#           rounding silu(-1) first would give -1.890625.
+#           P = -1.8828125 * 0.5 = -0.94140625 (a bf16 value)
+#   bf16 partials, rank-order sum:       4.375 - 0.94140625        = 3.43359375
+#   bf16 ring hop (t = 2: one rounding): bf16(3.43359375)          = 3.4375 (spacing 2^-6)
+#   fp32 partials, or no partials:       4.3603515625 - 0.94140625 = 3.4189453125
+#   unrounded definition:                3.4276186323648...
+# With a bias of 2^-6 on rank 0, added before the partial is rounded:
+#   P0 = 4.3759765625 -> bf16 4.375 (adding the bias after rounding would give
+#   4.390625 and Y = 3.44921875), so Y = 3.43359375; fp32: Y = 3.4345703125.
+_WORKED = dict(x=np.array([[1.0]]), wg=np.array([[1.5], [-1.0]]), wu=np.array([[3.0], [7.0]]),
+               wd=np.array([[1.1875, 0.5]]))
+
+
+def test_mlp_rounded_worked_example():
+    x, wg, wu, wd = _WORKED["x"], _WORKED["wg"], _WORKED["wu"], _WORKED["wd"]
+    e = O.mlp_sharded_rounded(x, wg, wu, wd, 2, None, "silu", "bf16", "direct")
+    assert [h.item() for h in e["h"]] == [3.671875, -1.8828125]
+    assert [p.item() for p in e["p"]] == [4.375, -0.94140625]
+    assert [p.item() for p in e["p_exact"]] == [4.3603515625, -0.94140625]
+    assert e["y"].item() == 3.43359375
+    assert O.mlp_sharded_rounded(x, wg, wu, wd, 2, None, "silu", "bf16", "ring")["y"].item() == 3.4375
+    for pd, order in (("f32", "direct"), ("f32", "ring"), (None, "direct")):
+        assert O.mlp_sharded_rounded(x, wg, wu, wd, 2, None, "silu", pd, order)["y"].item() == 3.4189453125
+    assert abs(O.mlp_unsharded(x, wg, wu, wd, None, "silu").item() - 3.4276186323648) < 1e-12
+    b = np.array([2.0 ** -6])
+    assert O.mlp_sharded_rounded(x, wg, wu, wd, 2, b, "silu", "bf16", "direct")["y"].item() == 3.43359375
+    assert O.mlp_sharded_rounded(x, wg, wu, wd, 2, b, "silu", "f32", "direct")["y"].item() == 3.4345703125
+    assert O.mlp_sharded_rounded(x, wg, wu, wd, 2, b, "silu", None, "direct")["y"].item() == 3.4345703125
+
+
+def test_mlp_rounded_within_the_rounding_bounds():
+    """On random inputs every rounding the function takes stays within half a
+    spacing of the value it rounds: the result differs from the unrounded
+    definition by at most sum_f |W_down[j, f]| * spacing(H[i, f]) / 2 (plus
+    half a spacing per bf16 partial), and the H rounding does change it."""
+    rng = np.random.default_rng(11)
+    n, h, f, t = 6, 48, 64, 4
+    bf = lambda a: O.round_to_bf16(a)
+    x = bf(rng.standard_normal((n, h)))
+    wg, wu, wd = (bf(rng.standard_normal(s) * 0.1) for s in [(f, h), (f, h), (h, f)])
+
+    def half_spacing(v):
+        _, e = np.frexp(np.maximum(np.abs(v), 2.0 ** -126))
+        return np.ldexp(1.0, e.astype(np.int64) - 9)
+
+    ref = O.mlp_unsharded(x, wg, wu, wd, None, "silu")
+    fused = O.mlp_sharded_rounded(x, wg, wu, wd, t, None, "silu", None)
+    hbound = sum(half_spacing(fused["h_exact"][r]) @ np.abs(O.row_shard(wd, t, r)).T for r in range(t))
+    assert np.all(np.abs(fused["y"] - ref) <= hbound * (1 + 1e-12))
+    assert np.any(fused["y"] != ref)
+    for r in range(t):
+        assert np.all(np.abs(fused["h"][r] - fused["h_exact"][r]) <= half_spacing(fused["h_exact"][r]))
+    wire = O.mlp_sharded_rounded(x, wg, wu, wd, t, None, "silu", "bf16")
+    pbound = sum(half_spacing(p) for p in wire["p_exact"])
+    assert np.all(np.abs(wire["y"] - fused["y"]) <= pbound * (1 + 1e-12))
+    assert np.any(wire["y"] != fused["y"])
+    for r in range(t):                         # partials are bf16 values
+        O.bf16_from_f64_bits(wire["p"][r])
+
+
+def test_round_to_f32_matches_torch():
+    rng = np.random.default_rng(12)
+    v = np.concatenate([rng.standard_normal(1000) * 10.0 ** rng.integers(-30, 30, 1000),
+                        [1.0 + 2.0 ** -24, 1.0 + 3 * 2.0 ** -24, -(1.0 + 2.0 ** -24), 0.0, -0.0]])
+    ours = O.round_to_f32(v)
+    lib = torch.tensor(v, dtype=torch.float64).to(torch.float32).to(torch.float64).numpy()
+    assert np.array_equal(ours, lib)
+    assert ours[-5] == 1.0 and ours[-4] == 1.0 + 2.0 ** -22      # ties to even
+
+
 def test_bias_counted_once():
     rng = np.random.default_rng(4)
     x, wg, wu, wd = _int_mats(rng, (2, 8), (8, 8), (8, 8), (8, 8))
