@@ -138,7 +138,11 @@ tp_status tp_linear_col(int t, int64_t n, int64_t in, int64_t out_full,
  *   reduce_results == 1: y [n, out] (row stride ldy, y_dtype) receives the
  *          sum.  DIRECT/RING write the partials first, then reduce them
  *          (RING hops round to partial_dtype); FUSED writes no partial
- *          (partials may be NULL).
+ *          (partials may be NULL).  A FUSED call of more than 128 rows that
+ *          is given partials[0] (n * ldp elements of partial_dtype, at least
+ *          32 MiB + 4 KiB) uses that buffer as scratch in which the last,
+ *          partial wave of output tiles is split along K (stream-K); its
+ *          contents are overwritten.
  *   partials[r] [n, out] in partial_dtype, row stride ldp (caller-owned
  *          scratch; contents are overwritten).
  * Requires in_full % t == 0 and (in_full/t) % 8 == 0.
@@ -173,9 +177,12 @@ tp_status tp_shard_reduce(int t, int64_t count, tp_dtype dtype, const void* cons
                           tp_dtype hop_dtype, int replicate, tp_stream stream);
 
 /*
- * Workspace bytes tp_mlp_forward needs: the intermediate H [n, f] bf16
- * (rank r's slice is columns [r*f/t, (r+1)*f/t)) plus, unless mode is
- * FUSED, t partials [n, h] of partial_dtype, each 256-byte aligned.
+ * Workspace bytes for tp_mlp_forward: the intermediate H [n, f] bf16 (rank
+ * r's slice is columns [r*f/t, (r+1)*f/t)) plus, unless mode is FUSED, t
+ * partials [n, h] of partial_dtype, each 256-byte aligned.  For a FUSED
+ * reduce of more than 128 token rows it adds 32 MiB + 4 KiB in which the
+ * down GEMM splits the tiles of its last, partial wave along K (stream-K):
+ * tp_mlp_forward also runs with only the H bytes, then without that split.
  * Returns 0 for invalid arguments.
  */
 size_t tp_mlp_workspace_size(int t, int64_t n, int64_t h, int64_t f,
@@ -194,8 +201,9 @@ size_t tp_mlp_workspace_size(int t, int64_t n, int64_t h, int64_t f,
  *   w_down[r]    [h, f/t] bf16, row stride ld_down.
  *   bias_down    NULL or [h] bf16, added once.
  *   act          TP_ACT_SILU_MUL or TP_ACT_GELU_TANH_MUL.
- *   workspace    device buffer of at least tp_mlp_workspace_size() bytes,
- *                256-byte aligned; overwritten.
+ *   workspace    device buffer of tp_mlp_workspace_size() bytes (a FUSED
+ *                reduce of more than 128 rows also accepts just the n*f*2
+ *                bytes of H, see above), 256-byte aligned; overwritten.
  *   y            [n, h] of y_dtype, contiguous.
  * Requires f % t == 0, (f/t) % 8 == 0 and h % 8 == 0.
  */
@@ -254,17 +262,23 @@ tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
  * It allocates nothing and calls no allocating routine.  The caller still
  * passes and owns x, the weights, the bias and y.
  *
- * Limit: tp_mlp_workspace_size(t, n, h, f, mode, partial_dtype) must not
- * exceed TP_STATIC_SCRATCH_BYTES (16 MiB), else TP_ERR_WORKSPACE and nothing
- * is launched.  Example: 64 tokens of an h=8192, f=28672 MLP at t=4 need
- * 12.1 MB with fp32 partials; a fused reduce needs only the n*f*2 bytes of H.
+ * Limit: the workspace tp_mlp_forward requires (tp_mlp_workspace_size(t, n,
+ * h, f, mode, partial_dtype), less the optional stream-K area of a FUSED
+ * reduce of more than 128 rows) must not exceed TP_STATIC_SCRATCH_BYTES
+ * (16 MiB), else TP_ERR_WORKSPACE and nothing is launched.  Example: 64
+ * tokens of an h=8192, f=28672 MLP at t=4 need 12.1 MB with fp32 partials;
+ * a fused reduce needs only the n*f*2 bytes of H.
  *
  * Costs and rules:
- *  - Every GPU on which the library is loaded holds the 16 MiB from module
- *    load until the process exits.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) and caches it; make that first call before any
- *    stream capture begins on that device.
+ *  - The 16 MiB belong to the library's device image, which CUDA loads
+ *    lazily: a GPU reserves them when the module is first loaded there, at
+ *    the latest in this entry point's first call on that device, and holds
+ *    them until the process exits.
+ *  - That first call on each device loads the module if needed and looks up
+ *    the array's device address (cudaGetSymbolAddress), caching it.  Loading
+ *    can synchronise the device and fails with TP_ERR_CUDA when the device
+ *    has no 16 MiB left, so make the first call at start-up, outside any
+ *    latency-critical loop and before any stream capture on that device.
  *  - All calls in the process share the one array per device and it keeps
  *    the previous call's contents.  Nothing in it needs to start at zero:
  *    each call writes every byte it later reads.  Calls that can overlap on

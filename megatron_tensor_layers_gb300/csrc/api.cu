@@ -31,16 +31,21 @@ void apply_knobs(tpk::GemmDesc& d) {
     d.split_clusters = g_split_clusters.load();
 }
 
+// Device address of the status word on the current device, looked up once per
+// device and cached.  Host threads may race on a device's first lookup: both
+// store the same address, and the relaxed atomics make that race benign.
 int* status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    static int* cache[64] = {nullptr};
-    if (cache[dev] == nullptr) {
+    static std::atomic<int*> cache[64];
+    int* cached = cache[dev].load(std::memory_order_relaxed);
+    if (cached == nullptr) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_tp_status) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<int*>(p);
+        cached = static_cast<int*>(p);
+        cache[dev].store(cached, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return cached;
 }
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -56,6 +61,23 @@ inline cudaStream_t cs(tp_stream s) { return reinterpret_cast<cudaStream_t>(s); 
     } while (0)
 
 }  // namespace
+
+// tp_mlp_forward's workspace: H [n, f] bf16, then (unless the reduce is
+// fused) t partials [n, h]; that much is required.  A fused reduce of more
+// than 128 rows (CTA-pair tiles) may also use the stream-K tail area of its
+// down GEMM, which tp_mlp_workspace_size includes.
+size_t tpk::mlp_workspace_required(int t, int64_t n, int64_t h, int64_t f, tp_reduce_mode mode, tp_dtype partial_dtype) {
+    if (t < 1 || t > TP_MAX_SHARDS || n < 0 || h <= 0 || f <= 0 || !dtype_ok(partial_dtype)) return 0;
+    if (mode != TP_REDUCE_DIRECT && mode != TP_REDUCE_RING && mode != TP_REDUCE_FUSED) return 0;
+    size_t bytes = align256(static_cast<size_t>(n) * static_cast<size_t>(f) * 2);
+    if (mode != TP_REDUCE_FUSED)
+        bytes += static_cast<size_t>(t) * align256(static_cast<size_t>(n) * static_cast<size_t>(h) * esize(partial_dtype));
+    return bytes;
+}
+
+static size_t mlp_tail_bytes(int64_t n, tp_reduce_mode mode) {
+    return (mode == TP_REDUCE_FUSED && n > 128) ? tpk::kSkWorkspaceBytes : 0;
+}
 
 extern "C" {
 
@@ -177,10 +199,13 @@ tp_status tp_shard_reduce(int t, int64_t count, tp_dtype dtype, const void* cons
 // call that wrote x (tp_mlp_forward's gate_up GEMM), so the split-K GEMM may
 // load weights before waiting for it; 0: the first kernel of the call, which
 // loads nothing before that wait.  Every launch may start early.
+// sk_ws / sk_bytes: the stream-K tail area of a fused reduce (flags already
+// zeroed in stream order), or null.
 static tp_status linear_row_impl(int t, int64_t n, int64_t in_full, int64_t out, const void* const* x, int64_t ldx,
                                  const void* const* w, int64_t ldw, const void* bias, int reduce_results,
                                  tp_reduce_mode mode, tp_dtype partial_dtype, void* const* partials, int64_t ldp,
-                                 void* y, int64_t ldy, tp_dtype y_dtype, int pdl_first, tp_stream stream) {
+                                 void* y, int64_t ldy, tp_dtype y_dtype, int pdl_first, tp_stream stream,
+                                 void* sk_ws = nullptr, size_t sk_bytes = 0) {
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
     TP_CHECK(n >= 0 && in_full > 0 && out > 0, TP_ERR_INVALID_ARG);
     TP_CHECK(n <= INT32_MAX && out <= INT32_MAX && in_full <= INT32_MAX, TP_ERR_INVALID_ARG);
@@ -236,6 +261,16 @@ static tp_status linear_row_impl(int t, int64_t n, int64_t in_full, int64_t out,
         d.bias[0] = bias;
         d.ldo = ldy;
         d.out_f32 = y_dtype == TP_F32;
+        if (sk_ws == nullptr && partials != nullptr && partials[0] != nullptr && n > 128 && dtype_ok(partial_dtype) &&
+            ldp >= out && al16(partials[0]) &&
+            static_cast<size_t>(n) * static_cast<size_t>(ldp) * esize(partial_dtype) >= tpk::kSkWorkspaceBytes) {
+            // a caller's partial buffer, unused by a fused reduce, holds the stream-K tail area
+            sk_ws = partials[0];
+            sk_bytes = static_cast<size_t>(n) * static_cast<size_t>(ldp) * esize(partial_dtype);
+            if (cudaMemsetAsync(sk_ws, 0, tpk::kSkFlagBytes, cs(stream)) != cudaSuccess) return TP_ERR_CUDA;
+        }
+        d.sk_ws = sk_ws;
+        d.sk_ws_bytes = sk_bytes;
         g_collectives++;
         return tpk::launch_gemm(d, cs(stream));
     }
@@ -264,12 +299,8 @@ tp_status tp_linear_row(int t, int64_t n, int64_t in_full, int64_t out, const vo
 }
 
 size_t tp_mlp_workspace_size(int t, int64_t n, int64_t h, int64_t f, tp_reduce_mode mode, tp_dtype partial_dtype) {
-    if (t < 1 || t > TP_MAX_SHARDS || n < 0 || h <= 0 || f <= 0 || !dtype_ok(partial_dtype)) return 0;
-    if (mode != TP_REDUCE_DIRECT && mode != TP_REDUCE_RING && mode != TP_REDUCE_FUSED) return 0;
-    size_t bytes = align256(static_cast<size_t>(n) * static_cast<size_t>(f) * 2);
-    if (mode != TP_REDUCE_FUSED)
-        bytes += static_cast<size_t>(t) * align256(static_cast<size_t>(n) * static_cast<size_t>(h) * esize(partial_dtype));
-    return bytes;
+    const size_t base = tpk::mlp_workspace_required(t, n, h, f, mode, partial_dtype);
+    return base == 0 ? 0 : base + mlp_tail_bytes(n, mode);
 }
 
 tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, int64_t ldx,
@@ -291,14 +322,15 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, 
         TP_CHECK(w_gate_up[r] != nullptr && w_down[r] != nullptr, TP_ERR_INVALID_ARG);
         TP_CHECK(al16(w_gate_up[r]) && al16(w_down[r]), TP_ERR_ALIGNMENT);
     }
-    const size_t need = tp_mlp_workspace_size(t, n, h, f, mode, partial_dtype);
+    const size_t need = tpk::mlp_workspace_required(t, n, h, f, mode, partial_dtype);
     TP_CHECK(workspace != nullptr || need == 0, TP_ERR_WORKSPACE);
     TP_CHECK(workspace_bytes >= need, TP_ERR_WORKSPACE);
     TP_CHECK((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, TP_ERR_ALIGNMENT);
     if (n == 0) return TP_OK;
 
     // Workspace: H [n, f] bf16 (rank r's slice = columns [r*fs, (r+1)*fs)),
-    // then t partials [n, h].
+    // then t partials [n, h], or, for a fused reduce when the workspace holds
+    // it, the stream-K tail area (its flags zeroed here, ahead of both GEMMs).
     char* ws = static_cast<char*>(workspace);
     uint16_t* hbuf = reinterpret_cast<uint16_t*>(ws);
     void* parts[TP_MAX_SHARDS] = {};
@@ -306,6 +338,12 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, 
         char* p = ws + align256(static_cast<size_t>(n) * f * 2);
         const size_t pb = align256(static_cast<size_t>(n) * h * esize(partial_dtype));
         for (int r = 0; r < t; ++r) parts[r] = p + r * pb;
+    }
+    void* sk_ws = nullptr;
+    const size_t tail = mlp_tail_bytes(n, mode);
+    if (tail > 0 && workspace_bytes >= need + tail) {
+        sk_ws = ws + need;
+        if (cudaMemsetAsync(sk_ws, 0, tpk::kSkFlagBytes, cs(stream)) != cudaSuccess) return TP_ERR_CUDA;
     }
 
     // 1) column-parallel gate_up with the gated activation in the epilogue.
@@ -337,7 +375,7 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, 
     const void* hx[TP_MAX_SHARDS];
     for (int r = 0; r < t; ++r) hx[r] = hbuf + r * fs;
     return linear_row_impl(t, n, f, h, hx, f, w_down, ld_down, bias_down, 1, mode, partial_dtype, parts, h, y, h,
-                           y_dtype, 1, stream);
+                           y_dtype, 1, stream, sk_ws, sk_ws != nullptr ? tail : 0);
 }
 
 tp_status vocab_parallel_embed(int t, int64_t vocab, int64_t h, const int32_t* ids, int64_t n,

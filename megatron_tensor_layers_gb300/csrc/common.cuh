@@ -107,6 +107,38 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// ------------------------------------------------ flags in global memory
+
+// A flag that one CTA raises after its global stores and another CTA waits
+// for: the store is a release and the load an acquire, both at GPU scope.
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *flag is non-zero, bounded like mbar_wait: gives up when *abort
+// becomes non-zero or after limit_ns (then raises *abort and records
+// TP_ERR_TIMEOUT).  Returns true when the flag was seen raised.
+__device__ __forceinline__ bool flag_wait(const int* flag, volatile int* abort, int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    if (ld_acquire_gpu(flag) != 0) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(flag) != 0) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > limit_ns) {
+            *abort = 1;
+            if (status) atomicExch(status, static_cast<int>(TP_ERR_TIMEOUT));
+            return false;
+        }
+    }
+}
+
 // ------------------------------------------------ programmatic dependent launch
 
 // Wait until the grid that precedes this one in the stream has completed and

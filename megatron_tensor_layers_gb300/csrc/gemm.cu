@@ -49,6 +49,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -86,6 +87,12 @@ struct GemmArgs {
     int split;                        // split-K kernel: CTAs per cluster sharing one output tile
     int pdl_prefetch;                 // 1: B may be loaded before waiting for the previous grid
     int* status;                      // library status word
+    // stream-K tail (pair kernel, store epilogue): tiles [sk_first, total_tiles)
+    // run as sk_parts K-parts each; sk_first == total_tiles: no tail split
+    int sk_first;
+    int sk_parts;
+    int* sk_flags;                    // one per (partial slot, CTA of the pair)
+    float* sk_scratch;                // partial slots of 256 x 256 fp32
 };
 
 // Tile index -> (group, row-tile, column-tile).  Tiles run in bands of
@@ -497,7 +504,7 @@ struct PairCfg {
     static constexpr int B_BYTES = 128 * BK * 2;             // this CTA's half of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
+    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
     // Store epilogue: per epilogue warp, 32 output rows of 128 bytes (64 bf16 or 32 fp32
     // columns) plus a 16-byte pad, so that a warp writes whole 128-byte lines of 4 rows per
     // store instruction instead of one 16-byte piece of 32 rows.
@@ -509,6 +516,36 @@ struct PairCfg {
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
+
+// Work item j of a cluster of the pair kernel: first its whole tiles (tile
+// cluster + i * nclusters below sk_first), then its stream-K units (unit u =
+// cluster + i * nclusters below the tail's tiles x sk_parts: tile sk_first +
+// u / sk_parts, part u % sk_parts of the tile's K blocks).  All roles of both
+// CTAs of a pair walk the same sequence.
+struct PairWork {
+    int tile;
+    int kb_lo, kb_hi;    // K blocks [kb_lo, kb_hi) of the tile's kb_per_tile
+    int part;            // 0: whole tile or the first part (which adds the others); > 0: a partial
+};
+
+__device__ __forceinline__ bool pair_work(const GemmArgs& a, int cluster, int nclusters, int j, int kb_per_tile,
+                                          PairWork& w) {
+    const int whole = a.sk_first > cluster ? (a.sk_first - cluster + nclusters - 1) / nclusters : 0;
+    if (j < whole) {
+        w.tile = cluster + j * nclusters;
+        w.kb_lo = 0;
+        w.kb_hi = kb_per_tile;
+        w.part = 0;
+        return true;
+    }
+    const int u = cluster + (j - whole) * nclusters;
+    if (u >= (a.total_tiles - a.sk_first) * a.sk_parts) return false;
+    w.tile = a.sk_first + u / a.sk_parts;
+    w.part = u % a.sk_parts;
+    w.kb_lo = static_cast<int>(static_cast<int64_t>(w.part) * kb_per_tile / a.sk_parts);
+    w.kb_hi = static_cast<int>(static_cast<int64_t>(w.part + 1) * kb_per_tile / a.sk_parts);
+    return true;
+}
 
 template <int STAGES, int EPI, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_constant__ GemmArgs args) {
@@ -527,8 +564,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
     auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * STAGES + 4));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * (2 * STAGES + 4) + 4);
+    const uint32_t sk_bar = bar_base + 8u * (2 * STAGES + 4);   // this CTA's epilogue warps stored a partial
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ptr + 8 * (2 * STAGES + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_ptr + 8 * (2 * STAGES + 5) + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -545,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), 8);              // 4 epilogue warps x 2 CTAs
         }
+        mbar_init(sk_bar, 4);                         // the 4 epilogue warps of this CTA
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -570,15 +609,17 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
             pdl_wait();                                // A may be the previous grid's output
             int grp = 0;
             uint32_t phase = 0;
-            for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
+            PairWork w;
+            for (int wi = 0; !aborted && pair_work(args, cluster, nclusters, wi, kb_per_tile, w); ++wi) {
                 int g, m, n;
-                tile_coords(args, tile, g, m, n);
+                tile_coords(args, w.tile, g, m, n);
                 const int a_row = m * Cfg::TILE_M + static_cast<int>(rank) * 128;
                 const int b_row = (EPI == EPI_GLU) ? (rank == 0 ? n * 128 : args.glu_up_row + n * 128)
                                                    : n * BN + static_cast<int>(rank) * 128;
-                int seg = 0, kb = 0;                   // (segment, block), advanced without division
-                for (int kk = 0; kk < kb_per_tile; kk += KSUB) {
-                    const int cnt = min(KSUB, kb_per_tile - kk);
+                int seg = w.kb_lo / args.k_blocks;     // (segment, block), then advanced without division
+                int kb = w.kb_lo - seg * args.k_blocks;
+                for (int kk = w.kb_lo; kk < w.kb_hi; kk += KSUB) {
+                    const int cnt = min(KSUB, w.kb_hi - kk);
                     if (!mbar_wait(empty_bar(grp), phase ^ 1u, abort_flag, args.status)) {
                         aborted = true;
                         break;
@@ -616,15 +657,16 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int tile = cluster; tile < args.total_tiles && !aborted; tile += nclusters) {
+            PairWork w;
+            for (int wi = 0; !aborted && pair_work(args, cluster, nclusters, wi, kb_per_tile, w); ++wi) {
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) {
                     aborted = true;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kk = 0; kk < kb_per_tile; kk += KSUB) {
-                    const int cnt = min(KSUB, kb_per_tile - kk);
+                for (int kk = w.kb_lo; kk < w.kb_hi; kk += KSUB) {
+                    const int cnt = min(KSUB, w.kb_hi - kk);
                     if (!mbar_wait(full_bar(grp), phase, abort_flag, args.status)) {
                         aborted = true;
                         break;
@@ -639,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
 #pragma unroll
                             for (int k = 0; k < BK / 16; ++k)
                                 tc_mma_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
-                                            ((kk + i) | k) != 0 ? 1u : 0u);
+                                            ((kk - w.kb_lo + i) | k) != 0 ? 1u : 0u);
                         }
                     }
                     tc_commit_pair(empty_bar(grp), 0x3);
@@ -662,9 +704,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
         const int row_in_tile = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = cluster; tile < args.total_tiles; tile += nclusters) {
+        uint32_t sk_phase = 0;
+        PairWork w;
+        for (int wi = 0; pair_work(args, cluster, nclusters, wi, kb_per_tile, w); ++wi) {
             int g, m, n;
-            tile_coords(args, tile, g, m, n);
+            tile_coords(args, w.tile, g, m, n);
             if (!mbar_wait_warp(tfull_bar(acc), acc_phase, abort_flag, args.status)) {
                 aborted = true;
                 break;
@@ -677,7 +721,53 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
             void* out = args.out[g];
             const uint16_t* bias = static_cast<const uint16_t*>(args.bias[g]);
             const int ncols = args.n_valid[g];
-            if (!warp_live) {          // rows past M (ragged last row-tile): nothing to read or store
+            // Stream-K tail: the partials of tile w.tile occupy slots sk_slot .. sk_slot + sk_parts - 2,
+            // each 256 x 256 fp32, this CTA's rows at [rank * 128, rank * 128 + 128).
+            const int sk_slot = (w.tile - args.sk_first) * (args.sk_parts - 1);
+            const size_t sk_row = (static_cast<size_t>(rank) * 128 + row_in_tile) * 256;
+            bool sk_owner = false;
+            if (EPI == EPI_STORE && w.part == 0 && w.tile >= args.sk_first && args.sk_parts > 1 && warp_live) {
+                // the first part adds the other parts: wait until each has stored its partial
+                bool ok = true;
+                for (int p = 1; p < args.sk_parts && ok; ++p)
+                    ok = flag_wait(args.sk_flags + (sk_slot + p - 1) * 2 + rank, abort_flag, args.status);
+                if (!__all_sync(0xffffffffu, ok)) aborted = true;
+                sk_owner = true;
+            }
+            if (EPI == EPI_STORE && w.part > 0) {
+                // A later part: store this CTA's rows of the fp32 accumulator to the part's slot; once
+                // all four epilogue warps have stored theirs, the first warp raises the slot's flag.
+                const int slot = sk_slot + w.part - 1;
+                float* dst = args.sk_scratch + static_cast<size_t>(slot) * (256 * 256) + sk_row;
+                if (warp_live) {
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        if (n * BN + c * 32 >= ncols) break;
+                        uint32_t r[32];
+                        tmem_ld32(taddr + c * 32, r);
+                        tmem_ld_wait();
+                        if (row_ok) {
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj)
+                                reinterpret_cast<float4*>(dst + c * 32)[jj] =
+                                    make_float4(__uint_as_float(r[4 * jj]), __uint_as_float(r[4 * jj + 1]),
+                                                __uint_as_float(r[4 * jj + 2]), __uint_as_float(r[4 * jj + 3]));
+                        }
+                    }
+                }
+                __threadfence();                      // this thread's partial is visible GPU-wide
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sk_bar);
+                if (q == 0) {
+                    bool ok = true;
+                    if (lane == 0) {
+                        ok = mbar_wait(sk_bar, sk_phase, abort_flag, args.status);
+                        if (ok) st_release_gpu(args.sk_flags + slot * 2 + rank, 1);
+                    }
+                    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) aborted = true;
+                }
+                sk_phase ^= 1u;
+            } else if (!warp_live || aborted) {   // rows past M (ragged last row-tile): nothing to read or store
             } else if (EPI == EPI_GLU) {
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; ++c) {
@@ -715,6 +805,21 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if (sk_owner && row_ok) {
+                        // the later parts' partials, added in part order
+                        for (int p = 1; p < args.sk_parts; ++p) {
+                            const float4* src = reinterpret_cast<const float4*>(
+                                args.sk_scratch + static_cast<size_t>(sk_slot + p - 1) * (256 * 256) + sk_row + c * 32);
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj) {
+                                const float4 s = src[jj];
+                                v[4 * jj] += s.x;
+                                v[4 * jj + 1] += s.y;
+                                v[4 * jj + 2] += s.z;
+                                v[4 * jj + 3] += s.w;
+                            }
+                        }
+                    }
                     if (bias != nullptr) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
@@ -768,6 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
                 acc = 0;
                 acc_phase ^= 1u;
             }
+            if (aborted) break;
         }
     }
 
@@ -1194,7 +1300,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn get_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
+    static std::atomic<EncodeTiledFn> cached{nullptr};  // racing first calls store the same entry point
+    EncodeTiledFn fn = cached.load(std::memory_order_relaxed);
     if (fn == nullptr) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -1203,33 +1310,92 @@ static EncodeTiledFn get_encode_fn() {
             q != cudaDriverEntryPointSuccess)
             return nullptr;
         fn = reinterpret_cast<EncodeTiledFn>(p);
+        cached.store(fn, std::memory_order_relaxed);
     }
     return fn;
+}
+
+// Encoded tensor maps, cached per host thread.  A GEMM call encodes one map
+// per operand and shard (up to 16), and an encoding depends only on the
+// pointer, the extents, the strides and the box, so a call that repeats an
+// earlier call's operands (every decode step, every layer of a replayed
+// schedule) copies the earlier encodings instead of encoding again.  The
+// cache is direct-mapped; a collision overwrites the older entry.
+struct MapKey {
+    const void* ptr;
+    uint64_t dims[3];
+    uint64_t strides[2];
+    uint32_t box_rows;
+    uint32_t rank;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && dims[0] == o.dims[0] && dims[1] == o.dims[1] && dims[2] == o.dims[2] &&
+               strides[0] == o.strides[0] && strides[1] == o.strides[1] && box_rows == o.box_rows && rank == o.rank;
+    }
+};
+struct MapEntry {
+    CUtensorMap map;
+    MapKey key;
+    bool valid;
+};
+constexpr int kMapCacheSlots = 128;
+
+static MapEntry& map_slot(const MapKey& k) {
+    thread_local MapEntry cache[kMapCacheSlots];
+    uint64_t h = reinterpret_cast<uintptr_t>(k.ptr) * 0x9E3779B97F4A7C15ull;
+    for (uint64_t v : {k.dims[0], k.dims[1], k.dims[2], k.strides[0], k.strides[1],
+                       static_cast<uint64_t>(k.box_rows) << 8 | k.rank})
+        h = (h ^ v) * 0x100000001B3ull;
+    return cache[(h >> 32) % kMapCacheSlots];
+}
+
+// Encode (or copy from the cache) one bf16 tensor map with 128-byte swizzle
+// and boxes of 64 elements by box_rows rows (by 2 in the third dimension).
+static bool encode_map(CUtensorMap* m, const void* ptr, uint32_t rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, int box_rows) {
+    MapKey k = {};
+    k.ptr = ptr;
+    k.rank = rank;
+    k.box_rows = static_cast<uint32_t>(box_rows);
+    for (uint32_t i = 0; i < rank; ++i) k.dims[i] = dims[i];
+    for (uint32_t i = 0; i + 1 < rank; ++i) k.strides[i] = strides[i];
+    MapEntry& e = map_slot(k);
+    if (e.valid && e.key == k) {
+        *m = e.map;
+        return true;
+    }
+    EncodeTiledFn enc = get_encode_fn();
+    if (enc == nullptr) return false;
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    e.map = *m;
+    e.key = k;
+    e.valid = true;
+    return true;
 }
 
 // bf16 K-major operand [rows, cols] with row stride ld (elements), tiles of
 // box_rows x 64 with 128-byte swizzle; out-of-range elements read as zero.
 static bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
-    EncodeTiledFn enc = get_encode_fn();
-    if (enc == nullptr) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_map(m, ptr, 2, dims, strides, box_rows);
 }
 
 static int sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    static int cache[64] = {0};
-    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    static std::atomic<int> cache[64];        // per device; relaxed: racing first calls store the same value
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (dev < 64) cache[dev] = n;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -1241,6 +1407,19 @@ static int raster_band(int tile_rows, int64_t k_total) {
     const int64_t tile_bytes = static_cast<int64_t>(tile_rows) * k_total * 2;
     const int64_t band = (static_cast<int64_t>(kRasterBandMB) << 20) / std::max<int64_t>(tile_bytes, 1);
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(band, 64)));
+}
+
+// Opt a kernel into its dynamic shared memory.  The attribute lasts for the
+// process, so it is set once per device (bit `dev` of `done`, one word per
+// kernel instantiation) and later launches skip the driver call.
+static bool smem_attribute_once(const void* kern, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    if (bit != 0) done.fetch_or(bit, std::memory_order_relaxed);
+    return true;
 }
 
 // Programmatic dependent launch (GemmDesc::pdl): the attribute lets the GEMM
@@ -1255,16 +1434,9 @@ static void set_pdl(cudaLaunchAttribute& at) {
 // rows of up) as a 3-D tensor {cols, half_rows, 2}: one box of box_rows rows of
 // each half lands as the gate tile followed by the up tile, in one TMA load.
 static bool make_map_glu(CUtensorMap* m, const void* ptr, int64_t half_rows, int64_t cols, int64_t ld, int box_rows) {
-    EncodeTiledFn enc = get_encode_fn();
-    if (enc == nullptr) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(half_rows), 2};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(half_rows * ld) * 2};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 2};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_map(m, ptr, 3, dims, strides, box_rows);
 }
 
 template <int BN, int STAGES, int EPI, int AROWS = BM, int KSUB = 1>
@@ -1293,8 +1465,8 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
         if (!ok) return TP_ERR_CUDA;
     }
     auto kern = tp_gemm_kernel<BN, STAGES, EPI, AROWS, KSUB>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
-        return TP_ERR_CUDA;
+    static std::atomic<uint64_t> smem_set{0};
+    if (!smem_attribute_once(reinterpret_cast<const void*>(kern), Cfg::SMEM_BYTES, smem_set)) return TP_ERR_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return TP_ERR_CUDA;
     const int grid = std::min(a.total_tiles, sms);
@@ -1330,8 +1502,8 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
         if (!make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, 128)) return TP_ERR_CUDA;
     }
     auto kern = tp_gemm_pair_kernel<STAGES, EPI, KSUB>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
-        return TP_ERR_CUDA;
+    static std::atomic<uint64_t> smem_set{0};
+    if (!smem_attribute_once(reinterpret_cast<const void*>(kern), Cfg::SMEM_BYTES, smem_set)) return TP_ERR_CUDA;
     const int sms = sm_count();
     if (sms < 2) return TP_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1348,17 +1520,38 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // A persistent grid of pairs that can all be resident at once (per device).
-    static int max_clusters[64] = {0};
+    static std::atomic<int> max_clusters[64];  // relaxed: racing first calls store the same value
     int dev = 0;
     cudaGetDevice(&dev);
-    int scratch_mc = 0;
-    int& mc = (dev >= 0 && dev < 64) ? max_clusters[dev] : scratch_mc;
+    const bool cached_dev = dev >= 0 && dev < 64;
+    int mc = cached_dev ? max_clusters[dev].load(std::memory_order_relaxed) : 0;
     if (mc <= 0) {
         int v = 0;
         if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess || v <= 0) v = sms / 2;
         mc = std::min(v, sms / 2);
+        if (cached_dev) max_clusters[dev].store(mc, std::memory_order_relaxed);
     }
     const int clusters = std::min(a.total_tiles, mc);
+    // Stream-K tail (store epilogue, given a workspace): when the last wave of whole tiles would
+    // leave clusters idle, its L tiles are cut into S = clusters / L parts along K, one unit per
+    // cluster, so that wave takes about 1/S of a tile's time.  Each part keeps at least two
+    // groups of K blocks.
+    a.sk_first = a.total_tiles;
+    a.sk_parts = 1;
+    if (EPI == EPI_STORE && d.sk_ws != nullptr && clusters == mc) {
+        const int waves = a.total_tiles / clusters;
+        const int tail = a.total_tiles - waves * clusters;
+        const int kbt = a.k_blocks * d.segs;
+        int parts = tail > 0 ? std::min(std::min(clusters / tail, kSkMaxParts), kbt / (2 * KSUB)) : 1;
+        const int64_t slots = static_cast<int64_t>(tail) * (parts - 1);
+        if (waves >= 1 && parts >= 2 && slots <= kSkMaxSlots && slots * 2 * 4 <= static_cast<int64_t>(kSkFlagBytes) &&
+            kSkFlagBytes + static_cast<size_t>(slots) * kSkSlotBytes <= d.sk_ws_bytes) {
+            a.sk_first = waves * clusters;
+            a.sk_parts = parts;
+            a.sk_flags = static_cast<int*>(d.sk_ws);
+            a.sk_scratch = reinterpret_cast<float*>(static_cast<char*>(d.sk_ws) + kSkFlagBytes);
+        }
+    }
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.numAttrs = d.pdl ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TP_ERR_CUDA;
@@ -1390,8 +1583,8 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
         if (!ok) return TP_ERR_CUDA;
     }
     auto kern = tp_gemm_splitk_kernel<BN, STAGES, EPI, KSUB>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
-        return TP_ERR_CUDA;
+    static std::atomic<uint64_t> smem_set{0};
+    if (!smem_attribute_once(reinterpret_cast<const void*>(kern), Cfg::SMEM_BYTES, smem_set)) return TP_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs * a.total_tiles, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1406,15 +1599,16 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // persistent: no more clusters than can be resident at once (cached per device and size)
-    static int max_clusters[64][9] = {};
+    static std::atomic<int> max_clusters[64][9];  // relaxed: racing first calls store the same value
     int dev = 0;
     cudaGetDevice(&dev);
-    int scratch_mc = 0;
-    int& mc = (dev >= 0 && dev < 64) ? max_clusters[dev][cs] : scratch_mc;
+    const bool cached_dev = dev >= 0 && dev < 64;
+    int mc = cached_dev ? max_clusters[dev][cs].load(std::memory_order_relaxed) : 0;
     if (mc <= 0) {
         int v = 0;
         if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess || v <= 0) return TP_ERR_CUDA;
         mc = v;
+        if (cached_dev) max_clusters[dev][cs].store(mc, std::memory_order_relaxed);
     }
     const int cap = d.split_clusters > 0 ? std::min(mc, d.split_clusters) : mc;
     cfg.gridDim = dim3(cs * std::min(a.total_tiles, cap), 1, 1);

@@ -9,6 +9,18 @@
 
 namespace tpk {
 
+// Stream-K tail of the CTA-pair GEMM with the store epilogue: when a
+// workspace is given (GemmDesc::sk_ws), the tiles of a partial last wave are
+// split along K into parts; every part after the first writes its fp32
+// accumulator (256 x 256) to a slot of the workspace and raises a flag, and
+// the first part adds them in order before its epilogue.  Workspace: flags
+// (zeroed by the caller before the launch), then the slots.
+constexpr size_t kSkFlagBytes = 4096;
+constexpr size_t kSkSlotBytes = 256u * 256u * 4u;
+constexpr int kSkMaxSlots = 128;
+constexpr int kSkMaxParts = 4;
+constexpr size_t kSkWorkspaceBytes = kSkFlagBytes + kSkMaxSlots * kSkSlotBytes;
+
 // One tensor-parallel GEMM launch: for each group g,
 //   D_g = sum_s A_{g,s} B_{g,s}^T, A [M, K] (lda), B [b_rows, K] (ldb), bf16.
 struct GemmDesc {
@@ -41,9 +53,18 @@ struct GemmDesc {
     // kernel of a call, whose predecessor may have written anything: nothing is loaded
     // before the wait.
     int pdl = 0;
+    // Stream-K tail workspace (see kSkWorkspaceBytes), or null: the pair kernel
+    // then runs whole tiles only.  Its flags must be zero when the launch starts.
+    void* sk_ws = nullptr;
+    size_t sk_ws_bytes = 0;
 };
 
 tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream);
+
+// Workspace bytes tp_mlp_forward cannot do without (H and the partials);
+// tp_mlp_workspace_size adds the optional stream-K tail area.  0 for invalid
+// arguments.
+size_t mlp_workspace_required(int t, int64_t n, int64_t h, int64_t f, tp_reduce_mode mode, tp_dtype partial_dtype);
 
 // The kernel launch_gemm picks for `d` on `sms` SMs: kind 0 = single-CTA tiles of
 // width bn, 1 = CTA pairs (256 x 256 tiles), 2 = split-K clusters of cs CTAs on

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "common.cuh"
@@ -193,25 +194,30 @@ __global__ void __launch_bounds__(256) shard_reduce_kernel(const __grid_constant
 
 template <bool IN_BF16, int G>
 static int resident_blocks() {
-    static int n = 0;
-    if (n <= 0) {
+    static std::atomic<int> n{0};               // relaxed: racing first calls store the same value
+    int c = n.load(std::memory_order_relaxed);
+    if (c <= 0) {
         int v = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, shard_reduce_kernel<IN_BF16, G>, 256, 0) != cudaSuccess ||
             v <= 0)
             v = 2;
-        n = v;
+        c = v;
+        n.store(c, std::memory_order_relaxed);
     }
-    return n;
+    return c;
 }
 
 static int sm_count_cached() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    static int cache[64] = {0};
-    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    static std::atomic<int> cache[64];        // per device; relaxed: racing first calls store the same value
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (dev < 64) cache[dev] = n;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
