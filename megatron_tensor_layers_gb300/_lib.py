@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import List, Optional, Sequence
 
 import torch
@@ -95,8 +96,17 @@ def _check(fn: str, code: int) -> None:
         raise TPError(fn, code)
 
 
+# The current stream as a raw handle, without building a torch Stream object
+# (torch's own kernel launchers use the same entry point); older builds fall
+# back to torch.cuda.current_stream().
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_raw_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
+        if _raw_stream is not None and _raw_device is not None:
+            return _raw_stream(_raw_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
 
@@ -105,12 +115,28 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+# Host arrays of per-shard device pointers.  The C ABI reads them during the
+# call only, so each thread reuses a small ring of arrays instead of building
+# new ctypes objects on every call (a call passes at most three lists).
+_PTR_RING = 8
+_tls = threading.local()
+
+
 def _ptrs(ts: Optional[Sequence[Optional[torch.Tensor]]]):
     if ts is None:
         return None
-    arr = (ctypes.c_void_p * len(ts))()
-    for i, t in enumerate(ts):
-        arr[i] = None if t is None else t.data_ptr()
+    n = len(ts)
+    if n > MAX_SHARDS:
+        arr = (ctypes.c_void_p * n)()
+    else:
+        ring = getattr(_tls, "ring", None)
+        if ring is None:
+            ring = _tls.ring = [(ctypes.c_void_p * MAX_SHARDS)() for _ in range(_PTR_RING)]
+            _tls.next = 0
+        i = _tls.next
+        _tls.next = (i + 1) % _PTR_RING
+        arr = ring[i]
+    arr[:n] = [None if t is None else t.data_ptr() for t in ts]
     return arr
 
 
@@ -133,35 +159,69 @@ def _dt(dtype) -> int:
 # on the GPU (a host pointer handed to a kernel would be an illegal address).
 
 
-def _tensor(name: str, t, shape=None, dtypes=None) -> torch.Tensor:
+# Each check takes a fast path (plain comparisons) and builds its message only
+# when it fails.  `name` is a string or a (list name, index) pair, formatted
+# only for the message.
+
+def _nm(name) -> str:
+    return f"{name[0]}[{name[1]}]" if isinstance(name, tuple) else name
+
+
+def _tensor(name, t, shape=None, dtypes=None) -> torch.Tensor:
     if not isinstance(t, torch.Tensor):
-        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
-    if shape is not None and tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+        raise TypeError(f"{_nm(name)} must be a torch.Tensor, got {type(t).__name__}")
+    if shape is not None and t.shape != shape:
+        raise ValueError(f"{_nm(name)} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     if dtypes is not None and t.dtype not in dtypes:
-        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {list(dtypes)}")
+        raise TypeError(f"{_nm(name)} has dtype {t.dtype}, expected one of {list(dtypes)}")
     return t
 
 
-def _matrix(name: str, t, shape=None, dtypes=None) -> torch.Tensor:
+def _matrix(name, t, shape=None, dtypes=None) -> torch.Tensor:
     """A row-major 2-D tensor (unit column stride, any row stride)."""
     _tensor(name, t, shape, dtypes)
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1) or t.stride(0) < t.shape[1]:
-        raise ValueError(f"{name} must be a row-major matrix with unit column stride")
+        raise ValueError(f"{_nm(name)} must be a row-major matrix with unit column stride")
     return t
 
 
-def _dense(name: str, t, shape=None, dtypes=None) -> torch.Tensor:
+def _dense(name, t, shape=None, dtypes=None) -> torch.Tensor:
     _tensor(name, t, shape, dtypes)
     if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+        raise ValueError(f"{_nm(name)} must be contiguous")
     return t
+
+
+def _matrices(name: str, ts, shape, dtypes) -> int:
+    """Every ts[r] is a row-major matrix of `shape` and one of `dtypes`, all
+    with one row stride, which is returned (the ABI takes one per list)."""
+    ld = None
+    for r, t in enumerate(ts):
+        if not (isinstance(t, torch.Tensor) and t.shape == shape and t.dtype in dtypes and t.dim() == 2):
+            _matrix((name, r), t, shape, dtypes)
+        s0, s1 = t.stride()
+        if (s1 != 1 and shape[1] > 1) or s0 < shape[1]:
+            _matrix((name, r), t, shape, dtypes)
+        if ld is None:
+            ld = s0
+        elif s0 != ld:
+            _same_ld(name, ts)
+    return ld
+
+
+def _denses(name: str, ts, shape, dtypes) -> None:
+    """Every ts[r] is a contiguous tensor of `shape` and one of `dtypes`."""
+    for r, t in enumerate(ts):
+        if not (isinstance(t, torch.Tensor) and t.shape == shape and t.dtype in dtypes and t.is_contiguous()):
+            _dense((name, r), t, shape, dtypes)
 
 
 def _same_ld(name: str, ts: Sequence[torch.Tensor]) -> None:
-    lds = {t.stride(0) for t in ts}
-    if len(lds) > 1:
-        raise ValueError(f"every {name}[r] must have the same row stride (got {sorted(lds)})")
+    ld = ts[0].stride(0)
+    for t in ts:
+        if t.stride(0) != ld:
+            lds = {u.stride(0) for u in ts}
+            raise ValueError(f"every {name}[r] must have the same row stride (got {sorted(lds)})")
 
 
 def _shard_count(name: str, ts) -> int:
@@ -172,16 +232,20 @@ def _shard_count(name: str, ts) -> int:
 
 def _on_gpu(*groups) -> None:
     """Every tensor (or list of tensors; None entries skipped) is a CUDA tensor of one device."""
-    devs = set()
+    dev = None
     for g in groups:
-        for t in (g if isinstance(g, (list, tuple)) else [g]):
+        if g is None:
+            continue
+        for t in ((g,) if isinstance(g, torch.Tensor) else g):
             if t is None:
                 continue
-            if not t.is_cuda:
+            d = t.get_device()
+            if d < 0:
                 raise ValueError("every tensor argument must be a CUDA tensor (the library has no CPU path)")
-            devs.add(t.device)
-    if len(devs) > 1:
-        raise ValueError(f"tensor arguments span devices {sorted(str(d) for d in devs)}")
+            if dev is None:
+                dev = d
+            elif d != dev:
+                raise ValueError(f"tensor arguments span devices cuda:{dev} and cuda:{d}")
 
 
 BF16 = (torch.bfloat16,)
@@ -205,9 +269,7 @@ def tp_linear_col(x: torch.Tensor, w: Sequence[torch.Tensor], *, act: str = "non
     if act not in ACTS:
         raise ValueError(f"act must be one of {list(ACTS)}")
     rows = w[0].shape[0] if w[0].dim() == 2 else -1
-    for r in range(t):
-        _matrix(f"w[{r}]", w[r], (rows, k), BF16)
-    _same_ld("w", w)
+    ldw = _matrices("w", w, (rows, k), BF16)
     gated = act != "none"
     if gated and rows % 2:
         raise ValueError("a gated weight block holds gate rows then as many up rows: its row count must be even")
@@ -217,7 +279,7 @@ def tp_linear_col(x: torch.Tensor, w: Sequence[torch.Tensor], *, act: str = "non
         if len(bias) != t:
             raise ValueError("bias must hold one vector per shard")
         for r in range(t):
-            _dense(f"bias[{r}]", bias[r], (os_,), BF16)
+            _dense(("bias", r), bias[r], (os_,), BF16)
     if y is None:
         if gather_output:
             y = torch.empty((n, out_full), dtype=y_dtype, device=x.device)
@@ -226,14 +288,12 @@ def tp_linear_col(x: torch.Tensor, w: Sequence[torch.Tensor], *, act: str = "non
     ys = [y] if gather_output else list(y)
     if len(ys) != (1 if gather_output else t):
         raise ValueError("y must be one tensor with gather_output, else one per shard")
-    for i, yi in enumerate(ys):
-        _matrix(f"y[{i}]", yi, (n, out_full if gather_output else os_), BF16_F32)
-    if len({yi.dtype for yi in ys}) > 1:
-        raise TypeError("every y[r] must have the same dtype")
-    _same_ld("y", ys)
-    _on_gpu(x, list(w), list(bias) if bias is not None else None, ys)
-    ldy = _ld(ys[0])
-    code = load().tp_linear_col(t, n, k, out_full, _ptr(x), _ld(x), _ptrs(w), _ld(w[0]), _ptrs(bias),
+    ldy = _matrices("y", ys, (n, out_full if gather_output else os_), BF16_F32)
+    for yi in ys:
+        if yi.dtype is not ys[0].dtype:
+            raise TypeError("every y[r] must have the same dtype")
+    _on_gpu(x, w, bias, ys)
+    code = load().tp_linear_col(t, n, k, out_full, _ptr(x), _ld(x), _ptrs(w), ldw, _ptrs(bias),
                                 ACTS[act], int(gather_output), _ptrs(ys), ldy, _dt(ys[0].dtype), _stream(stream))
     _check("tp_linear_col", code)
     return y
@@ -250,11 +310,8 @@ def tp_linear_row(x: Sequence[torch.Tensor], w: Sequence[torch.Tensor], *, bias:
         raise ValueError("x and w must hold the same number of shards")
     n, ks = _matrix("x[0]", x[0], dtypes=BF16).shape
     out = _matrix("w[0]", w[0], dtypes=BF16).shape[0]
-    for r in range(t):
-        _matrix(f"x[{r}]", x[r], (n, ks), BF16)
-        _matrix(f"w[{r}]", w[r], (out, ks), BF16)
-    _same_ld("x", x)
-    _same_ld("w", w)
+    ldx = _matrices("x", x, (n, ks), BF16)
+    ldw = _matrices("w", w, (out, ks), BF16)
     if mode not in MODES:
         raise ValueError(f"mode must be one of {list(MODES)}")
     if bias is not None:
@@ -267,15 +324,14 @@ def tp_linear_row(x: Sequence[torch.Tensor], w: Sequence[torch.Tensor], *, bias:
     if partials is not None:
         if len(partials) != t:
             raise ValueError("partials must hold one buffer per shard")
-        for r in range(t):
-            _matrix(f"partials[{r}]", partials[r], (n, out), (partials[0].dtype,) if r else BF16_F32)
-        _same_ld("partials", partials)
+        _matrix(("partials", 0), partials[0], (n, out), BF16_F32)
+        _matrices("partials", partials, (n, out), (partials[0].dtype,))
     if y is not None:
         _matrix("y", y, (n, out), BF16_F32)
-    _on_gpu(list(x), list(w), bias, partials, y)
+    _on_gpu(x, w, bias, partials, y)
     ldp = _ld(partials[0]) if partials is not None else out
     pdt = partials[0].dtype if partials is not None else partial_dtype
-    code = load().tp_linear_row(t, n, ks * t, out, _ptrs(x), _ld(x[0]), _ptrs(w), _ld(w[0]), _ptr(bias),
+    code = load().tp_linear_row(t, n, ks * t, out, _ptrs(x), ldx, _ptrs(w), ldw, _ptr(bias),
                                 int(reduce_results), MODES[mode], _dt(pdt), _ptrs(partials), ldp,
                                 _ptr(y), _ld(y) if y is not None else out, _dt(y.dtype) if y is not None else 0,
                                 _stream(stream))
@@ -289,8 +345,10 @@ def tp_shard_reduce(partials: Sequence[torch.Tensor], *, out: Optional[torch.Ten
     """All-reduce (sum) of t equally shaped partial buffers."""
     t = _shard_count("partials", partials)
     p0 = _dense("partials[0]", partials[0], dtypes=BF16_F32)
-    for r in range(t):
-        _dense(f"partials[{r}]", partials[r], tuple(p0.shape), (p0.dtype,))
+    shape, dt = p0.shape, p0.dtype
+    for r, p in enumerate(partials):
+        if not (isinstance(p, torch.Tensor) and p.shape == shape and p.dtype is dt and p.is_contiguous()):
+            _dense(("partials", r), p, shape, (dt,))
     if mode not in ("direct", "ring"):
         raise ValueError("mode must be 'direct' or 'ring'")
     if out is None and alloc_out and not replicate:
@@ -299,7 +357,7 @@ def tp_shard_reduce(partials: Sequence[torch.Tensor], *, out: Optional[torch.Ten
         _dense("out", out, dtypes=BF16_F32)
         if out.numel() != p0.numel():
             raise ValueError(f"out holds {out.numel()} elements, the partials {p0.numel()}")
-    _on_gpu(list(partials), out)
+    _on_gpu(partials, out)
     code = load().tp_shard_reduce(t, p0.numel(), _dt(p0.dtype), _ptrs(partials), _ptr(out),
                                   _dt(out.dtype) if out is not None else 0, MODES[mode], _dt(hop_dtype),
                                   int(replicate), _stream(stream))
@@ -321,10 +379,8 @@ def _mlp_args(x, w_gate_up, w_down, bias_down, act, mode):
     if rows % 2:
         raise ValueError("w_gate_up[r] holds gate rows then as many up rows: its row count must be even")
     fs = rows // 2
-    for r in range(t):
-        _dense(f"w_gate_up[{r}]", w_gate_up[r], (2 * fs, h), BF16)
-        _matrix(f"w_down[{r}]", w_down[r], (h, fs), BF16)
-    _same_ld("w_down", w_down)
+    _denses("w_gate_up", w_gate_up, (2 * fs, h), BF16)
+    _matrices("w_down", w_down, (h, fs), BF16)
     if bias_down is not None:
         _dense("bias_down", bias_down, (h,), BF16)
     return t, n, h, fs * t
@@ -348,7 +404,7 @@ def tp_mlp_forward(x: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_down: S
         y = torch.empty((n, h), dtype=y_dtype, device=x.device)
     _dense("workspace", workspace)
     _dense("y", y, (n, h), BF16_F32)
-    _on_gpu(x, list(w_gate_up), list(w_down), bias_down, workspace, y)
+    _on_gpu(x, w_gate_up, w_down, bias_down, workspace, y)
     code = load().tp_mlp_forward(t, n, h, f, _ptr(x), _ld(x), _ptrs(w_gate_up), _ptrs(w_down), _ld(w_down[0]),
                                  _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _ptr(y), _dt(y.dtype), _stream(stream))
@@ -375,7 +431,7 @@ def vocab_parallel_embed(ids: torch.Tensor, table: Sequence[Optional[torch.Tenso
             if rows_r:
                 raise ValueError(f"table[{r}] is None but rank {r} owns {rows_r} ids")
             continue
-        _dense(f"table[{r}]", table[r], (rows_r, h), (ref.dtype,))
+        _dense(("table", r), table[r], (rows_r, h), (ref.dtype,))
     n = ids.numel()
     if out is None:
         out = torch.empty((n, h), dtype=ref.dtype, device=ids.device)
@@ -384,8 +440,8 @@ def vocab_parallel_embed(ids: torch.Tensor, table: Sequence[Optional[torch.Tenso
         if len(partials) != t:
             raise ValueError("partials must hold one buffer per shard")
         for r in range(t):
-            _dense(f"partials[{r}]", partials[r], (n, h), (ref.dtype,))
-    _on_gpu(ids, list(table), out, partials)
+            _dense(("partials", r), partials[r], (n, h), (ref.dtype,))
+    _on_gpu(ids, table, out, partials)
     code = load().vocab_parallel_embed(t, vocab, h, _ptr(ids), n, _ptrs(table), _dt(ref.dtype), _ptr(out),
                                        _ptrs(partials), _stream(stream))
     _check("vocab_parallel_embed", code)
@@ -406,15 +462,15 @@ def lm_head_sharded(x: torch.Tensor, table: Sequence[Optional[torch.Tensor]], vo
             if widths[r]:
                 raise ValueError(f"table[{r}] is None but rank {r} owns {widths[r]} ids")
             continue
-        _dense(f"table[{r}]", table[r], (widths[r], h), BF16)
+        _dense(("table", r), table[r], (widths[r], h), BF16)
     if per_shard:
         if shard_logits is None:
             shard_logits = [torch.empty((n, wd), dtype=out_dtype, device=x.device) for wd in widths]
         if len(shard_logits) != t:
             raise ValueError("shard_logits must hold one buffer per shard")
         for r in range(t):
-            _dense(f"shard_logits[{r}]", shard_logits[r], (n, widths[r]), (shard_logits[0].dtype,) if r else BF16_F32)
-        _on_gpu(x, list(table), list(shard_logits))
+            _dense(("shard_logits", r), shard_logits[r], (n, widths[r]), (shard_logits[0].dtype,) if r else BF16_F32)
+        _on_gpu(x, table, shard_logits)
         code = load().lm_head_sharded(t, n, h, vocab, _ptr(x), _ld(x), _ptrs(table), None, 0,
                                       _ptrs(shard_logits), _dt(shard_logits[0].dtype), _stream(stream))
         _check("lm_head_sharded", code)
@@ -422,7 +478,7 @@ def lm_head_sharded(x: torch.Tensor, table: Sequence[Optional[torch.Tensor]], vo
     if logits is None:
         logits = torch.empty((n, vocab), dtype=out_dtype, device=x.device)
     _matrix("logits", logits, (n, vocab), BF16_F32)
-    _on_gpu(x, list(table), logits)
+    _on_gpu(x, table, logits)
     code = load().lm_head_sharded(t, n, h, vocab, _ptr(x), _ld(x), _ptrs(table), _ptr(logits), _ld(logits),
                                   None, _dt(logits.dtype), _stream(stream))
     _check("lm_head_sharded", code)
@@ -437,14 +493,14 @@ def tp_shard_gather(shards: Sequence[torch.Tensor], *, out: Optional[torch.Tenso
         raise ValueError("shards must be 2-D")
     rows = s0.shape[0]
     for r in range(t):
-        _dense(f"shards[{r}]", shards[r], dtypes=(s0.dtype,))
+        _dense(("shards", r), shards[r], dtypes=(s0.dtype,))
         if shards[r].dim() != 2 or shards[r].shape[0] != rows:
             raise ValueError(f"shards[{r}] must be [{rows}, cols_r]")
     cols = (ctypes.c_int64 * t)(*[s.shape[1] for s in shards])
     if out is None:
         out = torch.empty((rows, sum(s.shape[1] for s in shards)), dtype=shards[0].dtype, device=shards[0].device)
     _dense("out", out, (rows, sum(s.shape[1] for s in shards)), (s0.dtype,))
-    _on_gpu(list(shards), out)
+    _on_gpu(shards, out)
     code = load().tp_shard_gather(t, rows, cols, _dt(shards[0].dtype), _ptrs(shards), _ptr(out), _stream(stream))
     _check("tp_shard_gather", code)
     return out
@@ -506,7 +562,7 @@ def tp_mlp_forward_static(x: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_
     if y is None:
         y = torch.empty((n, h), dtype=y_dtype, device=x.device)
     _dense("y", y, (n, h), BF16_F32)
-    _on_gpu(x, list(w_gate_up), list(w_down), bias_down, y)
+    _on_gpu(x, w_gate_up, w_down, bias_down, y)
     code = load().tp_mlp_forward_static(t, n, h, f, _ptr(x), _ld(x), _ptrs(w_gate_up), _ptrs(w_down),
                                         _ld(w_down[0]), _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype),
                                         _ptr(y), _dt(y.dtype), _stream(stream))
@@ -530,7 +586,7 @@ def tp_mlp_forward_host(x_host: torch.Tensor, w_gate_up: Sequence[torch.Tensor],
     _dense("y_host", y_host, (n, h), BF16_F32)
     _dense("y_dev", y_dev, (n, h), (y_host.dtype,))
     _dense("workspace", workspace)
-    _on_gpu(x_dev, list(w_gate_up), list(w_down), bias_down, y_dev, workspace)
+    _on_gpu(x_dev, w_gate_up, w_down, bias_down, y_dev, workspace)
     if copy_stream is None:
         copy_stream = torch.cuda.Stream(device=x_dev.device)
     code = load().tp_mlp_forward_host(t, n, h, f, _ptr(x_host), _ptrs(w_gate_up), _ptrs(w_down), _ld(w_down[0]),
@@ -553,7 +609,7 @@ def tp_reduce_scatter_rmsnorm(partials: Sequence[torch.Tensor], weight: torch.Te
         raise ValueError("partials must be [n, h]")
     n, h = p0.shape
     for r in range(t):
-        _dense(f"partials[{r}]", partials[r], (n, h), (p0.dtype,))
+        _dense(("partials", r), partials[r], (n, h), (p0.dtype,))
     if mode not in ("direct", "ring"):
         raise ValueError("mode must be 'direct' or 'ring'")
     _dense("weight", weight, (h,), BF16)
@@ -564,7 +620,7 @@ def tp_reduce_scatter_rmsnorm(partials: Sequence[torch.Tensor], weight: torch.Te
     if out is None:
         out = torch.empty((n, h), dtype=torch.bfloat16, device=partials[0].device)
     _dense("out", out, (n, h), BF16)
-    _on_gpu(list(partials), weight, residual, residual_out, out)
+    _on_gpu(partials, weight, residual, residual_out, out)
     code = load().tp_reduce_scatter_rmsnorm(t, n, h, _dt(partials[0].dtype), _ptrs(partials), _ptr(residual),
                                             _ptr(weight), eps, MODES[mode], _ptr(residual_out), _ptr(out),
                                             _stream(stream))

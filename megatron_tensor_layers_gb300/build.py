@@ -86,5 +86,28 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB_PATH
 
 
+ABI_OVERHEAD_SRC = os.path.join(PKG, "abi_overhead", "abi_overhead.c")
+ABI_OVERHEAD_BIN = os.path.join(BUILD_DIR, "abi_overhead")
+
+
+def build_abi_overhead() -> str:
+    """Compile the host-overhead probe (a C program that times enqueues of
+    the C-ABI entry points with no Python in the loop) against the library;
+    returns the executable's path."""
+    lib = build()
+    if os.path.exists(ABI_OVERHEAD_BIN) and os.path.getmtime(ABI_OVERHEAD_BIN) >= max(
+            os.path.getmtime(lib), os.path.getmtime(ABI_OVERHEAD_SRC)):
+        return ABI_OVERHEAD_BIN
+    cuda = os.path.dirname(os.path.dirname(_nvcc()))
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    cmd = [shutil.which("gcc") or "gcc", "-O2", "-I", INCLUDE, "-I", os.path.join(cuda, "include"), ABI_OVERHEAD_SRC,
+           "-L", PKG, "-ltp_gb300", "-L", os.path.join(cuda, "lib64"), "-lcudart",
+           "-Wl,-rpath," + PKG + ":" + os.path.join(cuda, "lib64"), "-o", ABI_OVERHEAD_BIN]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("gcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+    return ABI_OVERHEAD_BIN
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
