@@ -3,9 +3,14 @@
 The Llama-3.1-70B-shaped MLP (h=8192, f=28672) runs on the GPU exactly as
 bench.py times it (t=4 and t=8, n=8192 prefill; n in {1,16,64} decode); the
 oracle computes a seeded sample of 32 token rows (first/last rows and both
-sides of a 128-row tile boundary included) in fp64 from the same bits.
-Output rows depend only on their own input row, so a sample is a complete
-check of those rows.  The shard reduce at its largest size is compared bit
+sides of a 128-row tile boundary included) in fp64 from the same bits, and
+the gates of ``gpu_helpers.mlp_check`` apply (2e-3 RMS against the oracle
+that rounds H to bf16, 1e-2 RMS against the unrounded definition).  Output
+rows depend only on their own input row, so a sample is a complete check of
+those rows.  With integer-valued inputs the same GEMM launches (CTA pairs,
+the raster bands, the K loop over 8192/7168 columns, bf16 partials, the
+fused reduce) are compared bit for bit on rows at both sides of every
+256-row tile and raster band.  The shard reduce at its largest size is compared bit
 for bit with the oracle's emulation on windows around every ring-chunk
 boundary, the LM head at its configured size on sampled rows, and the
 attention block's QKV and o_proj projections at the same model's shapes.
@@ -20,7 +25,7 @@ from megatron_tensor_layers_gb300 import _lib as tp
 from megatron_tensor_layers_gb300 import synth
 from megatron_tensor_layers_gb300.build import build
 
-from gpu_helpers import exact, f64, gemm_gate, half_ulp_bf16
+from gpu_helpers import exact, f64, gemm_gate, h_flip_check, half_ulp_bf16, mlp_check
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -50,21 +55,9 @@ def _shards(d, t):
     return wgu, wds
 
 
-def _reference(xs, hst, t, partial_bf16):
-    """fp64 rows of the unsharded MLP and the per-element allowance for the
-    bf16 roundings of H (and of the partials)."""
-    wg, wu, wd = hst["wg"], hst["wu"], hst["wd"]
-    fs = F // t
-    ref = O.mlp_unsharded(xs, wg, wu, wd, None, "silu")
-    extra = 0.0
-    for r in range(t):
-        blk = O.merged_column_shard([wg, wu], t, r)
-        h = O.glu(O.linear(xs, blk[:fs]), O.linear(xs, blk[fs:]), "silu")
-        bd = O.row_shard(wd, t, r)
-        extra = extra + half_ulp_bf16(h) @ np.abs(bd).T
-        if partial_bf16:
-            extra = extra + half_ulp_bf16(O.linear(h, bd))
-    return ref, extra
+def _check(y_rows, xs, d, t, **kw):
+    hst = d["host"]
+    return mlp_check(y_rows, xs, hst["wg"], hst["wu"], hst["wd"], t, **kw)
 
 
 @pytest.mark.parametrize("t", [4, 8])
@@ -82,19 +75,25 @@ def test_prefill_bench_launch_sequence(mlp70b, t):
     tp.tp_shard_reduce(parts, out=y, mode="direct")
     torch.cuda.synchronize()
     assert tp.tp_device_status() == 0
-    ref, extra = _reference(d["host"]["x"], d["host"], t, partial_bf16=True)
-    gemm_gate(f64(y[d["rows"]]), ref, bf16_out=True, extra=extra)
+    _check(f64(y[d["rows"]]), d["host"]["x"], d, t, partial="bf16", y_bf16=True, row_ids=d["rows"], n_total=NTOK)
+    # the gated column GEMM's H itself: the exact act(G) * U rounded to bf16, up to flips at midpoints
+    xs, hst = d["host"]["x"], d["host"]
+    for r in range(t):
+        blk = O.merged_column_shard([hst["wg"], hst["wu"]], t, r)
+        h_exact = O.glu(O.linear(xs, blk[:fs]), O.linear(xs, blk[fs:]), "silu")
+        h_flip_check(f64(hs[r][d["rows"]]), h_exact)
 
 
-@pytest.mark.parametrize("mode", ["fused", "ring"])
-def test_prefill_mlp_forward_modes(mlp70b, mode):
+@pytest.mark.parametrize("mode,pdt", [("fused", torch.float32), ("ring", torch.float32), ("ring", torch.bfloat16),
+                                      ("direct", torch.float32)])
+def test_prefill_mlp_forward_modes(mlp70b, mode, pdt):
     d = mlp70b
     t = 4
     wgu, wds = _shards(d, t)
-    y = tp.tp_mlp_forward(d["x"], wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
+    y = tp.tp_mlp_forward(d["x"], wgu, wds, mode=mode, partial_dtype=pdt, y_dtype=torch.float32)
     torch.cuda.synchronize()
-    ref, extra = _reference(d["host"]["x"], d["host"], t, partial_bf16=False)
-    gemm_gate(f64(y[d["rows"]]), ref, bf16_out=False, extra=extra)
+    _check(f64(y[d["rows"]]), d["host"]["x"], d, t, mode=mode, partial="bf16" if pdt == torch.bfloat16 else "f32",
+           row_ids=d["rows"], n_total=NTOK)
 
 
 @pytest.mark.parametrize("n", [1, 16, 64])
@@ -106,8 +105,24 @@ def test_decode_all_rows(mlp70b, n, mode):
     x = d["x"][:n].contiguous()
     y = tp.tp_mlp_forward(x, wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
     torch.cuda.synchronize()
-    ref, extra = _reference(f64(x), d["host"], t, partial_bf16=False)
-    gemm_gate(f64(y), ref, bf16_out=False, extra=extra)
+    _check(f64(y), f64(x), d, t, mode=mode)
+
+
+@pytest.mark.parametrize("n", [1, 16, 64])
+def test_decode_gated_column_h(mlp70b, n):
+    """The decode gate_up GEMM (t=4, 70B shapes) writes, for every token, the exact
+    act(G) * U rounded to bf16, up to flips at rounding midpoints."""
+    d = mlp70b
+    t = 4
+    fs = F // t
+    wgu, _ = _shards(d, t)
+    x = d["x"][:n].contiguous()
+    hs = tp.tp_linear_col(x, wgu, act="silu")
+    torch.cuda.synchronize()
+    xs, hst = f64(x), d["host"]
+    for r in range(t):
+        blk = O.merged_column_shard([hst["wg"], hst["wu"]], t, r)
+        h_flip_check(f64(hs[r]), O.glu(O.linear(xs, blk[:fs]), O.linear(xs, blk[fs:]), "silu"))
 
 
 @pytest.mark.parametrize("n", [200, 256, 300])
@@ -123,8 +138,122 @@ def test_mid_size_all_rows(mlp70b, n):
     torch.cuda.synchronize()
     assert tp.tp_device_status() == 0
     rows = [0, 127, 128, n - 1]
-    ref, extra = _reference(f64(x[rows]), d["host"], t, partial_bf16=False)
-    gemm_gate(f64(y[rows]), ref, bf16_out=False, extra=extra)
+    _check(f64(y[rows]), f64(x[rows]), d, t)
+
+
+# ------------------------------------------- integer-exact at the bench's shapes
+
+# rows at both sides of every 256-row pair tile (the raster bands of the bench's
+# GEMMs hold 16 or 18 such tiles, so their edges are among these), plus the ends
+TILE_EDGE_ROWS = sorted({0, NTOK - 1} | {e for k in range(1, NTOK // 256) for e in (256 * k - 1, 256 * k)})
+
+
+@pytest.fixture(scope="module")
+def int70b():
+    build()
+    tp.load()
+    d = {"x": synth.int_valued((NTOK, H), -3, 3, 20, device=DEV),
+         "wg": synth.int_valued((F, H), -3, 3, 21, device=DEV),
+         "wu": synth.int_valued((F, H), -3, 3, 22, device=DEV),
+         "wd": synth.int_valued((H, F), -3, 3, 23, device=DEV),
+         "h": synth.int_valued((NTOK, F), -3, 3, 24, device=DEV),     # stands in for the activation H
+         "bias": synth.int_valued((H,), -8, 8, 25, device=DEV)}
+    yield d
+    d.clear()
+    torch.cuda.empty_cache()
+
+
+def _ring_fold_bf16(pf, t, row_ids, count):
+    """Ring fold of sampled rows with every hop rounded to bf16: each element is
+    folded in the order of its chunk of the full [NTOK, H] buffer."""
+    cs = (count + t - 1) // t
+    flat = np.asarray(row_ids, np.int64)[:, None] * H + np.arange(H, dtype=np.int64)[None, :]
+    chunk = flat // cs
+    out = np.empty(flat.shape)
+    for c in np.unique(chunk):
+        m = chunk == c
+        order = O.ring_fold_order(t, int(c))
+        acc = pf[order[0]][m]
+        for r in order[1:]:
+            acc = O.round_to_bf16(acc + pf[r][m])
+        out[m] = acc
+    return out
+
+
+@pytest.mark.parametrize("t", [4, 8])
+def test_bench_gemms_integer_exact(int70b, t):
+    """The bench's GEMM launches at full size with integer-valued (-3..3) inputs,
+    whose every sum is an integer below 2^24 and so exact in fp32 whatever the
+    order: the column GEMM over the merged gate_up blocks (K = 8192; |acc| <=
+    73728), the row GEMM of each shard into bf16 partials through strided views
+    of one [n, f] activation buffer (K = f/t; |P| <= 64512, rounded once to
+    bf16 ties-to-even), their rank-order reduce, the ring reduce with bf16
+    hops, and the fused down GEMM + reduce with the bias (|Y| <= 258048 + 8).
+    Every output row listed in TILE_EDGE_ROWS is compared bit for bit."""
+    d = int70b
+    fs = F // t
+    rows = TILE_EDGE_ROWS
+    wgu = [torch.cat([d["wg"][r * fs:(r + 1) * fs], d["wu"][r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds = [d["wd"][:, r * fs:(r + 1) * fs].contiguous() for r in range(t)]
+    hs = [d["h"][:, r * fs:(r + 1) * fs] for r in range(t)]
+    xs = f64(d["x"][rows])
+    # column GEMM, fp32 out
+    ys = tp.tp_linear_col(d["x"], wgu, act="none", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for r in range(t):
+        exact(f64(ys[r][rows]), O.linear(xs, f64(wgu[r])))
+    del ys
+    # row GEMM into bf16 partials, then the direct and ring (bf16 hops) reduces
+    parts = tp.tp_linear_row(hs, wds, bias=d["bias"], reduce_results=False, partial_dtype=torch.bfloat16)
+    y_direct = tp.tp_shard_reduce(parts, mode="direct")
+    y_ring = tp.tp_shard_reduce(parts, mode="ring", hop_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    hrows = [f64(h[rows]) for h in hs]
+    bias = f64(d["bias"])
+    p_exact = [O.linear(hrows[r], f64(wds[r]), bias if r == 0 else None) for r in range(t)]
+    p_bf16 = [O.round_to_bf16(p) for p in p_exact]
+    for r in range(t):
+        exact(f64(parts[r][rows]), p_bf16[r])
+    exact(f64(y_direct[rows]), O.round_to_bf16(O.reduce_direct(p_bf16)))
+    exact(f64(y_ring[rows]), _ring_fold_bf16(p_bf16, t, rows, NTOK * H))
+    del parts, y_direct, y_ring
+    # fused down GEMM + reduce (one accumulator over all t shards), fp32 out
+    y_fused = tp.tp_linear_row(hs, wds, bias=d["bias"], mode="fused", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    exact(f64(y_fused[rows]), O.reduce_direct(p_exact))
+    # the same with scratch for the stream-K tail (the last partial wave's tiles split along K)
+    scratch = torch.empty((NTOK, H), dtype=torch.bfloat16, device=DEV)
+    y_sk = tp.tp_linear_row(hs, wds, bias=d["bias"], mode="fused", y_dtype=torch.float32, partials=[scratch] * t)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    exact(f64(y_sk[rows]), O.reduce_direct(p_exact))
+    assert torch.equal(y_sk, y_fused)
+
+
+@pytest.mark.parametrize("t,n", [(4, 768), (4, 1280), (8, 768), (2, 1000)])
+def test_fused_stream_k_tail_integer_exact(int70b, t, n):
+    """The fused down GEMM + reduce at sizes whose last wave of 256 x 256 tiles is
+    short (3 or 5 row tiles by 32 column tiles; a ragged 1000 rows), given scratch:
+    the tail tiles are split along K over the idle CTA pairs, the later parts park
+    fp32 partials in the scratch and the first part adds them.  Integer inputs keep
+    every sum exact, so the result must equal the oracle's in every row, with and
+    without the split."""
+    d = int70b
+    fs = F // t
+    wds = [d["wd"][:, r * fs:(r + 1) * fs].contiguous() for r in range(t)]
+    hs = [d["h"][:n, r * fs:(r + 1) * fs] for r in range(t)]
+    # a partial buffer with a wide row stride, so that it holds the 32 MiB + 4 KiB the split needs
+    scratch = torch.full((n, 2 * H), float("nan"), dtype=torch.float32, device=DEV)[:, :H]
+    y_sk = tp.tp_linear_row(hs, wds, bias=d["bias"], mode="fused", y_dtype=torch.float32, partials=[scratch] * t)
+    y_plain = tp.tp_linear_row(hs, wds, bias=d["bias"], mode="fused", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    assert torch.equal(y_sk, y_plain)
+    rows = sorted({0, 255, 256, n // 2, n - 257, n - 256, n - 1})
+    bias = f64(d["bias"])
+    ref = O.reduce_direct([O.linear(f64(hs[r][rows]), f64(wds[r]), bias if r == 0 else None) for r in range(t)])
+    exact(f64(y_sk[rows]), ref)
 
 
 @pytest.mark.parametrize("t", [2, 4, 8])

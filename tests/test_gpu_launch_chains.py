@@ -17,7 +17,7 @@ from megatron_tensor_layers_gb300 import _lib as tp
 from megatron_tensor_layers_gb300 import synth
 from megatron_tensor_layers_gb300.build import build
 
-from gpu_helpers import f64, gemm_gate, mlp_rounding_allowance
+from gpu_helpers import f64, mlp_check
 
 pytestmark = pytest.mark.gpu
 
@@ -95,9 +95,7 @@ def test_mlp_back_to_back_calls_share_workspace(mode):
     assert tp.tp_device_status() == 0
     wgf, wuf, wdf = f64(wg), f64(wu), f64(wd)
     for xi, yi in zip(xs, ys):
-        xf = f64(xi)
-        ref = O.mlp_unsharded(xf, wgf, wuf, wdf, None, "silu")
-        gemm_gate(f64(yi), ref, bf16_out=False, extra=mlp_rounding_allowance(xf, wgf, wuf, wdf, t, "silu", False))
+        mlp_check(f64(yi), f64(xi), wgf, wuf, wdf, t, mode=mode)
         alone = tp.tp_mlp_forward(xi, wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
         torch.cuda.synchronize()
         _same_bits(yi, alone)
