@@ -44,9 +44,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # taken for the current kernel.
 TRAFFIC_GLU_FULL = 8152473088 + 467175680
 TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the CTA-pair gate_up "
-                "GEMM at the bench size (1-pass capture, profiles/tp_gemm_pair_traffic_t4_n8192.md); "
-                "5.6x the algorithmic bytes: weights streamed once per 64 MB raster band of X rows, "
-                "band rows re-read from DRAM between waves")
+                "GEMM at the bench size (1-pass capture); 5.6x the algorithmic bytes: weights streamed once "
+                "per 64 MB raster band of X rows, band rows re-read from DRAM between waves")
 
 
 def load_peaks():
@@ -62,22 +61,35 @@ def load_peaks():
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    """nvidia-smi sampling of SM clocks and throttle reasons while running.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Every sample carries nvidia-smi's timestamp; ``mark_start`` / ``mark_end``
+    record the host clock around the timed region, and the summary describes
+    only the samples that fall inside it (with how many there were)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.out = None
+        self.t0 = None
+        self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __enter__(self):
         try:
             self.out = open(os.path.join("/tmp", f"tp_bench_clocks_{os.getpid()}.csv"), "w+")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -100,31 +112,42 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
-        if self.proc is None or self.out is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    def _rows(self):
+        from datetime import datetime
         self.out.flush()
         self.out.seek(0)
-        sm, smax, reasons, power = [], [], set(), []
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.out.read().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smax, power = float(parts[2]), float(parts[3]), float(parts[4])
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [s for s, p in zip(sm, power) if p > 300.0] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power)}
+            active = {nm for nm, v in zip(names, parts[6:10]) if v.lower().startswith("active")}
+            rows.append((ts, sm, smax, power, active))
+        return rows
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = self._rows()
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        sm = [r[1] for r in use]
+        reasons = sorted(set().union(*(r[4] for r in use)))
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[2] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_in_timed_region": len(inside),
+                "sample_period_ms": self.PERIOD_MS,
+                "power_cap_samples_in_timed_region": sum(1 for r in inside if "sw_power_cap" in r[4]),
+                "power_w_max": max(r[3] for r in use),
+                "basis": ("samples inside the timed region" if inside else
+                          "no sample fell inside the timed region: all samples of the run")}
 
 
 # ------------------------------------------------------------------ ours
@@ -224,11 +247,13 @@ def run_ours(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
+        clocks.mark_start()
         t_start.record(stream)
         for i in range(args.steps):
             step(evs[i])
         t_end.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
         if dist is not None:
             dist.barrier()
     elapsed = t_start.elapsed_time(t_end) / 1e3
@@ -244,16 +269,19 @@ def run_ours(args, rank, world, local_rank):
 
     col_flops = 4.0 * N_TOK * H * F
     red_bytes = (T + 1) * N_TOK * H * 2
-    # The denominator follows the regime the step ran in: a timed region that
-    # ran into the power cap (or lasts seconds) is compared with the sustained
-    # GEMM peak, which was measured under the same cap; a short region that
-    # stayed at boost clock is compared with the burst peak.
+    # The denominator follows the regime the step ran in, as the clock samples
+    # taken inside the timed region show it: a region in which some sample saw
+    # the power cap is compared with the sustained GEMM peak, which was measured
+    # under the same cap; otherwise (no cap seen, or no sample inside a region
+    # shorter than the sampling period) with the higher burst peak.
     clk = clocks.summary()
-    capped = "sw_power_cap" in clk.get("reasons", [])
-    long_region = capped or elapsed >= 2.0
-    tpeak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
-    tkind = (f"bf16 {'sustained' if long_region else 'burst'} ({peak_src}; "
-             f"{'power-capped' if capped else 'no power cap'} in the timed region)")
+    capped = clk.get("power_cap_samples_in_timed_region", 0) > 0
+    tpeak = peaks["bf16_tflops_sustained"] if capped else peaks["bf16_tflops"]
+    n_in = clk.get("samples_in_timed_region", 0)
+    seen = (f"power cap seen in {clk.get('power_cap_samples_in_timed_region', 0)} of {n_in} clock samples inside the "
+            f"{elapsed:.2f} s timed region" if n_in else
+            f"no clock sample inside the {elapsed:.2f} s timed region (period {ClockSampler.PERIOD_MS} ms)")
+    tkind = f"bf16 {'sustained' if capped else 'burst'} ({peak_src}; {seen})"
     roofline = {"bound": "tensor", "kernel": "tp_gemm_pair_kernel<6,GLU> (gate_up column GEMM + SiLU*up, CTA pairs)",
                 "achieved": col_flops / col_t / 1e12, "peak": tpeak, "unit": "TFLOP/s",
                 "frac": col_flops / col_t / 1e12 / tpeak, "peak_kind": tkind,
@@ -321,7 +349,8 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
-DETAIL_ROWS = ("prefill", "decode", "prefill_t8", "reduce_sweep", "seqpar", "embed", "lm_head", "tiny", "attn")
+DETAIL_ROWS = ("prefill", "decode", "prefill_t8", "reduce_sweep", "seqpar", "embed", "lm_head", "tiny", "attn",
+               "host")
 
 
 def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
@@ -348,6 +377,53 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
         out.update(_detail_tiny(torch, tp, synth, dev))
     if "attn" in rows:
         out.update(_detail_attn(torch, tp, synth, dev, hbm, ten))
+    if "host" in rows:
+        out["host_overhead"] = _detail_host_overhead(torch, tp, synth, dev)
+    return out
+
+
+def _detail_host_overhead(torch, tp, synth, dev):
+    """Host cost per call of the C-ABI entry points: from C (a probe program
+    with no Python in the loop) and through the Python binding, both timed on
+    the host clock from entry to return, calls enqueued back to back with a
+    stream sync every 16 calls so none blocks on the device."""
+    out = {}
+    try:
+        from megatron_tensor_layers_gb300.build import build_abi_overhead
+        exe = build_abi_overhead()
+        r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+        out["c_abi"] = json.loads(r.stdout) if r.returncode == 0 else {"error": (r.stdout + r.stderr)[-300:]}
+    except Exception as e:  # the probe is optional: report why it did not run
+        out["c_abi"] = {"error": str(e)[-300:]}
+    t, n, h, f = 2, 8, 1024, 3072
+    x, wgu, wds = make_mlp(torch, synth, t, n, h, f, dev, seed=300)
+    y = torch.empty((n, h), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tp.tp_mlp_workspace_size(t, n, h, f, "direct", torch.bfloat16), dtype=torch.uint8, device=dev)
+    parts = [torch.zeros((8192,), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    red = torch.empty((8192,), dtype=torch.bfloat16, device=dev)
+    hbuf = torch.empty((n, f), dtype=torch.bfloat16, device=dev)
+    hs = [hbuf[:, r * (f // t):(r + 1) * (f // t)] for r in range(t)]
+    calls = {
+        "tp_shard_reduce_t4_n1": lambda: tp.tp_shard_reduce(parts, out=red, mode="direct"),
+        "tp_linear_col_tiny_gated": lambda: tp.tp_linear_col(x, wgu, act="silu", y=hs),
+        "tp_linear_row_tiny_fused": lambda: tp.tp_linear_row(hs, wds, mode="fused", y=y),
+        "tp_mlp_forward_tiny_direct": lambda: tp.tp_mlp_forward(x, wgu, wds, mode="direct", workspace=ws, y=y),
+    }
+    py = {}
+    for name, fn in calls.items():
+        for _ in range(20):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for i in range(200):
+            t0 = time.perf_counter()
+            fn()
+            ts.append((time.perf_counter() - t0) * 1e6)
+            if i % 16 == 15:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        py[name] = {"host_us_median": statistics.median(ts), "host_us_mean": statistics.fmean(ts)}
+    out["python_binding"] = py
     return out
 
 
