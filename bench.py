@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the gate_up GEMM at the bench
 # size, from ncu (dram__bytes_read.sum + dram__bytes_write.sum); None until
 # taken for the current kernel.
-TRAFFIC_GLU_FULL = 8152473088 + 467175680
+TRAFFIC_GLU_FULL = 8332345344 + 467087872
 TRAFFIC_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the CTA-pair gate_up "
                 "GEMM at the bench size (1-pass capture); 5.6x the algorithmic bytes: weights streamed once "
                 "per 64 MB raster band of X rows, band rows re-read from DRAM between waves")
@@ -453,17 +453,21 @@ def _detail_attn(torch, tp, synth, dev, hbm, ten):
         parts = [torch.empty((n, h), dtype=torch.bfloat16, device=dev) for _ in range(t)]
         y = torch.empty((n, h), dtype=torch.bfloat16, device=dev)
 
-        def proj(c):
+        def proj(c, mode="direct"):
             def run():
                 tp.tp_linear_col(x, c[0], y=qkv)
-                tp.tp_linear_row(attn, c[1], partials=parts, y=y)
+                if mode == "fused":
+                    tp.tp_linear_row(attn, c[1], mode="fused", y=y)
+                else:
+                    tp.tp_linear_row(attn, c[1], partials=parts, y=y)
             return run
 
         if n < 8192:
-            gs = graph_time_cold(torch, [proj(c) for c in copies], 5)
-            if gs:
-                out[f"attn_proj_t8_n{n}"] = {"graph_us": gs * 1e6, "weight_GBps": wbytes / gs / 1e9,
-                                             "graph_hbm_frac": wbytes / gs / 1e9 / hbm}
+            for mode, tag in (("direct", ""), ("fused", "_fused")):
+                gs = graph_time_cold(torch, [proj(c, mode) for c in copies], 5)
+                if gs:
+                    out[f"attn_proj_t8_n{n}{tag}"] = {"graph_us": gs * 1e6, "weight_GBps": wbytes / gs / 1e9,
+                                                      "graph_hbm_frac": wbytes / gs / 1e9 / hbm}
         else:
             s = time_fn(torch, proj(copies[0]), 10)
             fl = 2.0 * n * h * (t * (qh + 2 * hd)) + 2.0 * n * h * (nh * hd)
@@ -474,20 +478,43 @@ def _detail_attn(torch, tp, synth, dev, hbm, ten):
     return out
 
 
-def _detail_prefill(torch, tp, dev, ten, wgu4, wds4, x, y):
-    out = {}
-    ws_f = torch.empty(tp.tp_mlp_workspace_size(T, N_TOK, H, F, "fused", torch.bfloat16), dtype=torch.uint8,
-                       device=dev)
-    # The prefill rows below are short bursts (a few launches), so they run nearer boost clock than
-    # the power-capped timed step: they are compared with the burst peak.
-    s = time_fn(torch, lambda: tp.tp_mlp_forward(x, wgu4, wds4, mode="fused", workspace=ws_f, y=y), 5)
-    out["prefill_t4_fused"] = {"ms": s * 1e3, "tflops": FLOPS / s / 1e12, "frac": FLOPS / s / 1e12 / ten}
-    ws_d = torch.empty(tp.tp_mlp_workspace_size(T, N_TOK, H, F, "ring", torch.bfloat16), dtype=torch.uint8,
-                       device=dev)
-    s = time_fn(torch, lambda: tp.tp_mlp_forward(x, wgu4, wds4, mode="ring", workspace=ws_d, y=y), 5)
-    out["prefill_t4_ring"] = {"ms": s * 1e3, "tflops": FLOPS / s / 1e12, "frac": FLOPS / s / 1e12 / ten}
-    del ws_f, ws_d
+def time_modes_interleaved(torch, fns, rounds=6, iters=3):
+    """Median device time (s) per call of each fn in `fns` (name -> fn), timed in
+    alternation (round r times every fn once, `iters` calls each), so that every
+    mode sees the same clock and power state."""
+    for fn in fns.values():
+        fn()
+    torch.cuda.synchronize()
+    times = {k: [] for k in fns}
+    for _ in range(rounds):
+        for k, fn in fns.items():
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(iters):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            times[k].append(a.elapsed_time(b) / 1e3 / iters)
+    return {k: statistics.median(v) for k, v in times.items()}
+
+
+def _prefill_modes(torch, tp, dev, ten, t, x, wgu, wds, y):
+    """tp_mlp_forward at n=8192 in direct (separate reduce), fused (down GEMM + reduce in one
+    accumulator) and ring order, timed in alternation.  These rows are bursts of a few launches,
+    nearer boost clock than the long timed step, so they are compared with the burst peak."""
+    ws = {m: torch.empty(tp.tp_mlp_workspace_size(t, N_TOK, H, F, m, torch.bfloat16), dtype=torch.uint8, device=dev)
+          for m in ("direct", "fused", "ring")}
+    fns = {m: (lambda m=m: tp.tp_mlp_forward(x, wgu, wds, mode=m, workspace=ws[m], y=y)) for m in ws}
+    med = time_modes_interleaved(torch, fns)
+    out = {f"prefill_t{t}_{m}": {"ms": s * 1e3, "tflops": FLOPS / s / 1e12, "frac": FLOPS / s / 1e12 / ten}
+           for m, s in med.items()}
+    out[f"prefill_t{t}_fused_vs_direct"] = med["direct"] / med["fused"]
+    del ws
     return out
+
+
+def _detail_prefill(torch, tp, dev, ten, wgu4, wds4, x, y):
+    return _prefill_modes(torch, tp, dev, ten, T, x, wgu4, wds4, y)
 
 
 def _detail_decode(torch, tp, dev, hbm, wgu4, wds4, x):
@@ -515,12 +542,7 @@ def _detail_prefill_t8(torch, tp, synth, dev, ten, y):
     """t=8 prefill, separate and fused."""
     out = {}
     x8, wgu8, wds8 = make_mlp(torch, synth, 8, N_TOK, H, F, dev, seed=50)
-    for mode in ("direct", "fused"):
-        ws8 = torch.empty(tp.tp_mlp_workspace_size(8, N_TOK, H, F, mode, torch.bfloat16), dtype=torch.uint8,
-                          device=dev)
-        s = time_fn(torch, lambda: tp.tp_mlp_forward(x8, wgu8, wds8, mode=mode, workspace=ws8, y=y), 5)
-        out[f"prefill_t8_{mode}"] = {"ms": s * 1e3, "tflops": FLOPS / s / 1e12, "frac": FLOPS / s / 1e12 / ten}
-        del ws8
+    out.update(_prefill_modes(torch, tp, dev, ten, 8, x8, wgu8, wds8, y))
     del x8, wgu8, wds8
     torch.cuda.empty_cache()
     return out
@@ -646,6 +668,16 @@ def _detail_vocab(torch, tp, synth, dev, hbm, ten, rows):
             gw = graph_time(torch, lambda: tp.vocab_parallel_embed(idv, shards, V, out=e), 100 if m == nt else 20)
             if gw:
                 rec["graph_us_l2_warm"] = gw * 1e6
+            if m == nt:
+                # The floor for a lookup this small: one launch of a contiguous copy of the same
+                # bytes (the rows' 8 MB read, 8 MB written), cold L2, timed the same way.  A lookup
+                # adds the dependent id load before its row loads.
+                srcs = [torch.empty((m, hh), dtype=torch.bfloat16, device=dev) for _ in range(sets)]
+                dsts = [torch.empty((m, hh), dtype=torch.bfloat16, device=dev) for _ in range(sets)]
+                cs = graph_time_cold(torch, [(lambda j: (lambda: dsts[j].copy_(srcs[j])))(j) for j in range(sets)], 4)
+                if cs:
+                    rec["copy_same_bytes_graph_us"] = cs * 1e6
+                del srcs, dsts
             del idss, outs, fns
             out[f"embed_t{t}{tag}"] = rec
         if "lm_head" not in rows:
