@@ -1,0 +1,76 @@
+"""One small case per kernel, for single-kernel profiler captures.
+
+    python -m megatron_tensor_layers_gb300.profile_cases <case>
+
+Each case runs the kernel it names twice on seeded synthetic inputs larger
+than the L2 but of a few GB at most, so that a capture of one launch
+(``-s 1 -c 1``) sees cold data and ends in seconds.  Cases: reduce, embed,
+gather, seqpar, decode (70B MLP, t=4, 16 tokens, direct then fused, twice),
+pair2048 (prefill MLP, 2048 tokens: the CTA-pair gate_up and down GEMMs),
+fused768 (fused down GEMM + reduce of 768 rows given scratch: its last wave
+split along K).
+"""
+
+import sys
+
+import torch
+
+from . import _lib as tp
+from . import synth
+from .build import build
+
+H, F = 8192, 28672
+
+
+def run(mode: str, dev: str = "cuda") -> None:
+    if mode == "reduce":                      # t=4, 2048 tokens: 4 x 32 MiB bf16 -> 32 MiB
+        parts = [torch.randn(2048 * H, device=dev).to(torch.bfloat16) for _ in range(4)]
+        out = torch.empty(2048 * H, dtype=torch.bfloat16, device=dev)
+        for _ in range(2): tp.tp_shard_reduce(parts, out=out)
+    elif mode == "embed":                     # 65536 ids, t=2, V=151936, h=1024 (269 MB moved)
+        V = 151936
+        table = synth.normal_bf16((V, 1024), 0.02, 6, device=dev)
+        shards = [table[:V // 2].contiguous(), table[V // 2:].contiguous()]
+        ids = synth.uniform_ids(65536, V, 5, device=dev)
+        for _ in range(2): tp.vocab_parallel_embed(ids, shards, V)
+    elif mode == "gather":                    # logits all-gather, t=2, 1024 rows of V=151936
+        V = 151936
+        sh = [synth.normal_bf16((1024, V // 2), 1.0, 3 + r, device=dev) for r in range(2)]
+        out = torch.empty((1024, V), dtype=torch.bfloat16, device=dev)
+        for _ in range(2): tp.tp_shard_gather(sh, out=out)
+    elif mode == "seqpar":                    # t=4, 2048 tokens
+        parts = [torch.randn((2048, H), device=dev).to(torch.bfloat16) for _ in range(4)]
+        resid = torch.randn((2048, H), device=dev).to(torch.bfloat16)
+        w = torch.randn((H,), device=dev).to(torch.bfloat16)
+        for _ in range(2): tp.tp_reduce_scatter_rmsnorm(parts, w, residual=resid, residual_out=resid)
+    elif mode == "decode":                    # 70B MLP decode, t=4, n=16: direct, then fused
+        t = 4; fs = F // t
+        x = synth.normal_bf16((16, H), 1.0, 0, device=dev)
+        wgu = [synth.normal_bf16((2 * fs, H), 0.02, 10 + r, device=dev) for r in range(t)]
+        wds = [synth.normal_bf16((H, fs), 0.02, 20 + r, device=dev) for r in range(t)]
+        for m in ("direct", "fused", "direct", "fused"):
+            tp.tp_mlp_forward(x, wgu, wds, mode=m, partial_dtype=torch.bfloat16)
+    elif mode == "pair2048":                  # prefill n=2048, t=4: gate_up + down (CTA pairs)
+        t = 4; fs = F // t
+        x = synth.normal_bf16((2048, H), 1.0, 0, device=dev)
+        wgu = [synth.normal_bf16((2 * fs, H), 0.02, 10 + r, device=dev) for r in range(t)]
+        wds = [synth.normal_bf16((H, fs), 0.02, 20 + r, device=dev) for r in range(t)]
+        for _ in range(2): tp.tp_mlp_forward(x, wgu, wds, mode="direct")
+    elif mode == "fused768":                  # fused down + reduce, 768 rows: its last wave split along K
+        t = 4; fs = F // t
+        hs = [synth.normal_bf16((768, fs), 1.0, 30 + r, device=dev) for r in range(t)]
+        wds = [synth.normal_bf16((H, fs), 0.02, 20 + r, device=dev) for r in range(t)]
+        scratch = torch.empty((768, 2 * H), dtype=torch.float32, device=dev)[:, :H]
+        for _ in range(2): tp.tp_linear_row(hs, wds, mode="fused", y_dtype=torch.float32, partials=[scratch] * t)
+    else:
+        raise ValueError(f"unknown case {mode}")
+    torch.cuda.synchronize()
+    if tp.tp_device_status() != 0:
+        raise RuntimeError("device status error")
+    print("ok", mode)
+
+
+if __name__ == "__main__":
+    build()
+    tp.load()
+    run(sys.argv[1])
