@@ -167,3 +167,20 @@ def test_gemm_kernel_choice(lib):
     for n in (1, 8, 64):
         assert plan(n, 640, h, groups=8, gated=True)[1] != 96
     assert lib.tp_debug_gemm_plan(0, 1, 1, 1, 1, 0, 152, None, None, None) == 1
+
+
+def test_mlp_workspace_sizes(lib):
+    """tp_mlp_workspace_size: H [n, f] bf16, plus t partials [n, h] unless the reduce
+    is fused, each 256-byte aligned; a fused reduce of more than 128 rows adds the
+    32 MiB + 4 KiB stream-K area of its down GEMM (optional: tp_mlp_forward also runs
+    with the H bytes alone)."""
+    al = lambda b: (b + 255) // 256 * 256
+    ws = lambda t, n, h, f, mode, pdt: lib.tp_mlp_workspace_size(t, n, h, f, _lib.MODES[mode], pdt)
+    tail = 4096 + 128 * 256 * 256 * 4
+    t, h, f = 4, 8192, 28672
+    for n in (1, 64, 128, 129, 8192):
+        hb = al(n * f * 2)
+        assert ws(t, n, h, f, "direct", 0) == hb + t * al(n * h * 2)
+        assert ws(t, n, h, f, "ring", 1) == hb + t * al(n * h * 4)
+        assert ws(t, n, h, f, "fused", 0) == hb + (tail if n > 128 else 0)
+    assert ws(0, 8, h, f, "direct", 0) == 0 and ws(4, -1, h, f, "direct", 0) == 0

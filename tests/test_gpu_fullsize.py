@@ -231,6 +231,48 @@ def test_bench_gemms_integer_exact(int70b, t):
     assert torch.equal(y_sk, y_fused)
 
 
+def test_fused_stream_k_tail_bf16_out_and_graph_replay(int70b):
+    """The stream-K tail through tp_mlp_forward's own workspace (flags zeroed by the
+    call, ahead of its gate_up GEMM), with a bias and a bf16 output: captured once in a
+    CUDA graph and replayed on new inputs, every replay gives the eager call's bits,
+    and the graph with the minimal workspace (no tail split) stays within the MLP gates."""
+    d = int70b
+    t, n = 4, 768
+    fs = F // t
+    wgu = [torch.cat([d["wg"][r * fs:(r + 1) * fs], d["wu"][r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds = [d["wd"][:, r * fs:(r + 1) * fs].contiguous() for r in range(t)]
+    bias = synth.normal_bf16((H,), 1.0, 26, device=DEV)
+    x = torch.empty((n, H), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(tp.tp_mlp_workspace_size(t, n, H, F, "fused", torch.bfloat16), dtype=torch.uint8, device=DEV)
+    y = torch.empty((n, H), dtype=torch.bfloat16, device=DEV)
+    x.copy_(synth.normal_bf16((n, H), 1.0, 27, device=DEV))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tp.tp_mlp_forward(x, wgu, wds, bias_down=bias, mode="fused", workspace=ws, y=y)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tp.tp_mlp_forward(x, wgu, wds, bias_down=bias, mode="fused", workspace=ws, y=y)
+    for seed in (28, 29, 30):
+        x.copy_(synth.normal_bf16((n, H), 1.0, seed, device=DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        from_graph = y.clone()
+        eager = tp.tp_mlp_forward(x, wgu, wds, bias_down=bias, mode="fused")
+        torch.cuda.synchronize()
+        assert tp.tp_device_status() == 0
+        assert torch.equal(from_graph, eager)
+    rows = [0, 255, 256, 511, 512, n - 1]
+    small_ws = torch.empty(n * F * 2, dtype=torch.uint8, device=DEV)            # H only: no tail split
+    y_small = tp.tp_mlp_forward(x, wgu, wds, bias_down=bias, mode="fused", workspace=small_ws, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    wg, wu, wd = f64(d["wg"]), f64(d["wu"]), f64(d["wd"])
+    for got, y_bf16 in ((f64(from_graph[rows]), True), (f64(y_small[rows]), False)):
+        mlp_check(got, f64(x[rows]), wg, wu, wd, t, bias=f64(bias), mode="fused", y_bf16=y_bf16)
+
+
 @pytest.mark.parametrize("t,n", [(4, 768), (4, 1280), (8, 768), (2, 1000)])
 def test_fused_stream_k_tail_integer_exact(int70b, t, n):
     """The fused down GEMM + reduce at sizes whose last wave of 256 x 256 tiles is
