@@ -146,3 +146,55 @@ def test_split_k_cluster_outputs_stay_inside(ydt):
     assert tp.tp_device_status() == 0
     for o in [yf] + hg + parts:
         assert intact(o[1], o[2], o[3])
+
+
+@pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
+def test_fused_stream_k_tail_stays_inside(ydt):
+    """The fused down GEMM + reduce whose last wave is split along K (768 rows: 3 row
+    tiles by 32 column tiles of 256): the output is a strided view with canaries, and
+    the scratch the call borrows (partials[0]) sits inside a canary-filled buffer with
+    rows of padding.  The kernel writes the output and, inside the scratch, only the
+    flags and the partial slots: every canary outside both survives."""
+    t, n, h, fs = 4, 768, 8192, 1024
+    hs = [ints((n, fs), 40 + r) for r in range(t)]
+    wds = [ints((h, fs), 50 + r) for r in range(t)]
+    y, ybuf, ymask, ycan = guarded(n, h, ydt)
+    # scratch: n rows of 2h fp32 (>= 32 MiB + 4 KiB) as the first h columns of each row,
+    # so the row padding and the band after the end are canaries
+    s, sbuf, smask, scan = guarded(n, h, torch.float32, pad_cols=h, pad_rows=3)
+    tp.tp_linear_row(hs, wds, mode="fused", y=y, y_dtype=ydt, partials=[s] * t)
+    plain = tp.tp_linear_row(hs, wds, mode="fused", y_dtype=ydt)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    assert intact(ybuf, ymask, ycan)
+    assert torch.equal(y, plain)                 # integer inputs: exact with or without the split
+    # the scratch's writes stay in its first 32 MiB + 4 KiB, which the caller's n * ldp elements cover
+    used = (4096 + 128 * 256 * 256 * 4) // 4
+    assert used <= n * 2 * h
+    assert bool(torch.all(sbuf[n * 2 * h:] == scan).item())
+
+
+def test_fused_stream_k_on_two_streams():
+    """Two fused MLP calls with the stream-K tail on two streams at once, each with its
+    own workspace (flags and slots): each result equals the same call made alone."""
+    t, n, h, f = 4, 768, 8192, 28672
+    fs = f // t
+    wgu = [synth.normal_bf16((2 * fs, h), 0.02, 60 + r, device=DEV) for r in range(t)]
+    wds = [synth.normal_bf16((h, fs), 0.02, 70 + r, device=DEV) for r in range(t)]
+    xs = [synth.normal_bf16((n, h), 1.0, 80 + i, device=DEV) for i in range(2)]
+    alone = [tp.tp_mlp_forward(x, wgu, wds, mode="fused") for x in xs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    wss = [torch.empty(tp.tp_mlp_workspace_size(t, n, h, f, "fused", torch.bfloat16), dtype=torch.uint8, device=DEV)
+           for _ in range(2)]
+    ys = [torch.empty((n, h), dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    for _ in range(3):
+        for i in range(2):
+            streams[i].wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(streams[i]):
+                tp.tp_mlp_forward(xs[i], wgu, wds, mode="fused", workspace=wss[i], y=ys[i],
+                                  stream=streams[i])
+        torch.cuda.synchronize()
+        assert tp.tp_device_status() == 0
+        for i in range(2):
+            assert torch.equal(ys[i], alone[i])
