@@ -117,7 +117,9 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 # Host arrays of per-shard device pointers.  The C ABI reads them during the
 # call only, so each thread reuses a small ring of arrays instead of building
-# new ctypes objects on every call (a call passes at most three lists).
+# new ctypes objects on every call (a call passes at most three lists).  An
+# array returned by _ptrs is therefore valid only until this thread's next
+# _PTR_RING calls of _ptrs: pass it straight to the C function.
 _PTR_RING = 8
 _tls = threading.local()
 
