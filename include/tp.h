@@ -139,10 +139,10 @@ tp_status tp_linear_col(int t, int64_t n, int64_t in, int64_t out_full,
  *          sum.  DIRECT/RING write the partials first, then reduce them
  *          (RING hops round to partial_dtype); FUSED writes no partial
  *          (partials may be NULL).  A FUSED call of more than 128 rows that
- *          is given partials[0] (n * ldp elements of partial_dtype, at least
- *          32 MiB + 4 KiB) uses that buffer as scratch in which the last,
- *          partial wave of output tiles is split along K (stream-K); its
- *          contents are overwritten.
+ *          is given a contiguous partials[0] (ldp == out; n * out elements
+ *          of partial_dtype, at least 32 MiB + 4 KiB) uses that buffer as
+ *          scratch in which the last, partial wave of output tiles is split
+ *          along K (stream-K); its contents are overwritten.
  *   partials[r] [n, out] in partial_dtype, row stride ldp (caller-owned
  *          scratch; contents are overwritten).
  * Requires in_full % t == 0 and (in_full/t) % 8 == 0.

@@ -261,12 +261,16 @@ static tp_status linear_row_impl(int t, int64_t n, int64_t in_full, int64_t out,
         d.bias[0] = bias;
         d.ldo = ldy;
         d.out_f32 = y_dtype == TP_F32;
-        if (sk_ws == nullptr && partials != nullptr && partials[0] != nullptr && n > 128 && dtype_ok(partial_dtype) &&
-            ldp >= out && al16(partials[0]) &&
-            static_cast<size_t>(n) * static_cast<size_t>(ldp) * esize(partial_dtype) >= tpk::kSkWorkspaceBytes) {
-            // a caller's partial buffer, unused by a fused reduce, holds the stream-K tail area
+        // A caller's partial buffer, unused by a fused reduce, may hold the stream-K tail area when
+        // its rows are contiguous (ldp == out): then its n * out elements are all the caller's, with
+        // no padding between rows that could belong to other data.
+        const size_t p0_bytes = (ldp == out && dtype_ok(partial_dtype))
+                                    ? static_cast<size_t>(n) * static_cast<size_t>(out) * esize(partial_dtype)
+                                    : 0;
+        if (sk_ws == nullptr && partials != nullptr && partials[0] != nullptr && n > 128 && al16(partials[0]) &&
+            p0_bytes >= tpk::kSkWorkspaceBytes) {
             sk_ws = partials[0];
-            sk_bytes = static_cast<size_t>(n) * static_cast<size_t>(ldp) * esize(partial_dtype);
+            sk_bytes = p0_bytes;
             if (cudaMemsetAsync(sk_ws, 0, tpk::kSkFlagBytes, cs(stream)) != cudaSuccess) return TP_ERR_CUDA;
         }
         d.sk_ws = sk_ws;

@@ -7,7 +7,7 @@ than the L2 but of a few GB at most, so that a capture of one launch
 (``-s 1 -c 1``) sees cold data and ends in seconds.  Cases: reduce, embed,
 gather, seqpar, decode (70B MLP, t=4, 16 tokens, direct then fused, twice),
 pair2048 (prefill MLP, 2048 tokens: the CTA-pair gate_up and down GEMMs),
-fused768 (fused down GEMM + reduce of 768 rows given scratch: its last wave
+fused1280 (fused down GEMM + reduce of 1280 rows given scratch: its last wave
 split along K).
 """
 
@@ -56,11 +56,11 @@ def run(mode: str, dev: str = "cuda") -> None:
         wgu = [synth.normal_bf16((2 * fs, H), 0.02, 10 + r, device=dev) for r in range(t)]
         wds = [synth.normal_bf16((H, fs), 0.02, 20 + r, device=dev) for r in range(t)]
         for _ in range(2): tp.tp_mlp_forward(x, wgu, wds, mode="direct")
-    elif mode == "fused768":                  # fused down + reduce, 768 rows: its last wave split along K
+    elif mode == "fused1280":                 # fused down + reduce, 1280 rows: its last wave split along K
         t = 4; fs = F // t
-        hs = [synth.normal_bf16((768, fs), 1.0, 30 + r, device=dev) for r in range(t)]
+        hs = [synth.normal_bf16((1280, fs), 1.0, 30 + r, device=dev) for r in range(t)]
         wds = [synth.normal_bf16((H, fs), 0.02, 20 + r, device=dev) for r in range(t)]
-        scratch = torch.empty((768, 2 * H), dtype=torch.float32, device=dev)[:, :H]
+        scratch = torch.empty((1280, H), dtype=torch.float32, device=dev)      # contiguous: lent as scratch
         for _ in range(2): tp.tp_linear_row(hs, wds, mode="fused", y_dtype=torch.float32, partials=[scratch] * t)
     else:
         raise ValueError(f"unknown case {mode}")

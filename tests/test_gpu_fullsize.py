@@ -273,10 +273,11 @@ def test_fused_stream_k_tail_bf16_out_and_graph_replay(int70b):
         mlp_check(got, f64(x[rows]), wg, wu, wd, t, bias=f64(bias), mode="fused", y_bf16=y_bf16)
 
 
-@pytest.mark.parametrize("t,n", [(4, 768), (4, 1280), (8, 768), (2, 1000)])
+@pytest.mark.parametrize("t,n", [(4, 1280), (8, 1280), (2, 1100)])
 def test_fused_stream_k_tail_integer_exact(int70b, t, n):
     """The fused down GEMM + reduce at sizes whose last wave of 256 x 256 tiles is
-    short (3 or 5 row tiles by 32 column tiles; a ragged 1000 rows), given scratch:
+    short (5 row tiles by 32 column tiles, the last ragged at 1100 rows), given a
+    contiguous fp32 partial buffer as scratch (n x 8192 x 4 bytes >= 32 MiB + 4 KiB):
     the tail tiles are split along K over the idle CTA pairs, the later parts park
     fp32 partials in the scratch and the first part adds them.  Integer inputs keep
     every sum exact, so the result must equal the oracle's in every row, with and
@@ -285,8 +286,7 @@ def test_fused_stream_k_tail_integer_exact(int70b, t, n):
     fs = F // t
     wds = [d["wd"][:, r * fs:(r + 1) * fs].contiguous() for r in range(t)]
     hs = [d["h"][:n, r * fs:(r + 1) * fs] for r in range(t)]
-    # a partial buffer with a wide row stride, so that it holds the 32 MiB + 4 KiB the split needs
-    scratch = torch.full((n, 2 * H), float("nan"), dtype=torch.float32, device=DEV)[:, :H]
+    scratch = torch.full((n, H), float("nan"), dtype=torch.float32, device=DEV)
     y_sk = tp.tp_linear_row(hs, wds, bias=d["bias"], mode="fused", y_dtype=torch.float32, partials=[scratch] * t)
     y_plain = tp.tp_linear_row(hs, wds, bias=d["bias"], mode="fused", y_dtype=torch.float32)
     torch.cuda.synchronize()
