@@ -150,28 +150,25 @@ def test_split_k_cluster_outputs_stay_inside(ydt):
 
 @pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
 def test_fused_stream_k_tail_stays_inside(ydt):
-    """The fused down GEMM + reduce whose last wave is split along K (768 rows: 3 row
-    tiles by 32 column tiles of 256): the output is a strided view with canaries, and
-    the scratch the call borrows (partials[0]) sits inside a canary-filled buffer with
-    rows of padding.  The kernel writes the output and, inside the scratch, only the
-    flags and the partial slots: every canary outside both survives."""
-    t, n, h, fs = 4, 768, 8192, 1024
+    """The fused down GEMM + reduce whose last wave is split along K (1100 rows: 5 row
+    tiles, the last ragged, by 32 column tiles of 256): the output is a strided view
+    with canaries, and the scratch the call borrows (a contiguous fp32 partials[0])
+    sits inside a canary-filled buffer.  The kernel writes the output and, inside the
+    scratch, only the flags and the partial slots: every canary outside both survives."""
+    t, n, h, fs = 4, 1100, 8192, 1024
     hs = [ints((n, fs), 40 + r) for r in range(t)]
     wds = [ints((h, fs), 50 + r) for r in range(t)]
     y, ybuf, ymask, ycan = guarded(n, h, ydt)
-    # scratch: n rows of 2h fp32 (>= 32 MiB + 4 KiB) as the first h columns of each row,
-    # so the row padding and the band after the end are canaries
-    s, sbuf, smask, scan = guarded(n, h, torch.float32, pad_cols=h, pad_rows=3)
+    s, sbuf, smask, scan = guarded(n, h, torch.float32, pad_cols=0, pad_rows=3)
     tp.tp_linear_row(hs, wds, mode="fused", y=y, y_dtype=ydt, partials=[s] * t)
     plain = tp.tp_linear_row(hs, wds, mode="fused", y_dtype=ydt)
     torch.cuda.synchronize()
     assert tp.tp_device_status() == 0
     assert intact(ybuf, ymask, ycan)
     assert torch.equal(y, plain)                 # integer inputs: exact with or without the split
-    # the scratch's writes stay in its first 32 MiB + 4 KiB, which the caller's n * ldp elements cover
-    used = (4096 + 128 * 256 * 256 * 4) // 4
-    assert used <= n * 2 * h
-    assert bool(torch.all(sbuf[n * 2 * h:] == scan).item())
+    # the scratch's writes stay in its first 32 MiB + 4 KiB, inside the caller's n * h elements
+    assert (4096 + 128 * 256 * 256 * 4) // 4 <= n * h
+    assert intact(sbuf, smask, scan)
 
 
 def test_fused_stream_k_on_two_streams():
@@ -198,3 +195,29 @@ def test_fused_stream_k_on_two_streams():
         assert tp.tp_device_status() == 0
         for i in range(2):
             assert torch.equal(ys[i], alone[i])
+
+
+@pytest.mark.parametrize("tile_n", [64, 96, 128, 256])
+@pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
+def test_few_row_gemm_outputs_stay_inside(tile_n, ydt):
+    """Five rows (the 8-row A tiles with the deepest B rings) at every tile width: the
+    plain, gated and row GEMMs write only inside their outputs."""
+    tp.tp_set_gemm_tile_n(tile_n)
+    try:
+        t, n, k, os_ = 3, 5, 1000, 200
+        x = ints((n, k), 160)
+        w = [ints((os_, k), 161 + r) for r in range(t)]
+        outs = [guarded(n, os_, ydt) for _ in range(t)]
+        tp.tp_linear_col(x, w, y=[o[0] for o in outs], y_dtype=ydt)
+        wgu = [ints((2 * os_, k), 165 + r) for r in range(t)]
+        hg = [guarded(n, os_, ydt) for _ in range(t)]
+        tp.tp_linear_col(x, wgu, act="silu", y=[o[0] for o in hg], y_dtype=ydt)
+        xs = [ints((n, k), 170 + r) for r in range(t)]
+        pg = [guarded(n, os_, torch.float32, pad_cols=0) for _ in range(t)]
+        tp.tp_linear_row(xs, w, reduce_results=False, partials=[o[0] for o in pg], partial_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert tp.tp_device_status() == 0
+        for o in outs + hg + pg:
+            assert intact(o[1], o[2], o[3])
+    finally:
+        tp.tp_set_gemm_tile_n(0)

@@ -468,6 +468,34 @@ def test_every_tile_width_integer_exact(tile_n):
 
 
 @pytest.mark.parametrize("tile_n", [64, 96, 128, 256], indirect=True)
+@pytest.mark.parametrize("n", [1, 5, 8, 9, 64])
+def test_every_tile_width_few_rows(tile_n, n):
+    """Decode-sized GEMMs at every tile width: up to 8 rows take the 8-row A tiles
+    with the deepest B rings (24 stages at width 64), 9 to 64 rows the 64-row A
+    tiles.  K = 2200 (35 blocks, a ragged last one) wraps every ring; the plain and
+    the row GEMMs are integer-exact, the gated GEMM's H is the exact rounding up to
+    flips at midpoints."""
+    t, k, os_ = 3, 2200, 328
+    x = ints((n, k), 130 + n)
+    w = [ints((os_, k), 131 + r) for r in range(t)]
+    y = tp.tp_linear_col(x, w, y_dtype=torch.float32)
+    xs = [ints((n, k), 140 + r) for r in range(t)]
+    ws = [ints((os_, k), 145 + r) for r in range(t)]
+    yd = tp.tp_linear_row(xs, ws, mode="direct", partial_dtype=torch.float32, y_dtype=torch.float32)
+    xg = normal((n, k), 1.0, 150)
+    wgu = [normal((2 * os_, k), 0.02, 151 + r) for r in range(t)]
+    hs = tp.tp_linear_col(xg, wgu, act="silu", y_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    for r in range(t):
+        exact(f64(y[r]), O.linear(f64(x), f64(w[r])))
+    exact(f64(yd), O.reduce_direct([O.linear(f64(xs[r]), f64(ws[r])) for r in range(t)]))
+    for r in range(t):
+        wr = f64(wgu[r])
+        h_flip_check(f64(hs[r]), O.glu(O.linear(f64(xg), wr[:os_]), O.linear(f64(xg), wr[os_:]), "silu"))
+
+
+@pytest.mark.parametrize("tile_n", [64, 96, 128, 256], indirect=True)
 def test_every_tile_width_gated(tile_n):
     t, n, h, fs = 2, 260, 320, 200
     x = normal((n, h), 1.0, 120)
