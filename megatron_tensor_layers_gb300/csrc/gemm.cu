@@ -177,11 +177,13 @@ __device__ __forceinline__ void store_chunk(void* base, int64_t ldo, int out_f32
 }
 
 // AROWS: shared-memory rows of a stage's A tile.  Launches with M <= 64
-// (decode) keep 64 rows and spend the room on a deeper B ring, since their
-// time is the weight stream and the bytes each SM keeps in flight bound it.
-// The M = 128 MMA then also reads the 64 rows that follow the A tile (the
-// same stage's B tile, already landed) as A rows 64-127; those accumulator
-// rows are never stored.
+// (decode) keep 64 rows, and launches with M <= 8 keep 8, and spend the room
+// on a deeper B ring, since their time is the weight stream and the bytes
+// each SM keeps in flight bound it.  The M = 128 MMA then also reads the
+// 16 KB that follow the stage's start as A rows AROWS-127 (the stage's B
+// tile and, for short stages, the start of the next stage); those
+// accumulator rows are never stored.  PAD_BYTES keeps that read window of
+// the last stage inside the allocation.
 //
 // STG_BYTES: the gated decode configurations also keep, per epilogue warp
 // that can hold rows (the first two), a 32-row staging area of one 32-column
@@ -200,13 +202,15 @@ struct GemmCfg {
     static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
     static constexpr int STG_ROW = 65;
     static constexpr int STG_BYTES = (EPI == EPI_GLU && AROWS < BM) ? 2 * 32 * STG_ROW * 4 : 0;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES;
+    static constexpr int MMA_A_BYTES = BM * BK * 2;                    // what the M = 128 MMA reads as A
+    static constexpr int TAIL_BYTES = STAGE_BYTES + STG_BYTES + BAR_BYTES;   // from the last stage's start
+    static constexpr int PAD_BYTES = (AROWS < BM && TAIL_BYTES < MMA_A_BYTES) ? MMA_A_BYTES - TAIL_BYTES : 0;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES + PAD_BYTES;
     static constexpr int OUT_COLS = (EPI == EPI_GLU) ? BN / 2 : BN;   // output columns per tile
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(BN % 32 == 0 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256; epilogue chunks of 32");
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
-    static_assert(AROWS == BM || (AROWS == 64 && B_BYTES >= 64 * BK * 2),
-                  "a 64-row A tile needs at least 64 rows of B behind it in the stage");
+    static_assert(AROWS == BM || AROWS == 64 || AROWS == 8, "A tiles of 128, 64 or 8 rows");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -1749,6 +1753,17 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
         }
         if (plan.bn == 256) return launch_split<256, 4, EPI_STORE>(a, d, cs, stream);
         return launch_split<128, 8, EPI_STORE, 2>(a, d, cs, stream);
+    }
+    if (d.M <= 8) {    // one to eight tokens: 8-row A tiles, deeper B rings still
+        if (glu) {
+            if (best == 256) return launch_cfg<256, 6, EPI_GLU, 8>(a, d, stream);
+            if (best == 128) return launch_cfg<128, 12, EPI_GLU, 8, 2>(a, d, stream);
+            return launch_cfg<64, 20, EPI_GLU, 8, 4>(a, d, stream);
+        }
+        if (best == 256) return launch_cfg<256, 6, EPI_STORE, 8>(a, d, stream);
+        if (best == 128) return launch_cfg<128, 12, EPI_STORE, 8, 2>(a, d, stream);
+        if (best == 96) return launch_cfg<96, 16, EPI_STORE, 8, 2>(a, d, stream);
+        return launch_cfg<64, 24, EPI_STORE, 8, 4>(a, d, stream);
     }
     if (d.M <= 64) {   // decode: 64-row A tiles, deeper B rings
         if (glu) {
