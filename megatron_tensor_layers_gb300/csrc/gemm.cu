@@ -926,10 +926,10 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
 // arrivals on each barrier.  Waits are bounded like every other wait of the
 // library, and a relaxed cluster barrier before exit keeps each CTA's shared
 // memory alive while its peers may still read it.
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int ROWS_ = 64>
 struct SplitCfg {
-    static constexpr int ROWS = 64;                          // staged rows (M <= 64)
-    static constexpr int A_BYTES = ROWS * BK * 2;            // 64-row A tile (see GemmCfg's AROWS)
+    static constexpr int ROWS = ROWS_;                       // staged rows: M <= 64, or M <= 8
+    static constexpr int A_BYTES = ROWS * BK * 2;            // 64- or 8-row A tile (see GemmCfg's AROWS)
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGING_BYTES = ROWS * BN * 4;      // fp32 accumulator rows
@@ -940,6 +940,8 @@ struct SplitCfg {
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static_assert(ROWS == 64 || ROWS == 8, "64 or 8 staged rows");
+    static_assert(STAGE_BYTES >= BM * BK * 2, "the M = 128 MMA reads 16 KB of A from the stage's start");
 };
 
 // Four fp32 accumulator values (float4 column `f4col` of `row`) summed over
@@ -989,9 +991,9 @@ __device__ __forceinline__ void store_quad(void* base, int64_t ldo, int out_f32,
     }
 }
 
-template <int BN, int STAGES, int EPI, int KSUB>
+template <int BN, int STAGES, int EPI, int KSUB, int ROWS>
 __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __grid_constant__ GemmArgs args) {
-    using Cfg = SplitCfg<BN, STAGES, EPI>;
+    using Cfg = SplitCfg<BN, STAGES, EPI, ROWS>;
     static_assert(KSUB >= 1 && STAGES % KSUB == 0, "stage groups of KSUB blocks (as in tp_gemm_kernel)");
     constexpr int GROUPS = STAGES / KSUB;
     extern __shared__ uint8_t smem_raw[];
@@ -1562,9 +1564,9 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
     return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
-template <int BN, int STAGES, int EPI, int KSUB = 1>
+template <int BN, int STAGES, int EPI, int KSUB = 1, int ROWS = 64>
 static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream_t stream) {
-    using Cfg = SplitCfg<BN, STAGES, EPI>;
+    using Cfg = SplitCfg<BN, STAGES, EPI, ROWS>;
     const int kb_all = a.k_blocks * d.segs;
     if (d.M > Cfg::ROWS || cs < 2 || cs > 8 || cs > kb_all) return TP_ERR_UNSUPPORTED;
     a.split = cs;
@@ -1586,7 +1588,7 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
                                          : make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box);
         if (!ok) return TP_ERR_CUDA;
     }
-    auto kern = tp_gemm_splitk_kernel<BN, STAGES, EPI, KSUB>;
+    auto kern = tp_gemm_splitk_kernel<BN, STAGES, EPI, KSUB, ROWS>;
     static std::atomic<uint64_t> smem_set{0};
     if (!smem_attribute_once(reinterpret_cast<const void*>(kern), Cfg::SMEM_BYTES, smem_set)) return TP_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1747,6 +1749,14 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
     }
     if (plan.kind == 2) {
         const int cs = plan.cs;
+        if (d.M <= 8) {   // 8 staged rows: 6 / 12 stages instead of 4 / 8
+            if (glu) {
+                if (plan.bn == 256) return launch_split<256, 6, EPI_GLU, 1, 8>(a, d, cs, stream);
+                return launch_split<128, 12, EPI_GLU, 2, 8>(a, d, cs, stream);
+            }
+            if (plan.bn == 256) return launch_split<256, 6, EPI_STORE, 1, 8>(a, d, cs, stream);
+            return launch_split<128, 12, EPI_STORE, 2, 8>(a, d, cs, stream);
+        }
         if (glu) {
             if (plan.bn == 256) return launch_split<256, 4, EPI_GLU>(a, d, cs, stream);
             return launch_split<128, 8, EPI_GLU, 2>(a, d, cs, stream);
