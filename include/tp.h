@@ -183,6 +183,13 @@ tp_status tp_shard_reduce(int t, int64_t count, tp_dtype dtype, const void* cons
  * reduce of more than 128 token rows it adds 32 MiB + 4 KiB in which the
  * down GEMM splits the tiles of its last, partial wave along K (stream-K):
  * tp_mlp_forward also runs with only the H bytes, then without that split.
+ * For a FUSED reduce of 1 to 8 token rows with h a multiple of 256 up to
+ * 1024, (f/t) % 64 == 0 and f/64 <= 128, it returns instead the larger of
+ * that and f/64 * n * h * 4 bytes (256-byte aligned): with that many bytes
+ * tp_mlp_forward runs both projections in one GEMM kernel whose CTA pairs
+ * each take a 64-column slice of a rank's f columns (H never leaves the
+ * chip), and a second kernel adds the slices' fp32 partials in slice order,
+ * rank 0's slices first; with only the H bytes it runs the two-GEMM path.
  * Returns 0 for invalid arguments.
  */
 size_t tp_mlp_workspace_size(int t, int64_t n, int64_t h, int64_t f,
@@ -202,8 +209,8 @@ size_t tp_mlp_workspace_size(int t, int64_t n, int64_t h, int64_t f,
  *   bias_down    NULL or [h] bf16, added once.
  *   act          TP_ACT_SILU_MUL or TP_ACT_GELU_TANH_MUL.
  *   workspace    device buffer of tp_mlp_workspace_size() bytes (a FUSED
- *                reduce of more than 128 rows also accepts just the n*f*2
- *                bytes of H, see above), 256-byte aligned; overwritten.
+ *                reduce also accepts just the n*f*2 bytes of H, see above),
+ *                256-byte aligned; overwritten.
  *   y            [n, h] of y_dtype, contiguous.
  * Requires f % t == 0, (f/t) % 8 == 0 and h % 8 == 0.
  */

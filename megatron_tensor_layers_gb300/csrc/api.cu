@@ -304,7 +304,8 @@ tp_status tp_linear_row(int t, int64_t n, int64_t in_full, int64_t out, const vo
 
 size_t tp_mlp_workspace_size(int t, int64_t n, int64_t h, int64_t f, tp_reduce_mode mode, tp_dtype partial_dtype) {
     const size_t base = tpk::mlp_workspace_required(t, n, h, f, mode, partial_dtype);
-    return base == 0 ? 0 : base + mlp_tail_bytes(n, mode);
+    if (base == 0) return 0;
+    return std::max(base + mlp_tail_bytes(n, mode), tpk::small_mlp_workspace(t, n, h, f, mode));
 }
 
 tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, int64_t ldx,
@@ -331,6 +332,33 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, 
     TP_CHECK(workspace_bytes >= need, TP_ERR_WORKSPACE);
     TP_CHECK((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, TP_ERR_ALIGNMENT);
     if (n == 0) return TP_OK;
+
+    // One to eight tokens with a fused reduce: one GEMM kernel for both
+    // projections plus the ordered reduce, when the workspace holds the
+    // slices' partials (tp_mlp_workspace_size includes them).
+    const size_t small = tpk::small_mlp_workspace(t, n, h, f, mode);
+    if (small > 0 && workspace_bytes >= small) {
+        tpk::SmallMlpDesc d;
+        d.t = t;
+        d.n = n;
+        d.h = h;
+        d.f = f;
+        d.x = x;
+        d.ldx = ldx;
+        for (int r = 0; r < t; ++r) {
+            d.w_gate_up[r] = w_gate_up[r];
+            d.w_down[r] = w_down[r];
+        }
+        d.ld_down = ld_down;
+        d.bias = bias_down;
+        d.act = act;
+        d.part = static_cast<float*>(workspace);
+        d.y = y;
+        d.y_f32 = y_dtype == TP_F32;
+        d.status = status_ptr();
+        g_collectives++;
+        return tpk::launch_small_mlp(d, cs(stream));
+    }
 
     // Workspace: H [n, f] bf16 (rank r's slice = columns [r*fs, (r+1)*fs)),
     // then t partials [n, h], or, for a fused reduce when the workspace holds

@@ -29,6 +29,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
 }
 
+// Gate activation of the gated MLP epilogues (SiLU or tanh-approximated GELU).
+__device__ __forceinline__ float act_fn(float g, int act) {
+    if (act == TP_ACT_GELU_TANH_MUL) {
+        const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+        return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
+    }
+    // SiLU.  The approximate divide (two special-function ops with the exponential instead of
+    // an IEEE divide's longer sequence) errs by about 2 ulp of fp32, far below the bf16
+    // rounding of the stored H; for g below about -87 the denominator passes 2^126 and the
+    // result is 0, which is also what a bf16 H would hold.
+    return __fdividef(g, 1.0f + __expf(-g));
+}
+
 // ---------------------------------------------------------------- timers
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -188,6 +201,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// 4-D tiled bulk-tensor load (coordinates innermost first), completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
+                                            int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -269,6 +291,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
+}
+
+// Each thread of the warp reads 8 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
@@ -383,6 +413,28 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+// 16-byte store to this CTA's shared memory.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Proxy fence between a thread's ordinary (generic-proxy) stores to its CTA's
+// shared memory and later asynchronous-proxy reads of those bytes (tcgen05.mma
+// operands, bulk copies).
+__device__ __forceinline__ void fence_proxy_async_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory to a CTA of the cluster; dst and bar are cluster
+// addresses (mapa), and the copy completes as transaction bytes on that CTA's
+// barrier.
+__device__ __forceinline__ void bulk_copy_s2s(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                              uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
 }
 
 // 2-D tiled TMA load into this CTA's shared memory whose completion bytes are

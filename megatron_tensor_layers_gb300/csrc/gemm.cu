@@ -121,18 +121,6 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& g,
     }
 }
 
-__device__ __forceinline__ float act_fn(float g, int act) {
-    if (act == TP_ACT_GELU_TANH_MUL) {
-        const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
-        return 0.5f * g * (1.0f + tanhf(k0 * (g + 0.044715f * g * g * g)));
-    }
-    // SiLU.  The approximate divide (two special-function ops with the exponential instead of
-    // an IEEE divide's longer sequence) errs by about 2 ulp of fp32, far below the bf16
-    // rounding of the stored H; for g below about -87 the denominator passes 2^126 and the
-    // result is 0, which is also what a bf16 H would hold.
-    return __fdividef(g, 1.0f + __expf(-g));
-}
-
 // Store one output element (bf16 or fp32) at (row, col).
 __device__ __forceinline__ void store_one(void* base, int64_t ldo, int out_f32, int64_t row, int col, float v) {
     if (out_f32)
@@ -1329,13 +1317,17 @@ static EncodeTiledFn get_encode_fn() {
 // cache is direct-mapped; a collision overwrites the older entry.
 struct MapKey {
     const void* ptr;
-    uint64_t dims[3];
-    uint64_t strides[2];
-    uint32_t box_rows;
+    uint64_t dims[4];
+    uint64_t strides[3];
+    uint32_t box[4];
     uint32_t rank;
     bool operator==(const MapKey& o) const {
-        return ptr == o.ptr && dims[0] == o.dims[0] && dims[1] == o.dims[1] && dims[2] == o.dims[2] &&
-               strides[0] == o.strides[0] && strides[1] == o.strides[1] && box_rows == o.box_rows && rank == o.rank;
+        if (ptr != o.ptr || rank != o.rank) return false;
+        for (int i = 0; i < 4; ++i)
+            if (dims[i] != o.dims[i] || box[i] != o.box[i]) return false;
+        for (int i = 0; i < 3; ++i)
+            if (strides[i] != o.strides[i]) return false;
+        return true;
     }
 };
 struct MapEntry {
@@ -1348,21 +1340,26 @@ constexpr int kMapCacheSlots = 128;
 static MapEntry& map_slot(const MapKey& k) {
     thread_local MapEntry cache[kMapCacheSlots];
     uint64_t h = reinterpret_cast<uintptr_t>(k.ptr) * 0x9E3779B97F4A7C15ull;
-    for (uint64_t v : {k.dims[0], k.dims[1], k.dims[2], k.strides[0], k.strides[1],
-                       static_cast<uint64_t>(k.box_rows) << 8 | k.rank})
+    for (uint64_t v : {k.dims[0], k.dims[1], k.dims[2], k.dims[3], k.strides[0], k.strides[1], k.strides[2],
+                       static_cast<uint64_t>(k.box[0]) | static_cast<uint64_t>(k.box[1]) << 16 |
+                           static_cast<uint64_t>(k.box[2]) << 32 | static_cast<uint64_t>(k.box[3]) << 48,
+                       static_cast<uint64_t>(k.rank)})
         h = (h ^ v) * 0x100000001B3ull;
     return cache[(h >> 32) % kMapCacheSlots];
 }
 
-// Encode (or copy from the cache) one bf16 tensor map with 128-byte swizzle
-// and boxes of 64 elements by box_rows rows (by 2 in the third dimension).
-static bool encode_map(CUtensorMap* m, const void* ptr, uint32_t rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides, int box_rows) {
+// Encode (or copy from the cache) one bf16 tensor map of rank 2 to 4 with
+// 128-byte swizzle and the given box (innermost first).
+static bool encode_map_box(CUtensorMap* m, const void* ptr, uint32_t rank, const cuuint64_t* dims,
+                           const cuuint64_t* strides, const cuuint32_t* box) {
+    if (rank < 2 || rank > 4) return false;
     MapKey k = {};
     k.ptr = ptr;
     k.rank = rank;
-    k.box_rows = static_cast<uint32_t>(box_rows);
-    for (uint32_t i = 0; i < rank; ++i) k.dims[i] = dims[i];
+    for (uint32_t i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+    }
     for (uint32_t i = 0; i + 1 < rank; ++i) k.strides[i] = strides[i];
     MapEntry& e = map_slot(k);
     if (e.valid && e.key == k) {
@@ -1371,9 +1368,9 @@ static bool encode_map(CUtensorMap* m, const void* ptr, uint32_t rank, const cuu
     }
     EncodeTiledFn enc = get_encode_fn();
     if (enc == nullptr) return false;
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 2};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, estr,
+    cuuint32_t bx[4] = {box[0], box[1], rank > 2 ? box[2] : 1u, rank > 3 ? box[3] : 1u};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, bx, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
@@ -1381,6 +1378,13 @@ static bool encode_map(CUtensorMap* m, const void* ptr, uint32_t rank, const cuu
     e.key = k;
     e.valid = true;
     return true;
+}
+
+// Boxes of 64 elements by box_rows rows (by 2 in the third dimension).
+static bool encode_map(CUtensorMap* m, const void* ptr, uint32_t rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, int box_rows) {
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 2};
+    return encode_map_box(m, ptr, rank, dims, strides, box);
 }
 
 // bf16 K-major operand [rows, cols] with row stride ld (elements), tiles of
@@ -1418,7 +1422,7 @@ static int raster_band(int tile_rows, int64_t k_total) {
 // Opt a kernel into its dynamic shared memory.  The attribute lasts for the
 // process, so it is set once per device (bit `dev` of `done`, one word per
 // kernel instantiation) and later launches skip the driver call.
-static bool smem_attribute_once(const void* kern, int bytes, std::atomic<uint64_t>& done) {
+bool smem_attribute_once(const void* kern, int bytes, std::atomic<uint64_t>& done) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
@@ -1443,6 +1447,49 @@ static bool make_map_glu(CUtensorMap* m, const void* ptr, int64_t half_rows, int
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(half_rows), 2};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(half_rows * ld) * 2};
     return encode_map(m, ptr, 3, dims, strides, box_rows);
+}
+
+bool make_operand_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    return make_map(m, ptr, rows, cols, ld, box_rows);
+}
+
+bool make_gated_operand_map(CUtensorMap* m, const void* ptr, int64_t half_rows, int64_t cols, int64_t ld,
+                            int box_rows) {
+    return make_map_glu(m, ptr, half_rows, cols, ld, box_rows);
+}
+
+bool make_kblock_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t k, int64_t ld, int box_rows,
+                     int box_kblocks) {
+    if (k % BK != 0) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(k / BK)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(BK) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows),
+                               static_cast<cuuint32_t>(box_kblocks)};
+    return encode_map_box(m, ptr, 3, dims, strides, box);
+}
+
+bool make_gated_kblock_map(CUtensorMap* m, const void* ptr, int64_t half_rows, int64_t k, int64_t ld, int box_rows,
+                           int box_kblocks) {
+    if (k % BK != 0) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(half_rows), 2,
+                                static_cast<cuuint64_t>(k / BK)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(half_rows * ld) * 2,
+                                   static_cast<cuuint64_t>(BK) * 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows), 2,
+                               static_cast<cuuint32_t>(box_kblocks)};
+    return encode_map_box(m, ptr, 4, dims, strides, box);
+}
+
+bool make_row_tile_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int tile_rows,
+                       int box_tiles) {
+    if (rows % tile_rows != 0) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(tile_rows),
+                                static_cast<cuuint64_t>(rows / tile_rows)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(ld * tile_rows) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(tile_rows),
+                               static_cast<cuuint32_t>(box_tiles)};
+    return encode_map_box(m, ptr, 3, dims, strides, box);
 }
 
 template <int BN, int STAGES, int EPI, int AROWS = BM, int KSUB = 1>

@@ -1,8 +1,10 @@
 // Internal launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "tp.h"
@@ -60,6 +62,61 @@ struct GemmDesc {
 };
 
 tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream);
+
+// Tensor maps of bf16 K-major operands as the GEMMs load them: 128-byte
+// swizzle, boxes 64 elements wide (along K) by box_rows rows, out-of-range
+// elements read as zero.  The gated form views [gate rows; up rows] as a 3-D
+// tensor {cols, half_rows, 2}, so that one box brings box_rows gate rows
+// followed by the same rows of up.  Encoded maps are cached per thread.
+bool make_operand_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows);
+bool make_gated_operand_map(CUtensorMap* m, const void* ptr, int64_t half_rows, int64_t cols, int64_t ld,
+                            int box_rows);
+// K-block views, for loading several K blocks with one copy: [rows, k] (row
+// stride ld, k a multiple of 64) seen as {64, rows, k/64} with the K-block
+// stride (128 bytes) below the row stride, so that one box {64, box_rows,
+// box_kblocks} lands as box_kblocks consecutive [box_rows][64] tiles, each in
+// the layout of a single-K-block box.  The gated form adds the gate/up
+// dimension: a box holds, per K block, box_rows gate rows then the same up
+// rows.
+bool make_kblock_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t k, int64_t ld, int box_rows,
+                     int box_kblocks);
+bool make_gated_kblock_map(CUtensorMap* m, const void* ptr, int64_t half_rows, int64_t k, int64_t ld, int box_rows,
+                           int box_kblocks);
+// Row tiles: [rows, cols] (rows a multiple of tile_rows) seen as {cols,
+// tile_rows, rows/tile_rows}; a box {64, tile_rows, box_tiles} lands as
+// box_tiles consecutive [tile_rows][64] tiles.
+bool make_row_tile_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int tile_rows,
+                       int box_tiles);
+
+// Opt a kernel into `bytes` of dynamic shared memory, once per device (bit
+// `dev` of `done`, one word per kernel).
+bool smem_attribute_once(const void* kern, int bytes, std::atomic<uint64_t>& done);
+
+// The MLP of one to eight tokens in one GEMM kernel plus an ordered reduce
+// (fused all-reduce): CTA pairs over 64-column slices of every rank's f
+// columns, for h a multiple of 256 up to 1024 and f/t a multiple of 64, at
+// most kSmallMlpMaxSlices slices.  Workspace: the slices' fp32 partials
+// [f/64][n][h].
+constexpr int kSmallMlpMaxRows = 8;
+constexpr int kSmallMlpMaxSlices = 128;
+struct SmallMlpDesc {
+    int t = 0;
+    int64_t n = 0, h = 0, f = 0;
+    const void* x = nullptr;
+    int64_t ldx = 0;
+    const void* w_gate_up[TP_MAX_SHARDS] = {};   // [2 f/t, h]: gate rows, then up rows
+    const void* w_down[TP_MAX_SHARDS] = {};      // [h, f/t], row stride ld_down
+    int64_t ld_down = 0;
+    const void* bias = nullptr;                   // [h] bf16 or null
+    int act = TP_ACT_SILU_MUL;
+    float* part = nullptr;                        // small_mlp_workspace bytes
+    void* y = nullptr;                            // [n, h] contiguous
+    int y_f32 = 0;
+    int* status = nullptr;
+};
+// Workspace bytes of the one-kernel path, or 0 when it does not apply.
+size_t small_mlp_workspace(int t, int64_t n, int64_t h, int64_t f, tp_reduce_mode mode);
+tp_status launch_small_mlp(const SmallMlpDesc& d, cudaStream_t stream);
 
 // Workspace bytes tp_mlp_forward cannot do without (H and the partials);
 // tp_mlp_workspace_size adds the optional stream-K tail area.  0 for invalid

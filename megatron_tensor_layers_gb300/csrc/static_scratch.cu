@@ -62,8 +62,9 @@ extern "C" tp_status tp_mlp_forward_static(int t, int64_t n, int64_t h, int64_t 
                                            int64_t ld_down, const void* bias_down, tp_act act,
                                            tp_reduce_mode mode, tp_dtype partial_dtype, void* y, tp_dtype y_dtype,
                                            tp_stream stream) {
-    // What tp_mlp_forward requires (H and the partials); the optional stream-K
-    // area of a fused reduce is used only if it fits as well.
+    // What tp_mlp_forward requires (H and the partials); the optional areas of
+    // a fused reduce (the stream-K slots, the one-kernel path's slice
+    // partials) are used only if they fit as well.
     const size_t need = tpk::mlp_workspace_required(t, n, h, f, mode, partial_dtype);
     if (need > static_cast<size_t>(TP_STATIC_SCRATCH_BYTES)) return TP_ERR_WORKSPACE;
     if (need == 0) {
@@ -75,8 +76,8 @@ extern "C" tp_status tp_mlp_forward_static(int t, int64_t n, int64_t h, int64_t 
     void* scratch = static_scratch_address();
     if (scratch == nullptr) return TP_ERR_CUDA;
     // Every byte of the scratch that this call reads is first written by this
-    // call (H by the gate_up GEMM, each partial by its rank's down GEMM), so
-    // nothing needs clearing between calls.
+    // call (H by the gate_up GEMM, each partial by the GEMM that produces it),
+    // so nothing needs clearing between calls.
     return tp_mlp_forward(t, n, h, f, x, ldx, w_gate_up, w_down, ld_down, bias_down, act, mode, partial_dtype,
                           scratch, TP_STATIC_SCRATCH_BYTES, y, y_dtype, stream);
 }

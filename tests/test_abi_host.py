@@ -184,3 +184,24 @@ def test_mlp_workspace_sizes(lib):
         assert ws(t, n, h, f, "ring", 1) == hb + t * al(n * h * 4)
         assert ws(t, n, h, f, "fused", 0) == hb + (tail if n > 128 else 0)
     assert ws(0, 8, h, f, "direct", 0) == 0 and ws(4, -1, h, f, "direct", 0) == 0
+
+
+def test_small_mlp_workspace_sizes(lib):
+    """A fused MLP of one to eight tokens with h a multiple of 256 up to 1024 and
+    f/t a multiple of 64 (at most 128 slices of 64 columns) runs as one GEMM kernel
+    plus an ordered reduce; its workspace holds the slices' fp32 partials
+    [f/64][n][h] (optional: with the H bytes alone the two-GEMM path runs)."""
+    al = lambda b: (b + 255) // 256 * 256
+    ws = lambda t, n, h, f, mode: lib.tp_mlp_workspace_size(t, n, h, f, _lib.MODES[mode], 0)
+    for n in range(1, 9):
+        assert ws(2, n, 1024, 3072, "fused") == al(48 * n * 1024 * 4)
+    assert ws(8, 8, 1024, 8192, "fused") == al(128 * 8 * 1024 * 4)
+    assert ws(3, 5, 512, 576, "fused") == al(9 * 5 * 512 * 4)
+    hb = lambda n, f: al(n * f * 2)
+    assert ws(2, 9, 1024, 3072, "fused") == hb(9, 3072)          # nine tokens
+    assert ws(2, 8, 1280, 3072, "fused") == hb(8, 3072)          # h above 1024
+    assert ws(2, 8, 640, 3072, "fused") == hb(8, 3072)           # h not a multiple of 256
+    assert ws(3, 8, 1024, 3072, "fused") == al(48 * 8 * 1024 * 4)  # three ranks of 1024 columns
+    assert ws(2, 8, 1024, 2080, "fused") == hb(8, 2080)          # f/t = 1040, not a multiple of 64
+    assert ws(8, 8, 1024, 8704, "fused") == hb(8, 8704)          # 136 slices
+    assert ws(2, 8, 1024, 3072, "direct") == hb(8, 3072) + 2 * al(8 * 1024 * 2)
