@@ -234,9 +234,14 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f,
  *   x_dev    device staging for X, [n, h] bf16; y_dev device [n, h] y_dtype.
  *   workspace  at least tp_mlp_workspace_size(t, ceil(n/chunks), h, f, mode,
  *              partial_dtype) bytes (one row block), 256-byte aligned.
- *   chunks   number of row blocks (1..64).  Block i's host->device copy runs
- *            on copy_stream under the compute of block i-1, its device->host
- *            copy under the compute of block i+1; the MLPs run on `stream`.
+ *   chunks   1..64: the rows are cut into blocks of at most ceil(n/chunks)
+ *            rows; with chunks >= 2 the first block has ceil(ceil(n/chunks)/2)
+ *            rows, the middle blocks ceil(n/chunks) and the last the rest (so
+ *            the exposed first copy and last read-back are about half a
+ *            block: n = 8192 in 4 chunks runs as 1024, 2048, 2048, 2048,
+ *            1024 rows).  Block i's host->device copy runs on copy_stream
+ *            under the compute of block i-1, its device->host copy under the
+ *            compute of block i+1; the MLPs run on `stream`.
  *   Other arguments as tp_mlp_forward.  When the call returns, all work is
  *   queued and `stream` completes after the last read-back (wait on it).
  * Errors as tp_mlp_forward; TP_ERR_WORKSPACE if the workspace is too small

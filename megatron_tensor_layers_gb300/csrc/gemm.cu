@@ -82,6 +82,7 @@ struct GemmArgs {
     int group_m;                      // tile raster: bands of group_m row-tiles (about kRasterBandMB of A rows)
     int bands_span_groups;            // 1: a band covers every group's columns (groups share A)
     int a_box_rows;                   // rows of A a TMA box loads (<= 128; fewer when M is small)
+    int kgroup_box;                   // tp_gemm_kernel: A and B maps are K-block views, one box per KSUB group
     int rotate_k;                     // start each tile's K loop at block (tile mod k_blocks)
     int act;                          // tp_act for the gated epilogue
     int split;                        // split-K kernel: CTAs per cluster sharing one output tile
@@ -212,6 +213,14 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     using Cfg = GemmCfg<BN, STAGES, EPI, AROWS>;
     static_assert(KSUB >= 1 && STAGES % KSUB == 0, "stage groups of KSUB blocks");
     constexpr int GROUPS = STAGES / KSUB;
+    // A group holds KSUB stages.  With one box per K block each stage is [A | B]; with K-block
+    // boxes (args.kgroup_box) the group is its KSUB A slabs, then its KSUB B tiles, so that one
+    // box can bring each (the A window of the M = 128 MMA reads on into the group's later
+    // tiles, never past the ring and its tail).
+    constexpr uint32_t kGroupBytes = KSUB * Cfg::STAGE_BYTES;
+    // Only the 64-row-A configurations (9 to 64 tokens) use K-block boxes; the others compile
+    // without the branch (at short K one more instruction per K block shows in the time).
+    constexpr bool kKGroup = KSUB > 1 && AROWS == 64;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles.
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -274,7 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                 // With a few rows of A every CTA would read the same line of A at the same k;
                 // starting each tile's K loop (each segment's, with segments) elsewhere spreads
                 // those reads over L2 and the weight reads over the DRAM channels.
-                const int rot = args.rotate_k ? tile % args.k_blocks : 0;
+                // With K-block boxes the rotation moves in whole groups, so that a group's KSUB
+                // blocks stay consecutive inside one segment.
+                const int rot = !args.rotate_k ? 0
+                                : args.kgroup_box ? (tile % (args.k_blocks / KSUB)) * KSUB
+                                                  : tile % args.k_blocks;
                 // (segment, block) advanced incrementally: no division in the issue loop
                 int seg = 0, kin = 0;
                 for (int kk = 0; kk < kb_per_tile; kk += KSUB) {
@@ -285,24 +298,44 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                     }
                     const uint32_t bar = full_bar(grp);
                     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * block_bytes);
+                    const uint32_t ga = base + grp * kGroupBytes;
+                    if (kKGroup && args.kgroup_box) {
+                        // the whole group in one A box and one B box (cnt == KSUB here)
+                        int kb = kin + rot;
+                        if (kb >= args.k_blocks) kb -= args.k_blocks;
+                        const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                        const int bi = args.segs > 1 ? seg : g;
+                        kin += KSUB;
+                        if (kin == args.k_blocks) {
+                            kin = 0;
+                            ++seg;
+                        }
+                        const uint32_t gb = ga + KSUB * Cfg::A_BYTES;    // the group's B tiles
+                        tma_load_3d(ga, &args.mapA[ai], bar, 0, m * BM, kb);
+                        if (EPI == EPI_GLU)
+                            tma_load_4d(gb, &args.mapB[bi], bar, 0, n * (BN / 2), 0, kb);
+                        else
+                            tma_load_3d(gb, &args.mapB[bi], bar, 0, n * BN, kb);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < KSUB; ++i) {
-                        if (i < cnt) {
-                            int kb = kin + rot;
-                            if (kb >= args.k_blocks) kb -= args.k_blocks;
-                            const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
-                            const int bi = args.segs > 1 ? seg : g;
-                            if (++kin == args.k_blocks) {
-                                kin = 0;
-                                ++seg;
-                            }
-                            const uint32_t sa = base + (grp * KSUB + i) * Cfg::STAGE_BYTES;
-                            const uint32_t sb = sa + Cfg::A_BYTES;
-                            tma_load_2d(sa, &args.mapA[ai], bar, kb * BK, m * BM);
-                            if (EPI == EPI_GLU) {   // gate rows and the same rows of up, one 3-D box
-                                tma_load_3d(sb, &args.mapB[bi], bar, kb * BK, n * (BN / 2), 0);
-                            } else {
-                                tma_load_2d(sb, &args.mapB[bi], bar, kb * BK, n * BN);
+                        for (int i = 0; i < KSUB; ++i) {
+                            if (i < cnt) {
+                                int kb = kin + rot;
+                                if (kb >= args.k_blocks) kb -= args.k_blocks;
+                                const int ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                                const int bi = args.segs > 1 ? seg : g;
+                                if (++kin == args.k_blocks) {
+                                    kin = 0;
+                                    ++seg;
+                                }
+                                const uint32_t sa = ga + i * Cfg::STAGE_BYTES;
+                                const uint32_t sb = sa + Cfg::A_BYTES;
+                                tma_load_2d(sa, &args.mapA[ai], bar, kb * BK, m * BM);
+                                if (EPI == EPI_GLU) {   // gate rows and the same rows of up, one 3-D box
+                                    tma_load_3d(sb, &args.mapB[bi], bar, kb * BK, n * (BN / 2), 0);
+                                } else {
+                                    tma_load_2d(sb, &args.mapB[bi], bar, kb * BK, n * BN);
+                                }
                             }
                         }
                     }
@@ -317,6 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t idesc = mma_idesc_bf16(BM, BN);
+            // Tile addresses inside a group: per stage [A | B], or (K-block boxes) the A slabs
+            // packed box-height apart, then the B tiles
+            const bool kg = kKGroup && args.kgroup_box != 0;
+            const uint32_t a_stride = kg ? static_cast<uint32_t>(args.a_box_rows) * 128u : Cfg::STAGE_BYTES;
+            const uint32_t b_first = kg ? KSUB * Cfg::A_BYTES : Cfg::A_BYTES;
+            const uint32_t b_stride = kg ? Cfg::B_BYTES : Cfg::STAGE_BYTES;
             int grp = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -338,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
 #pragma unroll
                     for (int i = 0; i < KSUB; ++i) {
                         if (i < cnt) {
-                            const uint32_t sa = base + (grp * KSUB + i) * Cfg::STAGE_BYTES;
-                            const uint64_t adesc = sw128_kmajor_desc(sa);
-                            const uint64_t bdesc = sw128_kmajor_desc(sa + Cfg::A_BYTES);
+                            const uint32_t ga = base + grp * kGroupBytes;
+                            const uint64_t adesc = sw128_kmajor_desc(ga + i * a_stride);
+                            const uint64_t bdesc = sw128_kmajor_desc(ga + b_first + i * b_stride);
 #pragma unroll
                             for (int k = 0; k < BK / 16; ++k) {
                                 // advance 16 bf16 = 32 bytes along K inside the swizzle row
@@ -1509,12 +1548,26 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
     // decode-sized A; with K segments the rotation stays inside each segment,
     // so the fused reduce still adds the shards in rank order
     a.rotate_k = d.M <= 64 ? 1 : 0;
-    for (int i = 0; i < nA; ++i)
-        if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
+    // Groups of KSUB K blocks load as one A box and one B box when every group is whole (a
+    // copy has a large fixed cost: at one box per K block a CTA streamed about 45 GB/s).
+    // Used with the 64-row A tiles (9 to 64 tokens: 70B MLP decode 0.5-0.8 % faster, the QKV
+    // GEMM 1.1-1.5 %); with the 8-row tiles it gained nothing and the tiny MLP's two-GEMM path
+    // lost 1-2 %, so those keep one box per K block.
+    a.kgroup_box = (KSUB > 1 && AROWS == 64 && d.K % (static_cast<int64_t>(BK) * KSUB) == 0) ? 1 : 0;
+    for (int i = 0; i < nA; ++i) {
+        const bool ok = a.kgroup_box ? make_kblock_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows, KSUB)
+                                     : make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows);
+        if (!ok) return TP_ERR_CUDA;
+    }
     for (int i = 0; i < nB; ++i) {
         const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
-        const bool ok = (EPI == EPI_GLU) ? make_map_glu(&a.mapB[i], d.b[i], d.glu_up_row, d.K, d.ldb, b_box)
-                                         : make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box);
+        bool ok;
+        if (EPI == EPI_GLU)
+            ok = a.kgroup_box ? make_gated_kblock_map(&a.mapB[i], d.b[i], d.glu_up_row, d.K, d.ldb, b_box, KSUB)
+                              : make_map_glu(&a.mapB[i], d.b[i], d.glu_up_row, d.K, d.ldb, b_box);
+        else
+            ok = a.kgroup_box ? make_kblock_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box, KSUB)
+                              : make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box);
         if (!ok) return TP_ERR_CUDA;
     }
     auto kern = tp_gemm_kernel<BN, STAGES, EPI, AROWS, KSUB>;

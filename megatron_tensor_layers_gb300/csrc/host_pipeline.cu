@@ -1,13 +1,16 @@
 // tp_mlp_forward_host: the tensor-parallel MLP for activations that live in
 // (pinned) host memory, with the copies overlapped with the compute.
 //
-// The n tokens are cut into `chunks` row blocks.  Block i is copied to the
-// device on `copy_stream`, the MLP of block i runs on `stream` once its copy
-// has landed (an event), and its output is copied back on `copy_stream` once
-// the MLP is done (another event).  All input copies are queued first in
-// order, so the copy of block i+1 runs under the compute of block i and the
-// read-back of block i under the compute of block i+1; only the first input
-// copy and the last read-back are exposed.  Rows are independent in every
+// The n tokens are cut into row blocks of at most ceil(n/chunks) rows.  Block
+// i is copied to the device on `copy_stream`, the MLP of block i runs on
+// `stream` once its copy has landed (an event), and its output is copied back
+// on `copy_stream` once the MLP is done (another event).  All input copies are
+// queued first in order, so the copy of block i+1 runs under the compute of
+// block i and the read-back of block i under the compute of block i+1; only
+// the first input copy and the last read-back are exposed, so with two or more
+// chunks the first and the last block are half as tall as the others
+// (chunks + 1 blocks): n = 8192 in 4 chunks runs as 1024, 2048, 2048, 2048,
+// 1024 rows.  Rows are independent in every
 // step of the MLP (page "6.2 Tensor-parallel inference", §1: each token's
 // output depends on its own row of X only), so splitting by rows changes no
 // result.
@@ -28,8 +31,12 @@ extern "C" tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
     if (chunks < 1 || chunks > 64 || n < 0 || h <= 0) return TP_ERR_INVALID_ARG;
     if (y_dtype != TP_BF16 && y_dtype != TP_F32) return TP_ERR_UNSUPPORTED;
     if (n == 0) return TP_OK;
-    const int64_t rows = (n + chunks - 1) / chunks;          // rows per block (the last may be shorter)
-    const int nblk = static_cast<int>((n + rows - 1) / rows);
+    const int64_t rows = (n + chunks - 1) / chunks;          // the tallest block
+    // block b covers rows [start(b), start(b + 1)): a half-height first block, then blocks of
+    // `rows`, the rest (at most `rows`, about half) last
+    const int64_t first = chunks > 1 ? std::min<int64_t>((rows + 1) / 2, n) : n;
+    const int nblk = first >= n ? 1 : 1 + static_cast<int>((n - first + rows - 1) / rows);
+    auto start = [&](int b) -> int64_t { return b == 0 ? 0 : std::min<int64_t>(n, first + (b - 1) * rows); };
     // The workspace must hold one block's MLP; validate the arguments with it
     // before anything is queued.
     const size_t need = tp_mlp_workspace_size(t, rows, h, f, mode, partial_dtype);
@@ -40,7 +47,7 @@ extern "C" tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaStream_t cp = reinterpret_cast<cudaStream_t>(copy_stream);
 
-    cudaEvent_t in_ready[64], out_ready[64];
+    cudaEvent_t in_ready[66], out_ready[66];
     int created = 0;
     tp_status st = TP_OK;
     for (; created < nblk; ++created) {
@@ -56,7 +63,7 @@ extern "C" tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
     }
     // every input copy first, in order, each followed by its event
     for (int b = 0; b < nblk && st == TP_OK; ++b) {
-        const int64_t r0 = b * rows, nr = std::min(rows, n - r0);
+        const int64_t r0 = start(b), nr = start(b + 1) - r0;
         if (cudaMemcpyAsync(static_cast<char*>(x_dev) + r0 * xrow, static_cast<const char*>(x_host) + r0 * xrow,
                             nr * xrow, cudaMemcpyHostToDevice, cp) != cudaSuccess ||
             cudaEventRecord(in_ready[b], cp) != cudaSuccess)
@@ -64,7 +71,7 @@ extern "C" tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
     }
     // compute block b once its input is on the device; read it back once computed
     for (int b = 0; b < nblk && st == TP_OK; ++b) {
-        const int64_t r0 = b * rows, nr = std::min(rows, n - r0);
+        const int64_t r0 = start(b), nr = start(b + 1) - r0;
         if (cudaStreamWaitEvent(cs, in_ready[b], 0) != cudaSuccess) {
             st = TP_ERR_CUDA;
             break;

@@ -8,7 +8,9 @@ than the L2 but of a few GB at most, so that a capture of one launch
 gather, seqpar, decode (70B MLP, t=4, 16 tokens, direct then fused, twice),
 pair2048 (prefill MLP, 2048 tokens: the CTA-pair gate_up and down GEMMs),
 fused1280 (fused down GEMM + reduce of 1280 rows given scratch: its last wave
-split along K).
+split along K), tiny (the tiny TP-MLP fused, t=2, h=1024, f=3072, 8 tokens: the
+one-kernel path, over 15 weight copies so that each call starts cold), qkv
+(the 70B attention QKV column GEMM at t=8, one token, two weight copies).
 """
 
 import sys
@@ -56,6 +58,21 @@ def run(mode: str, dev: str = "cuda") -> None:
         wgu = [synth.normal_bf16((2 * fs, H), 0.02, 10 + r, device=dev) for r in range(t)]
         wds = [synth.normal_bf16((H, fs), 0.02, 20 + r, device=dev) for r in range(t)]
         for _ in range(2): tp.tp_mlp_forward(x, wgu, wds, mode="direct")
+    elif mode == "tiny":                      # one-kernel fused MLP, 15 x 18.9 MB of weights
+        t, n, h, f = 2, 8, 1024, 3072
+        fs = f // t
+        sets = [(synth.normal_bf16((n, h), 1.0, 90 + 10 * j, device=dev),
+                 [synth.normal_bf16((2 * fs, h), 0.02, 91 + 10 * j + r, device=dev) for r in range(t)],
+                 [synth.normal_bf16((h, fs), 0.02, 95 + 10 * j + r, device=dev) for r in range(t)]) for j in range(15)]
+        for x, wgu, wds in sets:
+            tp.tp_mlp_forward(x, wgu, wds, mode="fused")
+    elif mode == "qkv":                       # 70B QKV, t=8, n=1: 8 x [1280, 8192], two weight copies
+        t = 8
+        copies = [[synth.normal_bf16((1280, H), 0.02, 900 + 50 * c + r, device=dev) for r in range(t)] for c in range(2)]
+        x = synth.normal_bf16((1, H), 1.0, 990, device=dev)
+        for _ in range(2):
+            for w in copies:
+                tp.tp_linear_col(x, w)
     elif mode == "fused1280":                 # fused down + reduce, 1280 rows: its last wave split along K
         t = 4; fs = F // t
         hs = [synth.normal_bf16((1280, fs), 1.0, 30 + r, device=dev) for r in range(t)]

@@ -636,9 +636,19 @@ def test_mlp_forward_host_matches_device_entry_point(chunks):
     torch.cuda.current_stream().synchronize()
     got = O.f32_bits_to_f64(yh.view(torch.int32).numpy().view(np.uint32))
     # rows are independent and every kernel choice depends only on the block's shape, so
-    # the host-buffer path gives the device entry point's bits where the blocks match
+    # the host-buffer path gives the device entry point's bits where the blocks match:
+    # one block, or with two or more chunks a half-height first block, blocks of
+    # ceil(n/chunks) rows, and the rest last
     if chunks == 1:
         assert torch.equal(yh.to(DEV), y_dev)
+    else:
+        first = (rows + 1) // 2
+        bounds = [0, first] + list(range(first + rows, n, rows)) + [n]
+        assert all(0 < b - a <= rows for a, b in zip(bounds, bounds[1:]))
+        for a, b in zip(bounds, bounds[1:]):
+            yb = tp.tp_mlp_forward(x[a:b], wgu, wds, mode="direct", partial_dtype=torch.float32,
+                                   y_dtype=torch.float32)
+            assert torch.equal(yh[a:b].to(DEV), yb), (a, b)
     mlp_check(got, f64(x), f64(wg), f64(wu), f64(wd), t)
 
 
