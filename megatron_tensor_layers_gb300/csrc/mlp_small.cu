@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_mlp_small_kernel(const __grid_
 
     if (threadIdx.x == 0) {
         abort_word = 0;
-        for (int i = 0; i < kb_n; ++i) mbar_init(bar0 + 8u * i, 1);
+        for (int i = 0; i < kb_n / kGroup; ++i) mbar_init(bar0 + 8u * i, 1);   // one per gate/up copy
         mbar_init(dw_bar, 1);
         mbar_init(mma1_bar, 1);
         mbar_init(hx_bar, 1);                       // own H tile written (+ the peer's copy of its tile)
@@ -171,9 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1) tp_mlp_small_kernel(const __grid_
             // The first kernel of the call: X and the weights may have been written by the
             // previous kernel of the stream, so nothing is loaded before the wait.
             pdl_wait();
-            // Six copies: X (all K blocks), the gate and up rows in groups of kGroup K blocks,
-            // the W_down tiles.  A copy's cost has a large fixed part, so few large boxes
-            // stream several times faster per SM than one box per K block.
+            // h/256 + 2 copies (six at h = 1024): X (all K blocks), the gate and up rows in
+            // groups of kGroup K blocks, the W_down tiles.  A copy's cost has a large fixed
+            // part, so few large boxes stream several times faster per SM than one box per
+            // K block.
             const int f0 = j * kSliceCols + static_cast<int>(q) * kHalfCols;
             const int groups = kb_n / kGroup;
             for (int gi = 0; gi < groups; ++gi) {

@@ -48,6 +48,7 @@ def _call_static(lib, t, n, h, f, x, wgu, wds, mode, pdt, y):
 
 @pytest.mark.parametrize("t,n,h,f,mode,pdt", [
     (2, 8, 1024, 3072, "direct", torch.bfloat16),     # the tiny TP-MLP config
+    (2, 8, 1024, 3072, "fused", torch.bfloat16),      # the same, one-kernel path (1.5 MB of slice partials)
     (4, 64, 8192, 28672, "direct", torch.float32),    # 70B-shaped decode, 12.1 MB of scratch
     (4, 64, 8192, 28672, "ring", torch.bfloat16),
     (8, 16, 8192, 28672, "fused", torch.bfloat16),
