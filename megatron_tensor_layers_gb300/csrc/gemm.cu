@@ -199,7 +199,7 @@ struct GemmCfg {
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(BN % 32 == 0 && BN <= 256, "M=128 MMA needs N % 16 == 0, N <= 256; epilogue chunks of 32");
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
-    static_assert(AROWS == BM || AROWS == 64 || AROWS == 8, "A tiles of 128, 64 or 8 rows");
+    static_assert(AROWS == BM || AROWS == 64 || AROWS == 16 || AROWS == 8, "A tiles of 128, 64, 16 or 8 rows");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -218,9 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     // box can bring each (the A window of the M = 128 MMA reads on into the group's later
     // tiles, never past the ring and its tail).
     constexpr uint32_t kGroupBytes = KSUB * Cfg::STAGE_BYTES;
-    // Only the 64-row-A configurations (9 to 64 tokens) use K-block boxes; the others compile
-    // without the branch (at short K one more instruction per K block shows in the time).
-    constexpr bool kKGroup = KSUB > 1 && AROWS == 64;
+    // Only the 16- and 64-row-A configurations (9 to 64 tokens) use K-block boxes; the others
+    // compile without the branch (at short K one more instruction per K block shows in the time).
+    constexpr bool kKGroup = KSUB > 1 && (AROWS == 64 || AROWS == 16);
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles.
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -955,8 +955,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_pair_kernel(const __grid_
 // memory alive while its peers may still read it.
 template <int BN, int STAGES, int EPI, int ROWS_ = 64>
 struct SplitCfg {
-    static constexpr int ROWS = ROWS_;                       // staged rows: M <= 64, or M <= 8
-    static constexpr int A_BYTES = ROWS * BK * 2;            // 64- or 8-row A tile (see GemmCfg's AROWS)
+    static constexpr int ROWS = ROWS_;                       // staged rows: M <= 64, M <= 16 or M <= 8
+    static constexpr int A_BYTES = ROWS * BK * 2;            // 64-, 16- or 8-row A tile (see GemmCfg's AROWS)
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGING_BYTES = ROWS * BN * 4;      // fp32 accumulator rows
@@ -967,7 +967,7 @@ struct SplitCfg {
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-    static_assert(ROWS == 64 || ROWS == 8, "64 or 8 staged rows");
+    static_assert(ROWS == 64 || ROWS == 16 || ROWS == 8, "64, 16 or 8 staged rows");
     static_assert(STAGE_BYTES >= BM * BK * 2, "the M = 128 MMA reads 16 KB of A from the stage's start");
 };
 
@@ -1553,7 +1553,7 @@ static tp_status launch_cfg(GemmArgs& a, const GemmDesc& d, cudaStream_t stream)
     // Used with the 64-row A tiles (9 to 64 tokens: 70B MLP decode 0.5-0.8 % faster, the QKV
     // GEMM 1.1-1.5 %); with the 8-row tiles it gained nothing and the tiny MLP's two-GEMM path
     // lost 1-2 %, so those keep one box per K block.
-    a.kgroup_box = (KSUB > 1 && AROWS == 64 && d.K % (static_cast<int64_t>(BK) * KSUB) == 0) ? 1 : 0;
+    a.kgroup_box = (KSUB > 1 && (AROWS == 64 || AROWS == 16) && d.K % (static_cast<int64_t>(BK) * KSUB) == 0) ? 1 : 0;
     for (int i = 0; i < nA; ++i) {
         const bool ok = a.kgroup_box ? make_kblock_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows, KSUB)
                                      : make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows);
@@ -1857,6 +1857,14 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
             if (plan.bn == 256) return launch_split<256, 6, EPI_STORE, 1, 8>(a, d, cs, stream);
             return launch_split<128, 12, EPI_STORE, 2, 8>(a, d, cs, stream);
         }
+        if (d.M <= 16) {  // 16 staged rows: 6 / 12 stages as well
+            if (glu) {
+                if (plan.bn == 256) return launch_split<256, 6, EPI_GLU, 1, 16>(a, d, cs, stream);
+                return launch_split<128, 12, EPI_GLU, 2, 16>(a, d, cs, stream);
+            }
+            if (plan.bn == 256) return launch_split<256, 6, EPI_STORE, 1, 16>(a, d, cs, stream);
+            return launch_split<128, 12, EPI_STORE, 2, 16>(a, d, cs, stream);
+        }
         if (glu) {
             if (plan.bn == 256) return launch_split<256, 4, EPI_GLU>(a, d, cs, stream);
             return launch_split<128, 8, EPI_GLU, 2>(a, d, cs, stream);
@@ -1874,6 +1882,17 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
         if (best == 128) return launch_cfg<128, 12, EPI_STORE, 8, 2>(a, d, stream);
         if (best == 96) return launch_cfg<96, 16, EPI_STORE, 8, 2>(a, d, stream);
         return launch_cfg<64, 24, EPI_STORE, 8, 4>(a, d, stream);
+    }
+    if (d.M <= 16) {   // nine to sixteen tokens: 16-row A tiles, rings deeper than with 64 rows
+        if (glu) {
+            if (best == 256) return launch_cfg<256, 6, EPI_GLU, 16>(a, d, stream);
+            if (best == 128) return launch_cfg<128, 10, EPI_GLU, 16, 2>(a, d, stream);
+            return launch_cfg<64, 20, EPI_GLU, 16, 4>(a, d, stream);
+        }
+        if (best == 256) return launch_cfg<256, 6, EPI_STORE, 16>(a, d, stream);
+        if (best == 128) return launch_cfg<128, 12, EPI_STORE, 16, 2>(a, d, stream);
+        if (best == 96) return launch_cfg<96, 14, EPI_STORE, 16, 2>(a, d, stream);
+        return launch_cfg<64, 20, EPI_STORE, 16, 4>(a, d, stream);
     }
     if (d.M <= 64) {   // decode: 64-row A tiles, deeper B rings
         if (glu) {

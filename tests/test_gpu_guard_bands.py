@@ -197,14 +197,15 @@ def test_fused_stream_k_on_two_streams():
             assert torch.equal(ys[i], alone[i])
 
 
+@pytest.mark.parametrize("n", [5, 13])
 @pytest.mark.parametrize("tile_n", [64, 96, 128, 256])
 @pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
-def test_few_row_gemm_outputs_stay_inside(tile_n, ydt):
-    """Five rows (the 8-row A tiles with the deepest B rings) at every tile width: the
-    plain, gated and row GEMMs write only inside their outputs."""
+def test_few_row_gemm_outputs_stay_inside(tile_n, ydt, n):
+    """Five and thirteen rows (the 8- and 16-row A tiles with the deepest B rings) at every
+    tile width: the plain, gated and row GEMMs write only inside their outputs."""
     tp.tp_set_gemm_tile_n(tile_n)
     try:
-        t, n, k, os_ = 3, 5, 1000, 200
+        t, k, os_ = 3, 1000, 200
         x = ints((n, k), 160)
         w = [ints((os_, k), 161 + r) for r in range(t)]
         outs = [guarded(n, os_, ydt) for _ in range(t)]

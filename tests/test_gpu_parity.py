@@ -468,14 +468,17 @@ def test_every_tile_width_integer_exact(tile_n):
 
 
 @pytest.mark.parametrize("tile_n", [64, 96, 128, 256], indirect=True)
-@pytest.mark.parametrize("n", [1, 5, 8, 9, 64])
-def test_every_tile_width_few_rows(tile_n, n):
+@pytest.mark.parametrize("k", [2200, 2560])
+@pytest.mark.parametrize("n", [1, 5, 8, 9, 12, 16, 17, 64])
+def test_every_tile_width_few_rows(tile_n, n, k):
     """Decode-sized GEMMs at every tile width: up to 8 rows take the 8-row A tiles
-    with the deepest B rings (24 stages at width 64), 9 to 64 rows the 64-row A
-    tiles.  K = 2200 (35 blocks, a ragged last one) wraps every ring; the plain and
-    the row GEMMs are integer-exact, the gated GEMM's H is the exact rounding up to
+    with the deepest B rings (24 stages at width 64), 9 to 16 rows the 16-row A
+    tiles, 17 to 64 rows the 64-row A tiles.  K = 2200 (35 blocks, a ragged last
+    one) wraps every ring with one box per K block; K = 2560 (40 blocks) loads the
+    16- and 64-row tiles' groups of K blocks as single boxes.  The plain and the
+    row GEMMs are integer-exact, the gated GEMM's H is the exact rounding up to
     flips at midpoints."""
-    t, k, os_ = 3, 2200, 328
+    t, os_ = 3, 328
     x = ints((n, k), 130 + n)
     w = [ints((os_, k), 131 + r) for r in range(t)]
     y = tp.tp_linear_col(x, w, y_dtype=torch.float32)
