@@ -196,9 +196,10 @@ tp_status tp_shard_reduce(int t, int64_t count, tp_dtype dtype, const void* cons
 }
 
 // pdl_first = 1: the previous launch of the stream is a kernel of the same
-// call that wrote x (tp_mlp_forward's gate_up GEMM), so the split-K GEMM may
-// load weights before waiting for it; 0: the first kernel of the call, which
-// loads nothing before that wait.  Every launch may start early.
+// call that wrote x (tp_mlp_forward's gate_up GEMM), so the GEMM (split-K or
+// single-CTA) may load its first ring of weights before waiting for it; 0: the
+// first kernel of the call, which loads nothing before that wait.  Every
+// launch may start early.
 // sk_ws / sk_bytes: the stream-K tail area of a fused reduce (flags already
 // zeroed in stream order), or null.
 static tp_status linear_row_impl(int t, int64_t n, int64_t in_full, int64_t out, const void* const* x, int64_t ldx,

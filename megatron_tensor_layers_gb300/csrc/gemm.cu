@@ -34,8 +34,8 @@
 // serialization: it may start while the previous kernel of the stream
 // drains.  Its producer executes griddepcontrol.wait before loading anything
 // that kernel may have written: for the first kernel of a library call that
-// is everything; only the split-K kernel, when it is a later kernel of the
-// same call (whose predecessor writes no weights), loads its first ring of
+// is everything; a split-K or single-CTA GEMM that is a later kernel of the
+// same call (whose predecessor writes no weights) loads its first ring of
 // weights before the wait.
 // The stage ring is split into groups of KSUB stages (K blocks) under one
 // full and one empty barrier each, so the producer and MMA threads wait, arm
@@ -270,13 +270,81 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
             // With a programmatic launch the previous grid of the stream may still be running
-            // (A can be its output).  Waiting before the first load keeps this loop as lean as
-            // it was: at decode sizes the producer's issue rate bounds the weight stream, and a
-            // variant that loaded the first ring of weights before the wait ran 6 % slower.
-            pdl_wait();
+            // (A can be its output).  When that grid is a kernel of the same call, which writes
+            // no B (pdl_prefetch), the first ring of the first tile's weights is loaded before
+            // the wait and its A blocks after it; the loop below then starts that tile past
+            // those groups, so the issue loop itself gains no branch (at decode sizes the
+            // producer's issue rate bounds the weight stream: a per-block check of whether a
+            // stage was already armed cost 6 %).
             int grp = 0;
             uint32_t phase = 0;
             const uint32_t block_bytes = static_cast<uint32_t>(args.a_box_rows * 128 + Cfg::B_BYTES);
+            const bool kgb = kKGroup && args.kgroup_box;
+            auto tile_rot = [&](int tile) {
+                return !args.rotate_k ? 0
+                       : kgb          ? (tile % (args.k_blocks / KSUB)) * KSUB
+                                      : tile % args.k_blocks;
+            };
+            // K block number, segment and A/B map of position kk of a tile's K loop
+            auto kpos = [&](int kk, int rot, int g, int& kb, int& ai, int& bi) {
+                const int seg = kk / args.k_blocks;
+                kb = kk - seg * args.k_blocks + rot;
+                if (kb >= args.k_blocks) kb -= args.k_blocks;
+                ai = args.segs > 1 ? seg : (args.a_per_group ? g : 0);
+                bi = args.segs > 1 ? seg : g;
+            };
+            int pre_kk = 0;                                // K blocks of the first tile already issued
+            if (args.pdl_prefetch && static_cast<int>(blockIdx.x) < args.total_tiles) {
+                int g, m, n;
+                tile_coords(args, blockIdx.x, g, m, n);
+                const int rot = tile_rot(blockIdx.x);
+                const int pre_groups = min(GROUPS, (kb_per_tile + KSUB - 1) / KSUB);
+                for (int gi = 0; gi < pre_groups; ++gi) {    // B, before the wait
+                    const int cnt = min(KSUB, kb_per_tile - gi * KSUB);
+                    mbar_arrive_expect_tx(full_bar(gi), static_cast<uint32_t>(cnt) * block_bytes);
+                    const uint32_t ga = base + gi * kGroupBytes;
+                    if (kgb) {
+                        int kb, ai, bi;
+                        kpos(gi * KSUB, rot, g, kb, ai, bi);
+                        const uint32_t gb = ga + KSUB * Cfg::A_BYTES;
+                        if (EPI == EPI_GLU)
+                            tma_load_4d(gb, &args.mapB[bi], full_bar(gi), 0, n * (BN / 2), 0, kb);
+                        else
+                            tma_load_3d(gb, &args.mapB[bi], full_bar(gi), 0, n * BN, kb);
+                    } else {
+                        for (int i = 0; i < cnt; ++i) {
+                            int kb, ai, bi;
+                            kpos(gi * KSUB + i, rot, g, kb, ai, bi);
+                            const uint32_t sb = ga + i * Cfg::STAGE_BYTES + Cfg::A_BYTES;
+                            if (EPI == EPI_GLU)
+                                tma_load_3d(sb, &args.mapB[bi], full_bar(gi), kb * BK, n * (BN / 2), 0);
+                            else
+                                tma_load_2d(sb, &args.mapB[bi], full_bar(gi), kb * BK, n * BN);
+                        }
+                    }
+                }
+                pdl_wait();
+                for (int gi = 0; gi < pre_groups; ++gi) {    // A, after it
+                    const int cnt = min(KSUB, kb_per_tile - gi * KSUB);
+                    const uint32_t ga = base + gi * kGroupBytes;
+                    if (kgb) {
+                        int kb, ai, bi;
+                        kpos(gi * KSUB, rot, g, kb, ai, bi);
+                        tma_load_3d(ga, &args.mapA[ai], full_bar(gi), 0, m * BM, kb);
+                    } else {
+                        for (int i = 0; i < cnt; ++i) {
+                            int kb, ai, bi;
+                            kpos(gi * KSUB + i, rot, g, kb, ai, bi);
+                            tma_load_2d(ga + i * Cfg::STAGE_BYTES, &args.mapA[ai], full_bar(gi), kb * BK, m * BM);
+                        }
+                    }
+                }
+                pre_kk = min(kb_per_tile, pre_groups * KSUB);
+                grp = pre_groups == GROUPS ? 0 : pre_groups;
+                phase = pre_groups == GROUPS ? 1u : 0u;
+            } else {
+                pdl_wait();
+            }
             for (int tile = blockIdx.x; tile < args.total_tiles && !aborted; tile += gridDim.x) {
                 int g, m, n;
                 tile_coords(args, tile, g, m, n);
@@ -285,12 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                 // those reads over L2 and the weight reads over the DRAM channels.
                 // With K-block boxes the rotation moves in whole groups, so that a group's KSUB
                 // blocks stay consecutive inside one segment.
-                const int rot = !args.rotate_k ? 0
-                                : args.kgroup_box ? (tile % (args.k_blocks / KSUB)) * KSUB
-                                                  : tile % args.k_blocks;
+                const int rot = tile_rot(tile);
                 // (segment, block) advanced incrementally: no division in the issue loop
-                int seg = 0, kin = 0;
-                for (int kk = 0; kk < kb_per_tile; kk += KSUB) {
+                const int kk0 = tile == static_cast<int>(blockIdx.x) ? pre_kk : 0;
+                int seg = kk0 / args.k_blocks, kin = kk0 - seg * args.k_blocks;
+                for (int kk = kk0; kk < kb_per_tile; kk += KSUB) {
                     const int cnt = min(KSUB, kb_per_tile - kk);   // a tile's last group may be short
                     if (!mbar_wait(empty_bar(grp), phase ^ 1u, abort_flag, args.status)) {
                         aborted = true;
@@ -299,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                     const uint32_t bar = full_bar(grp);
                     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt) * block_bytes);
                     const uint32_t ga = base + grp * kGroupBytes;
-                    if (kKGroup && args.kgroup_box) {
+                    if (kgb) {
                         // the whole group in one A box and one B box (cnt == KSUB here)
                         int kb = kin + rot;
                         if (kb >= args.k_blocks) kb -= args.k_blocks;

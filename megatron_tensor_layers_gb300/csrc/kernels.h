@@ -51,7 +51,8 @@ struct GemmDesc {
     // Programmatic dependent launch: the launch may start before the previous kernel of
     // the stream ends, and its producer waits for that kernel (griddepcontrol.wait) before
     // loading.  1: the previous kernel belongs to the same library call and writes no B,
-    // so the split-K kernel may load its first ring of B before the wait; 2: the first
+    // so the split-K and single-CTA kernels may load their first ring of B before the
+    // wait; 2: the first
     // kernel of a call, whose predecessor may have written anything: nothing is loaded
     // before the wait.
     int pdl = 0;

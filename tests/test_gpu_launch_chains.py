@@ -176,3 +176,26 @@ def test_event_wait_still_orders_a_programmatic_launch():
     xf = f64(x_new_host.to(DEV))
     for r in range(t):
         assert np.array_equal(f64(y[r]), O.linear(xf, f64(w[r])))
+
+
+@pytest.mark.parametrize("mode", ["direct", "ring"])
+@pytest.mark.parametrize("t,n,h,f", [(3, 1, 320, 1800), (3, 5, 320, 1800), (2, 12, 512, 2176), (4, 40, 256, 4352),
+                                     (4, 1, 8192, 28672), (4, 16, 8192, 28672)])
+def test_mlp_forward_equals_its_two_calls(mode, t, n, h, f):
+    """tp_mlp_forward's down GEMM loads its first ring of weights before it waits for
+    the gate_up GEMM (its predecessor in the call writes only H); a tp_linear_row call
+    loads nothing before its wait.  Same kernels and the same order of arithmetic, so
+    the MLP equals the gated tp_linear_col followed by tp_linear_row bit for bit.  K of
+    the down GEMM is 600 and 1088 (ragged last K blocks), 7168 at the 70B shapes; the
+    rings are shorter and longer than a tile's K loop; 1 to 40 rows take the 8-, 16- and
+    64-row A tiles."""
+    fs = f // t
+    x = synth.normal_bf16((n, h), 1.0, 400 + n, device=DEV)
+    wgu = [synth.normal_bf16((2 * fs, h), 0.02, 410 + r, device=DEV) for r in range(t)]
+    wds = [synth.normal_bf16((h, fs), 0.02, 420 + r, device=DEV) for r in range(t)]
+    y1 = tp.tp_mlp_forward(x, wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
+    hs = tp.tp_linear_col(x, wgu, act="silu")
+    y2 = tp.tp_linear_row(hs, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    _same_bits(y1, y2)
