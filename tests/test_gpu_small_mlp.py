@@ -185,3 +185,26 @@ def test_small_mlp_back_to_back_on_one_workspace():
         alone = tp.tp_mlp_forward(xi, wgu, wds, mode="fused", y_dtype=torch.float32)
         torch.cuda.synchronize()
         assert torch.equal(yi, alone)
+
+
+@pytest.mark.parametrize("t,n,h,f", [(2, 8, 1024, 3072), (3, 5, 512, 576)])
+def test_small_mlp_strided_operands(t, n, h, f):
+    """X as a column view of a wider buffer (row stride h + 64) and W_down as column
+    slices of the full [h, f] matrix (row stride f): the one-kernel path reads them
+    through their strides and gives the contiguous call's bits."""
+    fs = f // t
+    x_full = synth.normal_bf16((n, h + 64), 1.0, 500, device=DEV)
+    x = x_full[:, :h]
+    wg = synth.normal_bf16((f, h), 0.02, 501, device=DEV)
+    wu = synth.normal_bf16((f, h), 0.02, 502, device=DEV)
+    wd = synth.normal_bf16((h, f), 0.02, 503, device=DEV)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds_view = [wd[:, r * fs:(r + 1) * fs] for r in range(t)]
+    wds = [w.contiguous() for w in wds_view]
+    ws = torch.empty(_small_ws(t, n, h, f), dtype=torch.uint8, device=DEV)
+    y_strided = tp.tp_mlp_forward(x, wgu, wds_view, mode="fused", workspace=ws, y_dtype=torch.float32)
+    y_plain = tp.tp_mlp_forward(x.contiguous(), wgu, wds, mode="fused", workspace=ws, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    assert torch.equal(y_strided, y_plain)
+    mlp_check(f64(y_plain), f64(x), f64(wg), f64(wu), f64(wd), t, mode="fused")
