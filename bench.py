@@ -432,7 +432,8 @@ def _detail_attn(torch, tp, synth, dev, hbm, ten):
     """The attention block's tensor-parallel projections at Llama-3.1-70B shapes, t=8
     (64 query heads, 8 KV heads, head size 128, h=8192): the head-aligned QKV column GEMM
     (rank r: 8 query heads and 1 KV head, [1280, 8192]) and the o_proj row GEMM ([8192,
-    1024] per rank) into bf16 partials with the direct reduce.  The attention between them
+    1024] per rank) into bf16 partials with the direct reduce, or with the reduce fused into
+    the o_proj GEMM (rows tagged "_fused").  The attention between them
     is not part of the path; o_proj reads a seeded stand-in.  Decode (n=1, 64) is weight
     streaming, timed as CUDA graphs over two weight copies (2 x 302 MB, beyond the L2);
     prefill (n=8192) is compared with the tensor peak."""
@@ -470,9 +471,10 @@ def _detail_attn(torch, tp, synth, dev, hbm, ten):
                     out[f"attn_proj_t8_n{n}{tag}"] = {"graph_us": gs * 1e6, "weight_GBps": wbytes / gs / 1e9,
                                                       "graph_hbm_frac": wbytes / gs / 1e9 / hbm}
         else:
-            s = time_fn(torch, proj(copies[0]), 10)
             fl = 2.0 * n * h * (t * (qh + 2 * hd)) + 2.0 * n * h * (nh * hd)
-            out[f"attn_proj_t8_n{n}"] = {"ms": s * 1e3, "tflops": fl / s / 1e12, "frac": fl / s / 1e12 / ten}
+            for mode, tag in (("direct", ""), ("fused", "_fused")):
+                s = time_fn(torch, proj(copies[0], mode), 10)
+                out[f"attn_proj_t8_n{n}{tag}"] = {"ms": s * 1e3, "tflops": fl / s / 1e12, "frac": fl / s / 1e12 / ten}
         del x, attn, qkv, parts, y
     del copies
     torch.cuda.empty_cache()
