@@ -373,8 +373,12 @@ tp_status launch_small_mlp(const SmallMlpDesc& d, cudaStream_t stream) {
     a.status = d.status;
     const int slices = static_cast<int>(d.f / kSliceCols);
     const int smem = static_cast<int>(SmallLayout(a.h).total) + 1024;
+    // The shared memory depends on h, and the opt-in is set once per device: set it for the
+    // largest h, so that a first call with a smaller h does not cap later ones.
     static std::atomic<uint64_t> smem_set{0};
-    if (!smem_attribute_once(reinterpret_cast<const void*>(tp_mlp_small_kernel), smem, smem_set)) return TP_ERR_CUDA;
+    if (!smem_attribute_once(reinterpret_cast<const void*>(tp_mlp_small_kernel),
+                             static_cast<int>(SmallLayout(kMaxH).total) + 1024, smem_set))
+        return TP_ERR_CUDA;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * slices, 1, 1);

@@ -208,3 +208,48 @@ def test_small_mlp_strided_operands(t, n, h, f):
     assert tp.tp_device_status() == 0
     assert torch.equal(y_strided, y_plain)
     mlp_check(f64(y_plain), f64(x), f64(wg), f64(wu), f64(wd), t, mode="fused")
+
+
+def _random_shapes(count, seed):
+    """Seeded eligible shapes: t in 1..8, n in 1..8, h in {256, 512, 768, 1024}, f/t a multiple
+    of 64 with at most 128 slices of 64 columns in all."""
+    rnd = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        t = int(rnd.integers(1, 9))
+        n = int(rnd.integers(1, 9))
+        h = int(rnd.choice([256, 512, 768, 1024]))
+        per = int(rnd.integers(1, 128 // t + 1))          # slices per rank
+        out.append((t, n, h, 64 * per * t))
+    return out
+
+
+@pytest.mark.parametrize("t,n,h,f", _random_shapes(12, 77))
+def test_small_mlp_integer_exact_random_shapes(t, n, h, f):
+    act = "silu" if (t + n) % 2 else "gelu_tanh"
+    x, wg, wu, wd, bias = _integer_mlp(t, n, h, f, 3000 + 7 * t + n)
+    ref = O.mlp_sharded_rounded(x.numpy(), wg.numpy(), wu.numpy(), wd.numpy(), t, bias.numpy(), act, None)
+    wgu, wds = _shards(wg, wu, wd, t)
+    ws = torch.empty(_small_ws(t, n, h, f), dtype=torch.uint8, device=DEV)
+    y = tp.tp_mlp_forward(x.to(torch.bfloat16).to(DEV), wgu, wds, bias_down=bias.to(torch.bfloat16).to(DEV), act=act,
+                          mode="fused", workspace=ws, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    exact(f64(y), ref["y"])
+
+
+def test_small_mlp_smaller_h_first():
+    """The kernel's shared memory grows with h; a first call with a small h must not cap
+    the shared memory of later calls with a larger one (each shape in a fresh order)."""
+    for (t, n, h, f) in [(2, 3, 256, 512), (2, 3, 768, 1536), (2, 3, 1024, 2048), (2, 3, 512, 1024)]:
+        fs = f // t
+        x = synth.normal_bf16((n, h), 1.0, 600 + h, device=DEV)
+        wg = synth.normal_bf16((f, h), 0.02, 601 + h, device=DEV)
+        wu = synth.normal_bf16((f, h), 0.02, 602 + h, device=DEV)
+        wd = synth.normal_bf16((h, f), 0.02, 603 + h, device=DEV)
+        wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+        wds = [wd[:, r * fs:(r + 1) * fs].contiguous() for r in range(t)]
+        y = tp.tp_mlp_forward(x, wgu, wds, mode="fused", y_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert tp.tp_device_status() == 0
+        mlp_check(f64(y), f64(x), f64(wg), f64(wu), f64(wd), t, mode="fused")
