@@ -199,3 +199,40 @@ def test_mlp_forward_equals_its_two_calls(mode, t, n, h, f):
     torch.cuda.synchronize()
     assert tp.tp_device_status() == 0
     _same_bits(y1, y2)
+
+
+def _random_mlp_shapes(count, seed):
+    """Seeded shapes for tp_mlp_forward: t 1..8, f/t and h multiples of 8 (h up to 1600),
+    token counts across the 8-, 16- and 64-row A tiles, the single-CTA and pair kernels."""
+    rnd = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        t = int(rnd.integers(1, 9))
+        fs = 8 * int(rnd.integers(1, 150))
+        h = 8 * int(rnd.integers(8, 201))
+        n = int(rnd.choice([rnd.integers(1, 9), rnd.integers(9, 17), rnd.integers(17, 65), rnd.integers(65, 300)]))
+        out.append((t, n, h, fs * t))
+    return out
+
+
+@pytest.mark.parametrize("t,n,h,f", _random_mlp_shapes(16, 2026))
+def test_mlp_forward_random_shapes(t, n, h, f):
+    """Direct and ring: bit for bit the gated tp_linear_col followed by tp_linear_row.
+    Fused: the MLP gates against the oracle."""
+    fs = f // t
+    x = synth.normal_bf16((n, h), 1.0, 700 + n, device=DEV)
+    wgu = [synth.normal_bf16((2 * fs, h), 0.02, 710 + r, device=DEV) for r in range(t)]
+    wds = [synth.normal_bf16((h, fs), 0.02, 720 + r, device=DEV) for r in range(t)]
+    hs = tp.tp_linear_col(x, wgu, act="silu")
+    for mode in ("direct", "ring"):
+        y1 = tp.tp_mlp_forward(x, wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
+        y2 = tp.tp_linear_row(hs, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32)
+        torch.cuda.synchronize()
+        _same_bits(y1, y2)
+    yf = tp.tp_mlp_forward(x, wgu, wds, mode="fused", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    wg = torch.cat([w[:fs] for w in wgu])
+    wu = torch.cat([w[fs:] for w in wgu])
+    wd = torch.cat(wds, dim=1)
+    mlp_check(f64(yf), f64(x), f64(wg), f64(wu), f64(wd), t, mode="fused")
