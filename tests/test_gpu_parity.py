@@ -655,6 +655,41 @@ def test_mlp_forward_host_matches_device_entry_point(chunks):
     mlp_check(got, f64(x), f64(wg), f64(wu), f64(wd), t)
 
 
+@pytest.mark.parametrize("mode", ["direct", "fused"])
+@pytest.mark.parametrize("n,chunks", [(1, 1), (3, 8), (7, 2), (13, 64), (40, 5), (129, 3)])
+def test_mlp_forward_host_small_blocks(n, chunks, mode):
+    """Few tokens cut into many row blocks (down to one row): each block's MLP is the device
+    entry point's on that block, bit for bit; in fused mode blocks of up to 8 rows take the
+    one-kernel path (h = 1024, 64-column slices) when the workspace holds their partials."""
+    t, h, f = 2, 1024, 3072
+    fs = f // t
+    x = normal((n, h), 1.0, 250 + n)
+    wg, wu, wd = normal((f, h), 0.02, 251), normal((f, h), 0.02, 252), normal((h, f), 0.02, 253)
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
+    wds = [wd[:, r * fs:(r + 1) * fs] for r in range(t)]
+    rows = (n + chunks - 1) // chunks
+    ws = torch.empty(tp.tp_mlp_workspace_size(t, rows, h, f, mode, torch.float32), dtype=torch.uint8, device=DEV)
+    xh = torch.empty((n, h), dtype=torch.bfloat16, pin_memory=True)
+    xh.copy_(x)
+    yh = torch.full((n, h), float("nan"), dtype=torch.float32, pin_memory=True)
+    xd = torch.empty_like(x)
+    yd = torch.empty((n, h), dtype=torch.float32, device=DEV)
+    tp.tp_mlp_forward_host(xh, wgu, wds, y_host=yh, x_dev=xd, y_dev=yd, workspace=ws, mode=mode,
+                           partial_dtype=torch.float32, chunks=chunks)
+    torch.cuda.current_stream().synchronize()
+    assert tp.tp_device_status() == 0
+    first = (rows + 1) // 2 if chunks > 1 else n
+    bounds = [0] + ([first] if first < n else []) + list(range(first + rows, n, rows)) + [n]
+    bounds = sorted(set(bounds))
+    for a, b in zip(bounds, bounds[1:]):
+        yb = tp.tp_mlp_forward(x[a:b], wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32,
+                               workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(yh[a:b].to(DEV), yb), (a, b)
+    got = O.f32_bits_to_f64(yh.view(torch.int32).numpy().view(np.uint32))
+    mlp_check(got, f64(x), f64(wg), f64(wu), f64(wd), t, mode=mode)
+
+
 # ------------------------------------------- sequence parallelism (RS + norm)
 
 def _rs_fold_f32(pf, t, n, order):
