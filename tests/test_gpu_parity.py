@@ -725,6 +725,38 @@ def test_reduce_scatter_rmsnorm(t, n, h, order, dtype):
     assert np.all(np.abs(got - normed) <= bound), float(np.max(np.abs(got - normed) - bound))
 
 
+def _random_seqpar_shapes(count, seed):
+    """Seeded shapes: t 1..8, n 1..300 (rows not divisible by t included), h a multiple of 8
+    up to 32768, orders and partial dtypes mixed."""
+    rnd = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        t = int(rnd.integers(1, 9))
+        n = int(rnd.integers(1, 301))
+        h = 8 * int(rnd.choice([rnd.integers(1, 129), rnd.integers(129, 4097)]))
+        out.append((t, n, h, str(rnd.choice(["direct", "ring"])), bool(rnd.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("t,n,h,order,f32", _random_seqpar_shapes(12, 404))
+def test_reduce_scatter_rmsnorm_random(t, n, h, order, f32):
+    dtype = torch.float32 if f32 else torch.bfloat16
+    parts = [(synth.normal_f32((n, h), 1.0, 600 + r, device=DEV)).to(dtype) for r in range(t)]
+    resid = normal((n, h), 1.0, 620)
+    w = normal((h,), 1.0, 621)
+    res_out = torch.empty((n, h), dtype=torch.bfloat16, device=DEV)
+    _, out = tp.tp_reduce_scatter_rmsnorm(parts, w, residual=resid, eps=1e-6, mode=order, residual_out=res_out)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    pf = [f64(p) for p in parts]
+    x32 = (_rs_fold_f32(pf, t, n, order).astype(np.float32) + f64(resid).astype(np.float32)).astype(np.float32)
+    exact(f64(res_out), O.round_to_bf16(x32.astype(np.float64)))
+    _, normed, _ = O.sequence_parallel_residual_norm(pf, f64(resid), f64(w), 1e-6, order)
+    got = f64(out)
+    bound = half_ulp_bf16(normed) + 1e-4 * np.abs(normed) + 1e-6
+    assert np.all(np.abs(got - normed) <= bound), float(np.max(np.abs(got - normed) - bound))
+
+
 def test_reduce_scatter_rmsnorm_in_place_and_no_residual():
     t, n, h = 4, 16, 256
     parts = [normal((n, h), 1.0, 530 + r) for r in range(t)]
