@@ -399,3 +399,32 @@ def test_attention_projections_70b_t8(n):
     wof = f64(wo)
     parts = [O.linear(f64(attn[r][rows]), O.row_shard(wof, t, r)) for r in range(t)]
     gemm_gate(f64(y[rows]), O.reduce_direct(parts), bf16_out=False)
+
+
+
+# (t, n, out, K per shard): fused row GEMMs that take CTA pairs with 256 x 256 tiles and
+# leave a short last wave on the 76 resident pairs, drawn by a seeded search over t 2..8,
+# n 600..4096, out 8192..16384 and K a multiple of 8 (ragged last K blocks included).  The
+# tail tiles split into 2 (36-tile tails), 3 (24) and 4 (4, 8, 16) K parts.
+STREAM_K_SHAPES = [(7, 3962, 16384, 1976), (8, 3779, 12288, 344), (7, 3142, 8192, 680), (3, 3130, 8192, 576),
+                   (7, 3824, 8192, 736), (3, 3590, 8192, 1568),
+                   (2, 4002, 12288, 1856), (3, 2981, 8192, 1752), (8, 2974, 8192, 288), (2, 2481, 8192, 776)]
+
+
+@pytest.mark.parametrize("t,n,o,k", STREAM_K_SHAPES)
+def test_fused_stream_k_tail_shapes(t, n, o, k):
+    """Integer inputs: the fused GEMM with the stream-K tail (given a contiguous fp32
+    scratch of n x out x 4 >= 32 MiB + 4 KiB) equals the one without it in every element,
+    and the oracle on rows at both ends and both sides of a 256-row tile edge."""
+    assert tp.tp_debug_gemm_plan(n, o, k, segs=t)[:2] == ("pair", 256)
+    x = [synth.int_valued((n, k), -3, 3, 800 + r, device=DEV) for r in range(t)]
+    w = [synth.int_valued((o, k), -3, 3, 820 + r, device=DEV) for r in range(t)]
+    scratch = torch.full((n, o), float("nan"), dtype=torch.float32, device=DEV)
+    y_sk = tp.tp_linear_row(x, w, mode="fused", y_dtype=torch.float32, partials=[scratch] * t)
+    y_plain = tp.tp_linear_row(x, w, mode="fused", y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    assert torch.equal(y_sk, y_plain)
+    rows = sorted({0, 255, 256, n // 2, n - 257, n - 256, n - 1})
+    ref = O.reduce_direct([O.linear(f64(x[r][rows]), f64(w[r])) for r in range(t)])
+    exact(f64(y_sk[rows]), ref)
