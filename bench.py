@@ -385,7 +385,8 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
 
 def _detail_host_overhead(torch, tp, synth, dev):
     """Host cost per call of the C-ABI entry points: from C (a probe program
-    with no Python in the loop) and through the Python binding, both timed on
+    with no Python in the loop), through the Python binding, and through the
+    binding's prepared calls (checks and marshalling done once), all timed on
     the host clock from entry to return, calls enqueued back to back with a
     stream sync every 16 calls so none blocks on the device."""
     out = {}
@@ -410,21 +411,33 @@ def _detail_host_overhead(torch, tp, synth, dev):
         "tp_linear_row_tiny_fused": lambda: tp.tp_linear_row(hs, wds, mode="fused", y=y),
         "tp_mlp_forward_tiny_direct": lambda: tp.tp_mlp_forward(x, wgu, wds, mode="direct", workspace=ws, y=y),
     }
-    py = {}
-    for name, fn in calls.items():
-        for _ in range(20):
-            fn()
-        torch.cuda.synchronize()
-        ts = []
-        for i in range(200):
-            t0 = time.perf_counter()
-            fn()
-            ts.append((time.perf_counter() - t0) * 1e6)
-            if i % 16 == 15:
-                torch.cuda.synchronize()
-        torch.cuda.synchronize()
-        py[name] = {"host_us_median": statistics.median(ts), "host_us_mean": statistics.fmean(ts)}
-    out["python_binding"] = py
+    prepared = {
+        "tp_shard_reduce_t4_n1": tp.prepare(tp.tp_shard_reduce, parts, out=red, mode="direct"),
+        "tp_linear_col_tiny_gated": tp.prepare(tp.tp_linear_col, x, wgu, act="silu", y=hs),
+        "tp_linear_row_tiny_fused": tp.prepare(tp.tp_linear_row, hs, wds, mode="fused", y=y),
+        "tp_mlp_forward_tiny_direct": tp.prepare(tp.tp_mlp_forward, x, wgu, wds, mode="direct", workspace=ws, y=y),
+    }
+
+    def host_times(fns):
+        res = {}
+        for name, fn in fns.items():
+            for _ in range(20):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for i in range(200):
+                t0 = time.perf_counter()
+                fn()
+                ts.append((time.perf_counter() - t0) * 1e6)
+                if i % 16 == 15:
+                    torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            res[name] = {"host_us_median": statistics.median(ts), "host_us_mean": statistics.fmean(ts)}
+        return res
+
+    out["python_binding"] = host_times(calls)
+    # the same calls checked and marshalled once (tp.prepare), then made again and again
+    out["python_prepared"] = host_times(prepared)
     return out
 
 

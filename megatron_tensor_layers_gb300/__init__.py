@@ -8,9 +8,11 @@ is the Python binding of that ABI; the kernels are in ``csrc/``.
 """
 
 from ._lib import (  # noqa: F401
+    PreparedCall,
     TPError,
     lm_head_sharded,
     load,
+    prepare,
     tp_abi_version,
     tp_collective_count,
     tp_debug_expire_wait,

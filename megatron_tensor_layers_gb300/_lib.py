@@ -119,7 +119,8 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 # call only, so each thread reuses a small ring of arrays instead of building
 # new ctypes objects on every call (a call passes at most three lists).  An
 # array returned by _ptrs is therefore valid only until this thread's next
-# _PTR_RING calls of _ptrs: pass it straight to the C function.
+# _PTR_RING calls of _ptrs: pass it straight to the C function.  While
+# `prepare` records a call, every array is new (the recording keeps it).
 _PTR_RING = 8
 _tls = threading.local()
 
@@ -128,7 +129,7 @@ def _ptrs(ts: Optional[Sequence[Optional[torch.Tensor]]]):
     if ts is None:
         return None
     n = len(ts)
-    if n > MAX_SHARDS:
+    if n > MAX_SHARDS or getattr(_tls, "rec", None) is not None:   # a recorded call keeps its own array
         arr = (ctypes.c_void_p * n)()
     else:
         ring = getattr(_tls, "ring", None)
@@ -151,6 +152,86 @@ def _dt(dtype) -> int:
     if dtype not in DTYPES:
         raise TypeError(f"unsupported dtype {dtype}")
     return DTYPES[dtype]
+
+
+# ----------------------------------------------------------------- launches and prepared calls
+#
+# Every entry point below checks its arguments, marshals them and then makes
+# its C calls through _launch.  A serving loop makes the same calls on the same
+# buffers step after step, and in Python the checks and the marshalling cost
+# several times what the C ABI itself does.  `prepare(entry, ...)` runs an
+# entry point once with its launches recorded instead of made; the returned
+# PreparedCall then makes exactly those C calls, with arguments converted to
+# ctypes objects once, each time it is called.
+
+
+def _launch(name: str, *args) -> None:
+    rec = getattr(_tls, "rec", None)
+    fn = getattr(load(), name)
+    if rec is not None:
+        rec.append((name, fn, args))
+        return
+    code = fn(*args)
+    if code != TP_OK:
+        raise TPError(name, code)
+
+
+def _frozen(name: str, fn, args):
+    """A fresh handle of C function `name` that does no argument conversion,
+    and `args` converted once to ctypes objects of the declared types (ctypes
+    arrays pass as pointers to their first element, None as a null pointer)."""
+    if len(fn.argtypes) != len(args):
+        raise TypeError(f"{name} takes {len(fn.argtypes)} arguments, {len(args)} were recorded")
+    raw = load()[name]
+    raw.restype = fn.restype
+    return name, raw, tuple(a if isinstance(a, ctypes.Array) else ty(a) for ty, a in zip(fn.argtypes, args))
+
+
+class PreparedCall:
+    """An entry point's C calls with their arguments checked and marshalled once.
+
+    Calling it makes the same calls again, on the stream that was current (or
+    given) when it was prepared, and returns what the entry point returned then
+    (the same output tensors).  It keeps the tensors it was prepared with alive;
+    their contents may change between calls (that is the use: new inputs written
+    into the same buffers), but their storage must not be replaced or resized.
+    Ownership, layout and error behaviour are those of the entry point: a C call
+    that fails raises TPError, and later calls of the same PreparedCall are not
+    made."""
+
+    __slots__ = ("_calls", "_keep", "result")
+
+    def __init__(self, calls, keep, result):
+        self._calls = tuple(_frozen(name, fn, args) for name, fn, args in calls)
+        self._keep = keep
+        self.result = result
+
+    def __call__(self):
+        for name, raw, args in self._calls:
+            code = raw(*args)
+            if code != TP_OK:
+                raise TPError(name, code)
+        return self.result
+
+    def __len__(self) -> int:
+        return len(self._calls)
+
+
+def prepare(entry, *args, **kwargs) -> PreparedCall:
+    """Check and marshal `entry(*args, **kwargs)` (an entry point of this
+    module) once, without launching anything, and return the PreparedCall that
+    launches it.  Outputs the entry point would allocate are allocated now."""
+    if getattr(_tls, "rec", None) is not None:
+        raise RuntimeError("prepare() does not nest")
+    rec = []
+    _tls.rec = rec
+    try:
+        result = entry(*args, **kwargs)
+    finally:
+        _tls.rec = None
+    if not rec:
+        raise ValueError(f"{getattr(entry, '__name__', entry)!s} made no launch to prepare")
+    return PreparedCall(rec, (args, kwargs), result)
 
 
 # ----------------------------------------------------------------- argument checks
@@ -295,9 +376,8 @@ def tp_linear_col(x: torch.Tensor, w: Sequence[torch.Tensor], *, act: str = "non
         if yi.dtype is not ys[0].dtype:
             raise TypeError("every y[r] must have the same dtype")
     _on_gpu(x, w, bias, ys)
-    code = load().tp_linear_col(t, n, k, out_full, _ptr(x), _ld(x), _ptrs(w), ldw, _ptrs(bias),
-                                ACTS[act], int(gather_output), _ptrs(ys), ldy, _dt(ys[0].dtype), _stream(stream))
-    _check("tp_linear_col", code)
+    _launch("tp_linear_col", t, n, k, out_full, _ptr(x), _ld(x), _ptrs(w), ldw, _ptrs(bias),
+            ACTS[act], int(gather_output), _ptrs(ys), ldy, _dt(ys[0].dtype), _stream(stream))
     return y
 
 
@@ -333,11 +413,10 @@ def tp_linear_row(x: Sequence[torch.Tensor], w: Sequence[torch.Tensor], *, bias:
     _on_gpu(x, w, bias, partials, y)
     ldp = _ld(partials[0]) if partials is not None else out
     pdt = partials[0].dtype if partials is not None else partial_dtype
-    code = load().tp_linear_row(t, n, ks * t, out, _ptrs(x), ldx, _ptrs(w), ldw, _ptr(bias),
-                                int(reduce_results), MODES[mode], _dt(pdt), _ptrs(partials), ldp,
-                                _ptr(y), _ld(y) if y is not None else out, _dt(y.dtype) if y is not None else 0,
-                                _stream(stream))
-    _check("tp_linear_row", code)
+    _launch("tp_linear_row", t, n, ks * t, out, _ptrs(x), ldx, _ptrs(w), ldw, _ptr(bias),
+            int(reduce_results), MODES[mode], _dt(pdt), _ptrs(partials), ldp,
+            _ptr(y), _ld(y) if y is not None else out, _dt(y.dtype) if y is not None else 0,
+            _stream(stream))
     return y if reduce_results else partials
 
 
@@ -360,10 +439,9 @@ def tp_shard_reduce(partials: Sequence[torch.Tensor], *, out: Optional[torch.Ten
         if out.numel() != p0.numel():
             raise ValueError(f"out holds {out.numel()} elements, the partials {p0.numel()}")
     _on_gpu(partials, out)
-    code = load().tp_shard_reduce(t, p0.numel(), _dt(p0.dtype), _ptrs(partials), _ptr(out),
-                                  _dt(out.dtype) if out is not None else 0, MODES[mode], _dt(hop_dtype),
-                                  int(replicate), _stream(stream))
-    _check("tp_shard_reduce", code)
+    _launch("tp_shard_reduce", t, p0.numel(), _dt(p0.dtype), _ptrs(partials), _ptr(out),
+            _dt(out.dtype) if out is not None else 0, MODES[mode], _dt(hop_dtype),
+            int(replicate), _stream(stream))
     return out
 
 
@@ -407,10 +485,9 @@ def tp_mlp_forward(x: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_down: S
     _dense("workspace", workspace)
     _dense("y", y, (n, h), BF16_F32)
     _on_gpu(x, w_gate_up, w_down, bias_down, workspace, y)
-    code = load().tp_mlp_forward(t, n, h, f, _ptr(x), _ld(x), _ptrs(w_gate_up), _ptrs(w_down), _ld(w_down[0]),
-                                 _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype), _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(), _ptr(y), _dt(y.dtype), _stream(stream))
-    _check("tp_mlp_forward", code)
+    _launch("tp_mlp_forward", t, n, h, f, _ptr(x), _ld(x), _ptrs(w_gate_up), _ptrs(w_down), _ld(w_down[0]),
+            _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(y), _dt(y.dtype), _stream(stream))
     return y
 
 
@@ -444,9 +521,8 @@ def vocab_parallel_embed(ids: torch.Tensor, table: Sequence[Optional[torch.Tenso
         for r in range(t):
             _dense(("partials", r), partials[r], (n, h), (ref.dtype,))
     _on_gpu(ids, table, out, partials)
-    code = load().vocab_parallel_embed(t, vocab, h, _ptr(ids), n, _ptrs(table), _dt(ref.dtype), _ptr(out),
-                                       _ptrs(partials), _stream(stream))
-    _check("vocab_parallel_embed", code)
+    _launch("vocab_parallel_embed", t, vocab, h, _ptr(ids), n, _ptrs(table), _dt(ref.dtype), _ptr(out),
+            _ptrs(partials), _stream(stream))
     return out
 
 
@@ -473,17 +549,15 @@ def lm_head_sharded(x: torch.Tensor, table: Sequence[Optional[torch.Tensor]], vo
         for r in range(t):
             _dense(("shard_logits", r), shard_logits[r], (n, widths[r]), (shard_logits[0].dtype,) if r else BF16_F32)
         _on_gpu(x, table, shard_logits)
-        code = load().lm_head_sharded(t, n, h, vocab, _ptr(x), _ld(x), _ptrs(table), None, 0,
-                                      _ptrs(shard_logits), _dt(shard_logits[0].dtype), _stream(stream))
-        _check("lm_head_sharded", code)
+        _launch("lm_head_sharded", t, n, h, vocab, _ptr(x), _ld(x), _ptrs(table), None, 0,
+                _ptrs(shard_logits), _dt(shard_logits[0].dtype), _stream(stream))
         return shard_logits
     if logits is None:
         logits = torch.empty((n, vocab), dtype=out_dtype, device=x.device)
     _matrix("logits", logits, (n, vocab), BF16_F32)
     _on_gpu(x, table, logits)
-    code = load().lm_head_sharded(t, n, h, vocab, _ptr(x), _ld(x), _ptrs(table), _ptr(logits), _ld(logits),
-                                  None, _dt(logits.dtype), _stream(stream))
-    _check("lm_head_sharded", code)
+    _launch("lm_head_sharded", t, n, h, vocab, _ptr(x), _ld(x), _ptrs(table), _ptr(logits), _ld(logits),
+            None, _dt(logits.dtype), _stream(stream))
     return logits
 
 
@@ -503,8 +577,7 @@ def tp_shard_gather(shards: Sequence[torch.Tensor], *, out: Optional[torch.Tenso
         out = torch.empty((rows, sum(s.shape[1] for s in shards)), dtype=shards[0].dtype, device=shards[0].device)
     _dense("out", out, (rows, sum(s.shape[1] for s in shards)), (s0.dtype,))
     _on_gpu(shards, out)
-    code = load().tp_shard_gather(t, rows, cols, _dt(shards[0].dtype), _ptrs(shards), _ptr(out), _stream(stream))
-    _check("tp_shard_gather", code)
+    _launch("tp_shard_gather", t, rows, cols, _dt(shards[0].dtype), _ptrs(shards), _ptr(out), _stream(stream))
     return out
 
 
@@ -565,10 +638,9 @@ def tp_mlp_forward_static(x: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_
         y = torch.empty((n, h), dtype=y_dtype, device=x.device)
     _dense("y", y, (n, h), BF16_F32)
     _on_gpu(x, w_gate_up, w_down, bias_down, y)
-    code = load().tp_mlp_forward_static(t, n, h, f, _ptr(x), _ld(x), _ptrs(w_gate_up), _ptrs(w_down),
-                                        _ld(w_down[0]), _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype),
-                                        _ptr(y), _dt(y.dtype), _stream(stream))
-    _check("tp_mlp_forward_static", code)
+    _launch("tp_mlp_forward_static", t, n, h, f, _ptr(x), _ld(x), _ptrs(w_gate_up), _ptrs(w_down),
+            _ld(w_down[0]), _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype),
+            _ptr(y), _dt(y.dtype), _stream(stream))
     return y
 
 
@@ -591,11 +663,10 @@ def tp_mlp_forward_host(x_host: torch.Tensor, w_gate_up: Sequence[torch.Tensor],
     _on_gpu(x_dev, w_gate_up, w_down, bias_down, y_dev, workspace)
     if copy_stream is None:
         copy_stream = torch.cuda.Stream(device=x_dev.device)
-    code = load().tp_mlp_forward_host(t, n, h, f, _ptr(x_host), _ptrs(w_gate_up), _ptrs(w_down), _ld(w_down[0]),
-                                      _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype), _ptr(x_dev),
-                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(y_dev),
-                                      _ptr(y_host), _dt(y_host.dtype), chunks, _stream(stream), _stream(copy_stream))
-    _check("tp_mlp_forward_host", code)
+    _launch("tp_mlp_forward_host", t, n, h, f, _ptr(x_host), _ptrs(w_gate_up), _ptrs(w_down), _ld(w_down[0]),
+            _ptr(bias_down), ACTS[act], MODES[mode], _dt(partial_dtype), _ptr(x_dev),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(y_dev),
+            _ptr(y_host), _dt(y_host.dtype), chunks, _stream(stream), _stream(copy_stream))
     return y_host
 
 
@@ -623,8 +694,7 @@ def tp_reduce_scatter_rmsnorm(partials: Sequence[torch.Tensor], weight: torch.Te
         out = torch.empty((n, h), dtype=torch.bfloat16, device=partials[0].device)
     _dense("out", out, (n, h), BF16)
     _on_gpu(partials, weight, residual, residual_out, out)
-    code = load().tp_reduce_scatter_rmsnorm(t, n, h, _dt(partials[0].dtype), _ptrs(partials), _ptr(residual),
-                                            _ptr(weight), eps, MODES[mode], _ptr(residual_out), _ptr(out),
-                                            _stream(stream))
-    _check("tp_reduce_scatter_rmsnorm", code)
+    _launch("tp_reduce_scatter_rmsnorm", t, n, h, _dt(partials[0].dtype), _ptrs(partials), _ptr(residual),
+            _ptr(weight), eps, MODES[mode], _ptr(residual_out), _ptr(out),
+            _stream(stream))
     return residual_out, out
