@@ -1704,25 +1704,27 @@ static tp_status launch_pair(GemmArgs& a, const GemmDesc& d, cudaStream_t stream
         mc = std::min(v, sms / 2);
         if (cached_dev) max_clusters[dev].store(mc, std::memory_order_relaxed);
     }
-    const int clusters = std::min(a.total_tiles, mc);
-    // Stream-K tail (store epilogue, given a workspace): when the last wave of whole tiles would
-    // leave clusters idle, its L tiles are cut into S = clusters / L parts along K, one unit per
-    // cluster, so that wave takes about 1/S of a tile's time.  Each part keeps at least two
-    // groups of K blocks.
+    int clusters = std::min(a.total_tiles, mc);
+    // Stream-K (store epilogue, given a workspace).  When the last wave of whole tiles would leave
+    // pairs idle, its L tiles are cut into S = pairs / L parts along K, one unit per pair, so
+    // that wave takes about 1/S of a tile's time.  When there are fewer tiles than resident
+    // pairs (L = all of them, no whole wave), every tile is cut the same way and the grid grows
+    // to L x S pairs, each running one unit.  Each part keeps at least two groups of K blocks.
     a.sk_first = a.total_tiles;
     a.sk_parts = 1;
-    if (EPI == EPI_STORE && d.sk_ws != nullptr && clusters == mc) {
-        const int waves = a.total_tiles / clusters;
-        const int tail = a.total_tiles - waves * clusters;
+    if (EPI == EPI_STORE && d.sk_ws != nullptr) {
+        const int waves = a.total_tiles / mc;
+        const int tail = a.total_tiles - waves * mc;
         const int kbt = a.k_blocks * d.segs;
-        int parts = tail > 0 ? std::min(std::min(clusters / tail, kSkMaxParts), kbt / (2 * KSUB)) : 1;
+        const int parts = tail > 0 ? std::min(std::min(mc / tail, kSkMaxParts), kbt / (2 * KSUB)) : 1;
         const int64_t slots = static_cast<int64_t>(tail) * (parts - 1);
-        if (waves >= 1 && parts >= 2 && slots <= kSkMaxSlots && slots * 2 * 4 <= static_cast<int64_t>(kSkFlagBytes) &&
+        if (parts >= 2 && slots <= kSkMaxSlots && slots * 2 * 4 <= static_cast<int64_t>(kSkFlagBytes) &&
             kSkFlagBytes + static_cast<size_t>(slots) * kSkSlotBytes <= d.sk_ws_bytes) {
-            a.sk_first = waves * clusters;
+            a.sk_first = waves * mc;
             a.sk_parts = parts;
             a.sk_flags = static_cast<int*>(d.sk_ws);
             a.sk_scratch = reinterpret_cast<float*>(static_cast<char*>(d.sk_ws) + kSkFlagBytes);
+            if (waves == 0) clusters = tail * parts;   // <= mc: every unit's pair is resident
         }
     }
     cfg.gridDim = dim3(2 * clusters, 1, 1);

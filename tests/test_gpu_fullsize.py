@@ -428,3 +428,53 @@ def test_fused_stream_k_tail_shapes(t, n, o, k):
     rows = sorted({0, 255, 256, n // 2, n - 257, n - 256, n - 1})
     ref = O.reduce_direct([O.linear(f64(x[r][rows]), f64(w[r])) for r in range(t)])
     exact(f64(y_sk[rows]), ref)
+
+
+def _integer_mlp(t, n, h, f, seed):
+    """Inputs whose every intermediate is an exact small integer: x in {1, 2}, each gate row
+    sums 16 entries of x (G in [16, 32], where act(G) rounds back to G in bf16), each up row
+    takes 4 entries with signs (|U| <= 8), so H = G U is an integer of at most 256; W_down
+    and the bias are integers in -3..3 and -8..8, and every sum stays below 2^24."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randint(1, 3, (n, h), generator=g).double()
+    rows = torch.arange(f)[:, None]
+    wg = torch.zeros((f, h), dtype=torch.float64)
+    wg[rows, torch.randint(0, h // 16, (f, 1), generator=g) + torch.arange(16)[None, :] * (h // 16)] = 1.0
+    wu = torch.zeros((f, h), dtype=torch.float64)
+    wu[rows, torch.randint(0, h // 4, (f, 1), generator=g) + torch.arange(4)[None, :] * (h // 4)] = \
+        (torch.randint(0, 2, (f, 4), generator=g) * 2 - 1).double()
+    wd = torch.randint(-3, 4, (h, f), generator=g).double()
+    bias = torch.randint(-8, 9, (h,), generator=g).double()
+    return x, wg, wu, wd, bias
+
+
+@pytest.mark.parametrize("t,n,h,f", [(4, 200, 8192, 8192), (2, 129, 4096, 8192), (8, 256, 8192, 16384),
+                                     (4, 256, 6144, 8192), (4, 160, 2048, 4096), (2, 255, 1024, 4096)])
+def test_fused_stream_k_few_tiles_integer_exact(t, n, h, f):
+    """A fused MLP of 129 to 256 tokens: its down GEMM has one 256-row tile by h/256 column
+    tiles, fewer than the resident CTA pairs.  With the workspace's stream-K area every tile
+    is split along K into S = pairs / tiles parts (at most 4: 2 for 32 tiles, 3 for 24, 4 for
+    16 and fewer), one pair each; without it each tile runs whole.  Integer inputs keep
+    every intermediate exact, so both must equal the oracle in every element."""
+    assert tp.tp_debug_gemm_plan(n, h, f // t, segs=t)[:2] == ("pair", 256)
+    x, wg, wu, wd, bias = _integer_mlp(t, n, h, f, 3000 + n + t)
+    ref = O.mlp_sharded_rounded(x.numpy(), wg.numpy(), wu.numpy(), wd.numpy(), t, bias.numpy(), "silu", None)
+    assert all(np.array_equal(hr, np.round(hr)) for hr in ref["h"])
+    assert np.abs(ref["y"]).max() < 2 ** 24
+    fs = f // t
+    wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).to(torch.bfloat16).to(DEV).contiguous()
+           for r in range(t)]
+    wds = [wd[:, r * fs:(r + 1) * fs].to(torch.bfloat16).to(DEV).contiguous() for r in range(t)]
+    xd, bd = x.to(torch.bfloat16).to(DEV), bias.to(torch.bfloat16).to(DEV)
+    full = tp.tp_mlp_workspace_size(t, n, h, f, "fused")
+    base = -(-n * f * 2 // 256) * 256                   # H alone: no stream-K area
+    assert full == base + 32 * 1024 * 1024 + 4096
+    outs = []
+    for size in (full, base):
+        ws = torch.full((size,), 0xAB, dtype=torch.uint8, device=DEV)
+        outs.append(tp.tp_mlp_forward(xd, wgu, wds, bias_down=bd, mode="fused", workspace=ws,
+                                      y_dtype=torch.float32))
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == 0
+    assert torch.equal(outs[0], outs[1])
+    exact(f64(outs[0]), ref["y"])
