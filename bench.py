@@ -307,18 +307,19 @@ def run_ours(args, rank, world, local_rank):
 
     copy_stream = torch.cuda.Stream(device=dev)
     e2e_runs = {}
-    for chunks in (1, 2, 4, 8):
+    for chunks in (1, 2, 3, 4, 8):
         def e2e_step(chunks=chunks):
             tp.tp_mlp_forward_host(xh, wgu, wds, y_host=yh, x_dev=xd, y_dev=y, workspace=ws, mode="direct",
                                    chunks=chunks, stream=stream, copy_stream=copy_stream)
         e2e_runs[chunks] = (time_fn(torch, e2e_step, max(3, args.steps // 10), warm=2)
                             if not args.no_e2e else float("nan"))
     e2e_s = e2e_runs[E2E_CHUNKS]
+    blocks = tp.tp_mlp_host_blocks(N_TOK, E2E_CHUNKS)
     e2e = {"value": FLOPS / e2e_s / 1e12 * world, "unit": "TFLOP/s", "h2d_bytes_per_step": N_TOK * H * 2,
            "d2h_bytes_per_step": N_TOK * H * 2, "ms_per_step": e2e_s * 1e3,
-           "path": (f"pinned host X -> tp_mlp_forward_host (C ABI; chunks={E2E_CHUNKS}: {E2E_CHUNKS + 1} row blocks, "
-                    "the first and last half-height, copies overlapped with compute on a second stream) "
-                    "-> pinned host Y"),
+           "path": (f"pinned host X -> tp_mlp_forward_host (C ABI; chunks={E2E_CHUNKS}: row blocks of "
+                    f"{[b - a for a, b in zip(blocks, blocks[1:])]} tokens, copies overlapped with compute on a "
+                    "second stream) -> pinned host Y"),
            "ms_by_chunks": {str(k): v * 1e3 for k, v in e2e_runs.items()}}
     if args.no_e2e:                     # profiling runs: no end-to-end number (null, not NaN, in the JSON)
         e2e.update({"value": None, "ms_per_step": None, "ms_by_chunks": None})

@@ -232,20 +232,24 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f,
  *   x_host   [n, h] bf16, contiguous, page-locked host memory (read).
  *   y_host   [n, h] of y_dtype, contiguous, page-locked host memory (written).
  *   x_dev    device staging for X, [n, h] bf16; y_dev device [n, h] y_dtype.
- *   workspace  at least tp_mlp_workspace_size(t, ceil(n/chunks), h, f, mode,
- *              partial_dtype) bytes (one row block), 256-byte aligned.
- *   chunks   1..64: the rows are cut into blocks of at most ceil(n/chunks)
- *            rows; with chunks >= 2 the first block has ceil(ceil(n/chunks)/2)
- *            rows, the middle blocks ceil(n/chunks) and the last the rest (so
- *            the exposed first copy and last read-back are about half a
- *            block: n = 8192 in 4 chunks runs as 1024, 2048, 2048, 2048,
- *            1024 rows).  Block i's host->device copy runs on copy_stream
+ *   workspace  at least tp_mlp_workspace_size(t, m, h, f, mode, partial_dtype)
+ *              bytes, m the tallest row block (tp_mlp_host_blocks), 256-byte
+ *              aligned.
+ *   chunks   1..64: 1 runs all rows as one block.  With chunks >= 2 the first
+ *            and the last block have e = ceil(n / (4 chunks)) rows (rounded up
+ *            to a multiple of 128 when at least e rows stay between them), and
+ *            the n - 2e rows between them form chunks - 1 blocks of equal
+ *            height (rounded up to a multiple of 128 where the last of them
+ *            keeps rows; that one takes the rest).  n = 8192 in 2 chunks runs
+ *            as 1024, 6144, 1024 rows; in 4 chunks as 512, 2432, 2432, 2304,
+ *            512.  The exposed first copy and last read-back are the short
+ *            edge blocks'.  Block i's host->device copy runs on copy_stream
  *            under the compute of block i-1, its device->host copy under the
  *            compute of block i+1; the MLPs run on `stream`.
  *   Other arguments as tp_mlp_forward.  When the call returns, all work is
  *   queued and `stream` completes after the last read-back (wait on it).
  * Errors as tp_mlp_forward; TP_ERR_WORKSPACE if the workspace is too small
- * for one block.
+ * for the tallest block.
  */
 tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
                               const void* x_host,
@@ -256,6 +260,16 @@ tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
                               void* x_dev, void* workspace, size_t workspace_bytes,
                               void* y_dev, void* y_host, tp_dtype y_dtype,
                               int chunks, tp_stream stream, tp_stream copy_stream);
+
+/*
+ * The row blocks tp_mlp_forward_host cuts n tokens into with `chunks` (host
+ * logic only, no CUDA call).  Returns the block count k (0 for n = 0), or -1
+ * if n < 0 or chunks is outside 1..64.  When starts is not NULL and
+ * max_blocks >= k, writes the k + 1 boundaries: block b covers rows
+ * [starts[b], starts[b + 1]), starts[0] = 0, starts[k] = n; otherwise writes
+ * nothing (call with NULL first to learn k; k <= chunks + 1).
+ */
+int tp_mlp_host_blocks(int64_t n, int chunks, int64_t* starts, int max_blocks);
 
 /*
  * tp_mlp_forward for callers that cannot allocate device memory.  This entry

@@ -22,6 +22,8 @@ from ._lib import (  # noqa: F401
     tp_mlp_forward,
     tp_mlp_forward_host,
     tp_mlp_forward_static,
+    tp_mlp_host_blocks,
+    tp_mlp_host_workspace_size,
     tp_mlp_workspace_size,
     tp_reduce_scatter_rmsnorm,
     tp_reset_collective_count,

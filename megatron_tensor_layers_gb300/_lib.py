@@ -34,7 +34,7 @@ EXPORTED = [
     "tp_mlp_workspace_size", "tp_mlp_forward", "vocab_parallel_embed", "lm_head_sharded",
     "tp_shard_gather", "tp_device_status", "tp_collective_count", "tp_reset_collective_count",
     "tp_debug_expire_wait", "tp_set_gemm_tile_n", "tp_mlp_forward_static", "tp_set_gemm_cta_pair", "tp_mlp_forward_host",
-    "tp_reduce_scatter_rmsnorm", "tp_set_gemm_split", "tp_debug_gemm_plan",
+    "tp_reduce_scatter_rmsnorm", "tp_set_gemm_split", "tp_debug_gemm_plan", "tp_mlp_host_blocks",
 ]
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -82,6 +82,7 @@ def load() -> ctypes.CDLL:
         "tp_mlp_forward_host": (I32, [I32, I64, I64, I64, P, P, P, I64, P, I32, I32, I32, P, P, ctypes.c_size_t, P, P,
                                       I32, I32, P, P]),
         "tp_mlp_forward_static": (I32, [I32, I64, I64, I64, P, I64, P, P, I64, P, I32, I32, I32, P, I32, P]),
+        "tp_mlp_host_blocks": (I32, [I64, I32, P, I32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -644,13 +645,34 @@ def tp_mlp_forward_static(x: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_
     return y
 
 
+def tp_mlp_host_blocks(n: int, chunks: int) -> List[int]:
+    """Boundaries of the row blocks tp_mlp_forward_host runs n tokens in: block b
+    covers rows [starts[b], starts[b + 1])."""
+    lib = load()
+    k = lib.tp_mlp_host_blocks(n, chunks, None, 0)
+    if k < 0:
+        raise ValueError("n must be >= 0 and chunks in 1..64")
+    starts = (ctypes.c_int64 * (k + 1))()
+    lib.tp_mlp_host_blocks(n, chunks, starts, k)
+    return list(starts)
+
+
+def tp_mlp_host_workspace_size(t: int, n: int, h: int, f: int, chunks: int, mode: str = "direct",
+                               partial_dtype=torch.bfloat16) -> int:
+    """Workspace bytes tp_mlp_forward_host needs: one MLP of its tallest row block."""
+    s = tp_mlp_host_blocks(n, chunks)
+    rows = max((b - a for a, b in zip(s, s[1:])), default=0)
+    return tp_mlp_workspace_size(t, rows, h, f, mode, partial_dtype)
+
+
 def tp_mlp_forward_host(x_host: torch.Tensor, w_gate_up: Sequence[torch.Tensor], w_down: Sequence[torch.Tensor], *,
                         y_host: torch.Tensor, x_dev: torch.Tensor, y_dev: torch.Tensor, workspace: torch.Tensor,
                         bias_down: Optional[torch.Tensor] = None, act: str = "silu", mode: str = "direct",
                         partial_dtype=torch.bfloat16, chunks: int = 2, stream=None, copy_stream=None):
     """tp_mlp_forward on pinned host activations with chunked, overlapped
-    copies (see include/tp.h).  Returns y_host; the work is complete when
-    `stream` is."""
+    copies (see include/tp.h).  The workspace holds one MLP of the tallest
+    row block (tp_mlp_host_workspace_size).  Returns y_host; the work is
+    complete when `stream` is."""
     if not (isinstance(x_host, torch.Tensor) and isinstance(y_host, torch.Tensor)
             and x_host.is_pinned() and y_host.is_pinned()):
         raise ValueError("x_host and y_host must be page-locked host tensors")

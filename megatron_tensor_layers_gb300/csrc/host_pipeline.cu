@@ -1,16 +1,18 @@
 // tp_mlp_forward_host: the tensor-parallel MLP for activations that live in
 // (pinned) host memory, with the copies overlapped with the compute.
 //
-// The n tokens are cut into row blocks of at most ceil(n/chunks) rows.  Block
-// i is copied to the device on `copy_stream`, the MLP of block i runs on
-// `stream` once its copy has landed (an event), and its output is copied back
-// on `copy_stream` once the MLP is done (another event).  All input copies are
-// queued first in order, so the copy of block i+1 runs under the compute of
-// block i and the read-back of block i under the compute of block i+1; only
-// the first input copy and the last read-back are exposed, so with two or more
-// chunks the first and the last block are half as tall as the others
-// (chunks + 1 blocks): n = 8192 in 4 chunks runs as 1024, 2048, 2048, 2048,
-// 1024 rows.  Rows are independent in every
+// The n tokens are cut into row blocks.  Block i is copied to the device on
+// `copy_stream`, the MLP of block i runs on `stream` once its copy has landed
+// (an event), and its output is copied back on `copy_stream` once the MLP is
+// done (another event).  All input copies are queued first in order, so the
+// copy of block i+1 runs under the compute of block i and the read-back of
+// block i under the compute of block i+1; only the first input copy and the
+// last read-back are exposed.  So with two or more chunks the first and the
+// last block are short, about n/(4*chunks) rows, and the rows between them
+// form chunks-1 blocks: n = 8192 in 2 chunks runs as 1024, 6144 and 1024
+// rows.  An MLP row costs far more than copying it (8192 x 28672 weights:
+// about 0.8 us of compute against under 0.1 us of copy), so a short block
+// still hides the next, tall block's copy.  Rows are independent in every
 // step of the MLP (page "6.2 Tensor-parallel inference", §1: each token's
 // output depends on its own row of X only), so splitting by rows changes no
 // result.
@@ -20,6 +22,50 @@
 #include <cstdint>
 
 #include "tp.h"
+
+namespace {
+
+constexpr int kMaxBlocks = 65;   // chunks <= 64: at most chunks + 1 blocks
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// Row-block boundaries: block b covers rows [s[b], s[b + 1]).  Returns the block
+// count (0 for n = 0).  Edges are rounded up to a multiple of 128 rows (the
+// GEMMs' tile height) where the rows between them stay at least as many, and
+// middle blocks where the last of them keeps rows.
+int host_blocks(int64_t n, int chunks, int64_t* s) {
+    s[0] = 0;
+    if (n <= 0) return 0;
+    if (chunks == 1 || n < 3) {
+        s[1] = n;
+        return 1;
+    }
+    int64_t e = (n + 4 * chunks - 1) / (4 * chunks);
+    if (3 * round_up(e, 128) <= n) e = round_up(e, 128);   // the rows between keep at least an edge's height
+    const int64_t m = n - 2 * e;                    // >= 1: e <= ceil(n / 8) < n / 2 for n >= 3
+    const int mb = chunks - 1;
+    int64_t mr = (m + mb - 1) / mb;
+    if (round_up(mr, 128) * (mb - 1) < m) mr = round_up(mr, 128);
+    int k = 0;
+    s[++k] = e;
+    for (int64_t r = e; r < n - e;) {
+        r = std::min(r + mr, n - e);
+        s[++k] = r;
+    }
+    s[++k] = n;
+    return k;
+}
+
+}  // namespace
+
+extern "C" int tp_mlp_host_blocks(int64_t n, int chunks, int64_t* starts, int max_blocks) {
+    if (n < 0 || chunks < 1 || chunks > 64) return -1;
+    int64_t s[kMaxBlocks + 1];
+    const int k = host_blocks(n, chunks, s);
+    if (starts != nullptr && max_blocks >= k)
+        for (int b = 0; b <= k; ++b) starts[b] = s[b];
+    return k;
+}
 
 extern "C" tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f, const void* x_host,
                                          const void* const* w_gate_up, const void* const* w_down, int64_t ld_down,
@@ -31,14 +77,13 @@ extern "C" tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
     if (chunks < 1 || chunks > 64 || n < 0 || h <= 0) return TP_ERR_INVALID_ARG;
     if (y_dtype != TP_BF16 && y_dtype != TP_F32) return TP_ERR_UNSUPPORTED;
     if (n == 0) return TP_OK;
-    const int64_t rows = (n + chunks - 1) / chunks;          // the tallest block
-    // block b covers rows [start(b), start(b + 1)): a half-height first block, then blocks of
-    // `rows`, the rest (at most `rows`, about half) last
-    const int64_t first = chunks > 1 ? std::min<int64_t>((rows + 1) / 2, n) : n;
-    const int nblk = first >= n ? 1 : 1 + static_cast<int>((n - first + rows - 1) / rows);
-    auto start = [&](int b) -> int64_t { return b == 0 ? 0 : std::min<int64_t>(n, first + (b - 1) * rows); };
-    // The workspace must hold one block's MLP; validate the arguments with it
-    // before anything is queued.
+    int64_t bounds[kMaxBlocks + 1];
+    const int nblk = host_blocks(n, chunks, bounds);
+    auto start = [&](int b) -> int64_t { return bounds[b]; };
+    int64_t rows = 0;                                          // the tallest block
+    for (int b = 0; b < nblk; ++b) rows = std::max(rows, bounds[b + 1] - bounds[b]);
+    // The workspace must hold the tallest block's MLP; validate the arguments
+    // with it before anything is queued.
     const size_t need = tp_mlp_workspace_size(t, rows, h, f, mode, partial_dtype);
     if (need == 0) return TP_ERR_INVALID_ARG;
     if (workspace_bytes < need) return TP_ERR_WORKSPACE;
@@ -47,7 +92,7 @@ extern "C" tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaStream_t cp = reinterpret_cast<cudaStream_t>(copy_stream);
 
-    cudaEvent_t in_ready[66], out_ready[66];
+    cudaEvent_t in_ready[kMaxBlocks], out_ready[kMaxBlocks];
     int created = 0;
     tp_status st = TP_OK;
     for (; created < nblk; ++created) {

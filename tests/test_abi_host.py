@@ -128,9 +128,45 @@ def test_host_pipeline_rejects_on_host(lib):
                                    FAKE, 0, 1, None, None) == 1
     assert lib.tp_mlp_forward_host(2, 8, 64, 128, FAKE, two, two, 64, None, 1, 0, 0, FAKE, FAKE, 1 << 20, FAKE,
                                    FAKE, 0, 0, None, None) == 1
-    # a workspace smaller than one row block
+    # a workspace smaller than the tallest row block
     assert lib.tp_mlp_forward_host(2, 8, 64, 128, FAKE, two, two, 64, None, 1, 0, 0, FAKE, FAKE, 16, FAKE,
                                    FAKE, 0, 2, None, None) == 7
+
+
+def test_host_blocks(lib):
+    """The row blocks of tp_mlp_forward_host (host logic): short first and last blocks of
+    e = ceil(n / (4 chunks)) rows, rounded up to 128 while at least e rows stay between them,
+    and chunks - 1 middle blocks of equal height, rounded up to 128 while the last of them
+    keeps rows."""
+    def sizes(n, c):
+        s = _lib.tp_mlp_host_blocks(n, c)
+        return [b - a for a, b in zip(s, s[1:])]
+    assert sizes(8192, 1) == [8192]
+    assert sizes(8192, 2) == [1024, 6144, 1024]
+    assert sizes(8192, 3) == [768, 3328, 3328, 768]
+    assert sizes(8192, 4) == [512, 2432, 2432, 2304, 512]
+    assert sizes(520, 2) == [128, 264, 128]          # ceil(520 / 8) = 65 -> 128
+    assert sizes(40, 5) == [2, 9, 9, 9, 9, 2]        # 128-row edges would leave no middle
+    assert sizes(257, 2) == [33, 191, 33]            # nor here more than one row
+    assert sizes(3, 2) == [1, 1, 1] and sizes(2, 2) == [2] and sizes(1, 64) == [1] and sizes(0, 2) == []
+    for n in (1, 2, 3, 7, 100, 129, 255, 256, 257, 1000, 4099, 8192, 70001):
+        for c in (1, 2, 3, 5, 8, 17, 64):
+            s = _lib.tp_mlp_host_blocks(n, c)
+            b = [y - x for x, y in zip(s, s[1:])]
+            assert s[0] == 0 and s[-1] == n and all(v > 0 for v in b), (n, c)
+            assert len(b) <= c + 1, (n, c)
+            if c > 1 and n >= 3:
+                e = -(-n // (4 * c))
+                assert len(b) >= 3 and b[0] == b[-1] and b[0] in (e, -(-e // 128) * 128), (n, c)
+                assert sum(b[1:-1]) >= b[0] and max(b[1:-1]) - min(b[1:-2] or b[1:2]) <= 128, (n, c)
+    # the C query: the count with no buffer, nothing written when the buffer is short, -1 on bad input
+    assert lib.tp_mlp_host_blocks(8192, 2, None, 0) == 3
+    buf = (ctypes.c_int64 * 4)(-1, -1, -1, -1)
+    assert lib.tp_mlp_host_blocks(8192, 2, buf, 2) == 3 and list(buf) == [-1] * 4
+    assert lib.tp_mlp_host_blocks(8192, 2, buf, 3) == 3 and list(buf) == [0, 1024, 7168, 8192]
+    assert lib.tp_mlp_host_blocks(-1, 2, None, 0) == -1
+    assert lib.tp_mlp_host_blocks(8, 0, None, 0) == -1 and lib.tp_mlp_host_blocks(8, 65, None, 0) == -1
+    assert _lib.tp_mlp_host_workspace_size(4, 8192, 8192, 28672, 2) == _lib.tp_mlp_workspace_size(4, 6144, 8192, 28672)
 
 
 def test_gemm_kernel_choice(lib):

@@ -630,8 +630,8 @@ def test_mlp_forward_host_matches_device_entry_point(chunks):
     xh = torch.empty((n, h), dtype=torch.bfloat16, pin_memory=True)
     xh.copy_(x)
     yh = torch.full((n, h), float("nan"), dtype=torch.float32, pin_memory=True)
-    rows = (n + chunks - 1) // chunks
-    ws = torch.empty(tp.tp_mlp_workspace_size(t, rows, h, f, "direct", torch.float32), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(tp.tp_mlp_host_workspace_size(t, n, h, f, chunks, "direct", torch.float32), dtype=torch.uint8,
+                     device=DEV)
     xd = torch.empty_like(x)
     yd = torch.empty((n, h), dtype=torch.float32, device=DEV)
     tp.tp_mlp_forward_host(xh, wgu, wds, y_host=yh, x_dev=xd, y_dev=yd, workspace=ws, mode="direct",
@@ -640,14 +640,13 @@ def test_mlp_forward_host_matches_device_entry_point(chunks):
     got = O.f32_bits_to_f64(yh.view(torch.int32).numpy().view(np.uint32))
     # rows are independent and every kernel choice depends only on the block's shape, so
     # the host-buffer path gives the device entry point's bits where the blocks match:
-    # one block, or with two or more chunks a half-height first block, blocks of
-    # ceil(n/chunks) rows, and the rest last
+    # one block, or with two or more chunks short first and last blocks around chunks - 1
+    # taller ones
     if chunks == 1:
         assert torch.equal(yh.to(DEV), y_dev)
     else:
-        first = (rows + 1) // 2
-        bounds = [0, first] + list(range(first + rows, n, rows)) + [n]
-        assert all(0 < b - a <= rows for a, b in zip(bounds, bounds[1:]))
+        bounds = tp.tp_mlp_host_blocks(n, chunks)
+        assert len(bounds) == chunks + 2 and bounds[1] == n - bounds[-2] == 128
         for a, b in zip(bounds, bounds[1:]):
             yb = tp.tp_mlp_forward(x[a:b], wgu, wds, mode="direct", partial_dtype=torch.float32,
                                    y_dtype=torch.float32)
@@ -667,8 +666,8 @@ def test_mlp_forward_host_small_blocks(n, chunks, mode):
     wg, wu, wd = normal((f, h), 0.02, 251), normal((f, h), 0.02, 252), normal((h, f), 0.02, 253)
     wgu = [torch.cat([wg[r * fs:(r + 1) * fs], wu[r * fs:(r + 1) * fs]]).contiguous() for r in range(t)]
     wds = [wd[:, r * fs:(r + 1) * fs] for r in range(t)]
-    rows = (n + chunks - 1) // chunks
-    ws = torch.empty(tp.tp_mlp_workspace_size(t, rows, h, f, mode, torch.float32), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(tp.tp_mlp_host_workspace_size(t, n, h, f, chunks, mode, torch.float32), dtype=torch.uint8,
+                     device=DEV)
     xh = torch.empty((n, h), dtype=torch.bfloat16, pin_memory=True)
     xh.copy_(x)
     yh = torch.full((n, h), float("nan"), dtype=torch.float32, pin_memory=True)
@@ -678,9 +677,8 @@ def test_mlp_forward_host_small_blocks(n, chunks, mode):
                            partial_dtype=torch.float32, chunks=chunks)
     torch.cuda.current_stream().synchronize()
     assert tp.tp_device_status() == 0
-    first = (rows + 1) // 2 if chunks > 1 else n
-    bounds = [0] + ([first] if first < n else []) + list(range(first + rows, n, rows)) + [n]
-    bounds = sorted(set(bounds))
+    bounds = tp.tp_mlp_host_blocks(n, chunks)
+    assert bounds[0] == 0 and bounds[-1] == n and len(bounds) <= chunks + 2
     for a, b in zip(bounds, bounds[1:]):
         yb = tp.tp_mlp_forward(x[a:b], wgu, wds, mode=mode, partial_dtype=torch.float32, y_dtype=torch.float32,
                                workspace=ws)

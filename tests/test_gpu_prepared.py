@@ -106,8 +106,8 @@ def test_prepared_mlp_forward_host():
         return {"y_host": torch.empty((n, h), dtype=torch.float32).pin_memory(),
                 "x_dev": torch.empty((n, h), dtype=torch.bfloat16, device=DEV),
                 "y_dev": torch.empty((n, h), dtype=torch.float32, device=DEV),
-                "workspace": torch.empty(tp.tp_mlp_workspace_size(t, (n + 1) // 2, h, f, "direct"),
-                                         dtype=torch.uint8, device=DEV)}
+                "workspace": torch.empty(tp.tp_mlp_host_workspace_size(t, n, h, f, 2), dtype=torch.uint8,
+                                         device=DEV)}
 
     x_host = torch.empty((n, h), dtype=torch.bfloat16).pin_memory()
     mine = buffers()
