@@ -7,8 +7,10 @@ parallelism.  Only the test suite, ``__graft_entry__.smoke()`` and the
 The CUDA library never imports, links or calls anything here, and nothing
 here imports the CUDA library: the two sides share no code.
 
-Functions whose results are not pinned by an independent check say
-"parity unpinned" in their docstring.
+Every function is pinned by checks independent of it (tests/test_oracle_pins.py:
+the pages' worked examples, closed forms, brute force on small integers and
+library routines); a function without such a pin would say "parity unpinned"
+in its docstring, and none does.
 """
 
 from .tp_oracle import *  # noqa: F401,F403

@@ -256,8 +256,8 @@ def gelu_tanh(x: np.ndarray) -> np.ndarray:
 def glu(gate: np.ndarray, up: np.ndarray, act: str) -> np.ndarray:
     """The gated activation between the two MLP matmuls: act(gate) * up
     (tp.py TPMLP: silu(gate_proj(x)) * up_proj(x)).  act is "silu" or
-    "gelu_tanh" (the latter is an option; "parity unpinned" beyond its
-    closed-form identities)."""
+    "gelu_tanh" (the latter an option of this library; both activations are
+    pinned to torch's own and to closed-form identities)."""
     if act == "silu":
         return silu(gate) * up
     if act == "gelu_tanh":
