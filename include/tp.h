@@ -264,10 +264,11 @@ tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
 /*
  * The row blocks tp_mlp_forward_host cuts n tokens into with `chunks` (host
  * logic only, no CUDA call).  Returns the block count k (0 for n = 0), or -1
- * if n < 0 or chunks is outside 1..64.  When starts is not NULL and
- * max_blocks >= k, writes the k + 1 boundaries: block b covers rows
- * [starts[b], starts[b + 1]), starts[0] = 0, starts[k] = n; otherwise writes
- * nothing (call with NULL first to learn k; k <= chunks + 1).
+ * if n < 0 or chunks is outside 1..64.  starts is NULL or a host array of
+ * max_blocks + 1 entries; when it is not NULL and max_blocks >= k, the call
+ * writes the k + 1 boundaries: block b covers rows [starts[b], starts[b + 1]),
+ * starts[0] = 0, starts[k] = n.  Otherwise it writes nothing (call with NULL
+ * first to learn k; k <= chunks + 1).
  */
 int tp_mlp_host_blocks(int64_t n, int chunks, int64_t* starts, int max_blocks);
 
