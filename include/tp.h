@@ -40,6 +40,10 @@
  *    are captured into CUDA graphs like any other.
  *  - Nothing here is thread-safe against concurrent calls that share output
  *    buffers; calls on different streams with disjoint buffers are fine.
+ *  - Zero tokens (n = 0, or count / rows = 0) is a valid call: every other
+ *    argument is checked as usual, the pointers to data of zero rows (x, y,
+ *    partials, out, logits, shard_logits, ids, residual, the host buffers)
+ *    may be NULL, and the call returns TP_OK without any CUDA call.
  */
 #ifndef TP_GB300_H
 #define TP_GB300_H

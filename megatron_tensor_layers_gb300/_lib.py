@@ -674,7 +674,7 @@ def tp_mlp_forward_host(x_host: torch.Tensor, w_gate_up: Sequence[torch.Tensor],
     row block (tp_mlp_host_workspace_size).  Returns y_host; the work is
     complete when `stream` is."""
     if not (isinstance(x_host, torch.Tensor) and isinstance(y_host, torch.Tensor)
-            and x_host.is_pinned() and y_host.is_pinned()):
+            and (x_host.numel() == 0 or x_host.is_pinned()) and (y_host.numel() == 0 or y_host.is_pinned())):
         raise ValueError("x_host and y_host must be page-locked host tensors")
     t, n, h, f = _mlp_args(x_dev, w_gate_up, w_down, bias_down, act, mode)
     _dense("x_host", x_host, (n, h), BF16)

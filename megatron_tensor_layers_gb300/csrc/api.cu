@@ -106,7 +106,7 @@ tp_status tp_linear_col(int t, int64_t n, int64_t in, int64_t out_full, const vo
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
     TP_CHECK(n >= 0 && in > 0 && out_full > 0, TP_ERR_INVALID_ARG);
     TP_CHECK(n <= INT32_MAX && out_full <= INT32_MAX && in <= INT32_MAX, TP_ERR_INVALID_ARG);
-    TP_CHECK(x != nullptr && w != nullptr && y != nullptr, TP_ERR_INVALID_ARG);
+    TP_CHECK((x != nullptr || n == 0) && w != nullptr && y != nullptr, TP_ERR_INVALID_ARG);
     TP_CHECK(act == TP_ACT_NONE || act == TP_ACT_SILU_MUL || act == TP_ACT_GELU_TANH_MUL, TP_ERR_INVALID_ARG);
     TP_CHECK(gather_output == 0 || gather_output == 1, TP_ERR_INVALID_ARG);
     TP_CHECK(dtype_ok(y_dtype), TP_ERR_UNSUPPORTED);
@@ -123,7 +123,7 @@ tp_status tp_linear_col(int t, int64_t n, int64_t in, int64_t out_full, const vo
         TP_CHECK(al16(w[r]), TP_ERR_ALIGNMENT);
         if (bias != nullptr) TP_CHECK(bias[r] != nullptr, TP_ERR_INVALID_ARG);
         if (!gather_output || r == 0) {
-            TP_CHECK(y[r] != nullptr, TP_ERR_INVALID_ARG);
+            TP_CHECK(y[r] != nullptr || n == 0, TP_ERR_INVALID_ARG);
             TP_CHECK(al16(y[r]), TP_ERR_ALIGNMENT);
         }
     }
@@ -164,12 +164,12 @@ static tp_status shard_reduce_impl(int t, int64_t count, tp_dtype dtype, const v
     TP_CHECK(count >= 0 && partials != nullptr, TP_ERR_INVALID_ARG);
     TP_CHECK(mode == TP_REDUCE_DIRECT || mode == TP_REDUCE_RING, TP_ERR_INVALID_ARG);
     TP_CHECK(replicate == 0 || replicate == 1, TP_ERR_INVALID_ARG);
-    TP_CHECK(out != nullptr || replicate, TP_ERR_INVALID_ARG);
+    TP_CHECK(out != nullptr || replicate || count == 0, TP_ERR_INVALID_ARG);
     TP_CHECK(dtype_ok(dtype) && dtype_ok(hop_dtype), TP_ERR_UNSUPPORTED);
     TP_CHECK(out == nullptr || dtype_ok(out_dtype), TP_ERR_UNSUPPORTED);
     TP_CHECK(!(hop_dtype == TP_BF16 && dtype != TP_BF16), TP_ERR_UNSUPPORTED);
     for (int r = 0; r < t; ++r) {
-        TP_CHECK(partials[r] != nullptr, TP_ERR_INVALID_ARG);
+        TP_CHECK(partials[r] != nullptr || count == 0, TP_ERR_INVALID_ARG);
         TP_CHECK(al16(partials[r]), TP_ERR_ALIGNMENT);
     }
     TP_CHECK(out == nullptr || al16(out), TP_ERR_ALIGNMENT);
@@ -226,17 +226,17 @@ static tp_status linear_row_impl(int t, int64_t n, int64_t in_full, int64_t out,
         if (reduce_results) TP_CHECK(ldp == out, TP_ERR_UNSUPPORTED);   // the reduce streams contiguous partials
     }
     if (reduce_results) {
-        TP_CHECK(y != nullptr, TP_ERR_INVALID_ARG);
+        TP_CHECK(y != nullptr || n == 0, TP_ERR_INVALID_ARG);
         TP_CHECK(dtype_ok(y_dtype), TP_ERR_UNSUPPORTED);
         TP_CHECK(al16(y), TP_ERR_ALIGNMENT);
         TP_CHECK(ldy >= out, TP_ERR_INVALID_ARG);
         if (!fused) TP_CHECK(ldy == out, TP_ERR_UNSUPPORTED);
     }
     for (int r = 0; r < t; ++r) {
-        TP_CHECK(x[r] != nullptr && w[r] != nullptr, TP_ERR_INVALID_ARG);
+        TP_CHECK((x[r] != nullptr || n == 0) && w[r] != nullptr, TP_ERR_INVALID_ARG);
         TP_CHECK(al16(x[r]) && al16(w[r]), TP_ERR_ALIGNMENT);
         if (!fused) {
-            TP_CHECK(partials[r] != nullptr, TP_ERR_INVALID_ARG);
+            TP_CHECK(partials[r] != nullptr || n == 0, TP_ERR_INVALID_ARG);
             TP_CHECK(al16(partials[r]), TP_ERR_ALIGNMENT);
         }
     }
@@ -316,7 +316,8 @@ tp_status tp_mlp_forward(int t, int64_t n, int64_t h, int64_t f, const void* x, 
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
     TP_CHECK(n >= 0 && h > 0 && f > 0, TP_ERR_INVALID_ARG);
     TP_CHECK(n <= INT32_MAX && h <= INT32_MAX && f <= INT32_MAX, TP_ERR_INVALID_ARG);
-    TP_CHECK(x != nullptr && w_gate_up != nullptr && w_down != nullptr && y != nullptr, TP_ERR_INVALID_ARG);
+    TP_CHECK((x != nullptr || n == 0) && w_gate_up != nullptr && w_down != nullptr && (y != nullptr || n == 0),
+             TP_ERR_INVALID_ARG);
     TP_CHECK(act == TP_ACT_SILU_MUL || act == TP_ACT_GELU_TANH_MUL, TP_ERR_INVALID_ARG);
     TP_CHECK(mode == TP_REDUCE_DIRECT || mode == TP_REDUCE_RING || mode == TP_REDUCE_FUSED, TP_ERR_INVALID_ARG);
     TP_CHECK(dtype_ok(partial_dtype) && dtype_ok(y_dtype), TP_ERR_UNSUPPORTED);
@@ -417,7 +418,7 @@ tp_status vocab_parallel_embed(int t, int64_t vocab, int64_t h, const int32_t* i
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
     TP_CHECK(vocab > 0 && vocab <= INT32_MAX && h > 0 && h <= INT32_MAX && n >= 0, TP_ERR_INVALID_ARG);
     TP_CHECK(n <= static_cast<int64_t>(INT32_MAX) * 4, TP_ERR_INVALID_ARG);   // one warp per id, four per block
-    TP_CHECK(table != nullptr && out != nullptr && (ids != nullptr || n == 0), TP_ERR_INVALID_ARG);
+    TP_CHECK(table != nullptr && ((out != nullptr && ids != nullptr) || n == 0), TP_ERR_INVALID_ARG);
     TP_CHECK(dtype_ok(dtype), TP_ERR_UNSUPPORTED);
     TP_CHECK((h * esize(dtype)) % 16 == 0, TP_ERR_ALIGNMENT);
     TP_CHECK(al16(out), TP_ERR_ALIGNMENT);
@@ -441,7 +442,7 @@ tp_status vocab_parallel_embed(int t, int64_t vocab, int64_t h, const int32_t* i
         }
         d.table[r] = table[r];
         if (partials != nullptr) {
-            TP_CHECK(partials[r] != nullptr, TP_ERR_INVALID_ARG);
+            TP_CHECK(partials[r] != nullptr || n == 0, TP_ERR_INVALID_ARG);
             TP_CHECK(al16(partials[r]), TP_ERR_ALIGNMENT);
             d.partials[r] = partials[r];
         }
@@ -457,8 +458,8 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab, const void
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
     TP_CHECK(n >= 0 && h > 0 && vocab > 0, TP_ERR_INVALID_ARG);
     TP_CHECK(n <= INT32_MAX && vocab <= INT32_MAX && h <= INT32_MAX, TP_ERR_INVALID_ARG);
-    TP_CHECK(x != nullptr && table != nullptr, TP_ERR_INVALID_ARG);
-    TP_CHECK(logits != nullptr || shard_logits != nullptr, TP_ERR_INVALID_ARG);
+    TP_CHECK((x != nullptr || n == 0) && table != nullptr, TP_ERR_INVALID_ARG);
+    TP_CHECK(logits != nullptr || shard_logits != nullptr || n == 0, TP_ERR_INVALID_ARG);
     TP_CHECK(dtype_ok(out_dtype), TP_ERR_UNSUPPORTED);
     TP_CHECK(h % 8 == 0, TP_ERR_ALIGNMENT);
     TP_CHECK(al16(x) && ld_ok(ldx, h, 2), TP_ERR_ALIGNMENT);
@@ -478,9 +479,7 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab, const void
     d.b_rows = per;
     d.out_f32 = out_dtype == TP_F32;
     d.ldo = logits != nullptr ? ldl : 0;
-    d.status = status_ptr();
     d.pdl = 2;
-    apply_knobs(d);
     int g = 0;
     for (int r = 0; r < t; ++r) {
         const int64_t start = std::min<int64_t>(r * per, vocab);
@@ -493,7 +492,7 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab, const void
         d.n_valid[g] = rows;
         if (logits != nullptr) {
             d.out[g] = static_cast<char*>(logits) + start * eo;
-        } else {
+        } else if (n > 0) {
             TP_CHECK(shard_logits[r] != nullptr, TP_ERR_INVALID_ARG);
             TP_CHECK(al16(shard_logits[r]), TP_ERR_ALIGNMENT);
             d.out[g] = shard_logits[r];
@@ -501,6 +500,9 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab, const void
         ++g;
     }
     d.groups = g;
+    if (n == 0) return TP_OK;
+    d.status = status_ptr();
+    apply_knobs(d);
     if (logits == nullptr) {
         // per-shard buffers are contiguous [n, rows_r]: one launch per distinct width
         int first = 0;
@@ -517,12 +519,11 @@ tp_status lm_head_sharded(int t, int64_t n, int64_t h, int64_t vocab, const void
             }
             e.N = d.n_valid[first];
             e.ldo = d.n_valid[first];
-            if (n > 0) st = tpk::launch_gemm(e, cs(stream));
+            st = tpk::launch_gemm(e, cs(stream));
             first = last + 1;
         }
         return st;
     }
-    if (n == 0) return TP_OK;
     g_collectives++;
     return tpk::launch_gemm(d, cs(stream));
 }
@@ -531,7 +532,8 @@ tp_status tp_reduce_scatter_rmsnorm(int t, int64_t n, int64_t h, tp_dtype dtype,
                                     const void* residual, const void* weight, float eps, tp_reduce_mode mode,
                                     void* residual_out, void* out, tp_stream stream) {
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
-    TP_CHECK(n >= 0 && h > 0 && partials != nullptr && weight != nullptr && out != nullptr, TP_ERR_INVALID_ARG);
+    TP_CHECK(n >= 0 && h > 0 && partials != nullptr && weight != nullptr && (out != nullptr || n == 0),
+             TP_ERR_INVALID_ARG);
     TP_CHECK(mode == TP_REDUCE_DIRECT || mode == TP_REDUCE_RING, TP_ERR_INVALID_ARG);
     TP_CHECK(eps >= 0.0f, TP_ERR_INVALID_ARG);
     TP_CHECK(dtype_ok(dtype), TP_ERR_UNSUPPORTED);
@@ -541,7 +543,7 @@ tp_status tp_reduce_scatter_rmsnorm(int t, int64_t n, int64_t h, tp_dtype dtype,
                  (residual_out == nullptr || al16(residual_out)),
              TP_ERR_ALIGNMENT);
     for (int r = 0; r < t; ++r) {
-        TP_CHECK(partials[r] != nullptr, TP_ERR_INVALID_ARG);
+        TP_CHECK(partials[r] != nullptr || n == 0, TP_ERR_INVALID_ARG);
         TP_CHECK(al16(partials[r]), TP_ERR_ALIGNMENT);
     }
     if (n == 0) return TP_OK;
@@ -564,7 +566,7 @@ tp_status tp_reduce_scatter_rmsnorm(int t, int64_t n, int64_t h, tp_dtype dtype,
 tp_status tp_shard_gather(int t, int64_t rows, const int64_t* cols, tp_dtype dtype, const void* const* shards,
                           void* out, tp_stream stream) {
     TP_CHECK(t >= 1 && t <= TP_MAX_SHARDS, TP_ERR_INVALID_ARG);
-    TP_CHECK(rows >= 0 && cols != nullptr && shards != nullptr && out != nullptr, TP_ERR_INVALID_ARG);
+    TP_CHECK(rows >= 0 && cols != nullptr && shards != nullptr && (out != nullptr || rows == 0), TP_ERR_INVALID_ARG);
     TP_CHECK(dtype_ok(dtype), TP_ERR_UNSUPPORTED);
     tpk::GatherDesc d;
     d.t = t;
@@ -573,7 +575,7 @@ tp_status tp_shard_gather(int t, int64_t rows, const int64_t* cols, tp_dtype dty
     d.out = out;
     for (int r = 0; r < t; ++r) {
         TP_CHECK(cols[r] >= 0, TP_ERR_INVALID_ARG);
-        TP_CHECK(cols[r] == 0 || shards[r] != nullptr, TP_ERR_INVALID_ARG);
+        TP_CHECK(cols[r] == 0 || rows == 0 || shards[r] != nullptr, TP_ERR_INVALID_ARG);
         d.cols[r] = cols[r];
         d.shards[r] = shards[r];
     }

@@ -73,10 +73,13 @@ extern "C" tp_status tp_mlp_forward_host(int t, int64_t n, int64_t h, int64_t f,
                                          tp_dtype partial_dtype, void* x_dev, void* workspace,
                                          size_t workspace_bytes, void* y_dev, void* y_host, tp_dtype y_dtype,
                                          int chunks, tp_stream stream, tp_stream copy_stream) {
-    if (x_host == nullptr || y_host == nullptr || x_dev == nullptr || y_dev == nullptr) return TP_ERR_INVALID_ARG;
     if (chunks < 1 || chunks > 64 || n < 0 || h <= 0) return TP_ERR_INVALID_ARG;
+    if (n > 0 && (x_host == nullptr || y_host == nullptr || x_dev == nullptr || y_dev == nullptr))
+        return TP_ERR_INVALID_ARG;
     if (y_dtype != TP_BF16 && y_dtype != TP_F32) return TP_ERR_UNSUPPORTED;
-    if (n == 0) return TP_OK;
+    if (n == 0)   // nothing to copy or compute: the MLP entry point checks the other arguments
+        return tp_mlp_forward(t, 0, h, f, x_dev, h, w_gate_up, w_down, ld_down, bias_down, act, mode, partial_dtype,
+                              workspace, workspace_bytes, y_dev, y_dtype, stream);
     int64_t bounds[kMaxBlocks + 1];
     const int nblk = host_blocks(n, chunks, bounds);
     auto start = [&](int b) -> int64_t { return bounds[b]; };

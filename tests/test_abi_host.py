@@ -103,6 +103,41 @@ def test_reduce_embed_head_gather_reject_on_host(lib):
     assert lib.tp_shard_gather(2, 4, cols, 0, two, FAKE, None) == 1
 
 
+def test_zero_tokens_on_host(lib):
+    """n = 0 is a valid call: data pointers of zero rows may be NULL, the other arguments are
+    still checked, and nothing reaches CUDA (these calls run without a GPU)."""
+    w, none2 = _arr(2), _arr(2, None)
+    assert lib.tp_linear_col(2, 0, 64, 128, None, 64, w, 64, None, 1, 0, none2, 64, 0, None) == 0
+    assert lib.tp_linear_col(2, 0, 64, 128, None, 64, w, 64, None, 0, 1, none2, 128, 1, None) == 0
+    assert lib.tp_linear_col(0, 0, 64, 128, None, 64, w, 64, None, 1, 0, none2, 64, 0, None) == 1   # t still checked
+    assert lib.tp_linear_col(2, 0, 64, 128, None, 64, none2, 64, None, 1, 0, none2, 64, 0, None) == 1   # weights
+    for mode in (0, 1, 2):
+        assert lib.tp_linear_row(2, 0, 128, 64, none2, 64, w, 64, None, 1, mode, 0, none2, 64, None, 64, 0,
+                                 None) == 0
+    assert lib.tp_linear_row(2, 0, 131, 64, none2, 66, w, 66, None, 1, 0, 0, none2, 64, None, 64, 0, None) == 2
+    assert lib.tp_shard_reduce(2, 0, 0, none2, None, 0, 0, 0, 0, None) == 0
+    assert lib.tp_shard_reduce(2, 0, 1, none2, None, 0, 0, 0, 0, None) == 4          # bf16 hops on f32 data
+    for mode in (0, 2):
+        assert lib.tp_mlp_forward(2, 0, 64, 128, None, 64, w, w, 64, None, 1, mode, 0, None, 0, None, 0, None) == 0
+        assert lib.tp_mlp_forward_static(2, 0, 64, 128, None, 64, w, w, 64, None, 1, mode, 0, None, 0, None) == 0
+        assert lib.tp_mlp_forward_host(2, 0, 64, 128, None, w, w, 64, None, 1, mode, 0, None, None, 0, None, None,
+                                       0, 2, None, None) == 0
+    assert lib.tp_mlp_forward(2, 0, 64, 128, None, 64, w, w, 64, None, 0, 0, 0, None, 0, None, 0, None) == 1  # act
+    assert lib.tp_mlp_forward_host(2, 0, 64, 128, None, none2, w, 64, None, 1, 0, 0, None, None, 0, None, None,
+                                   0, 2, None, None) == 1                            # weights still checked
+    assert lib.vocab_parallel_embed(2, 10, 16, None, 0, w, 0, None, none2, None) == 0
+    assert lib.vocab_parallel_embed(2, 10, 12, None, 0, w, 0, None, None, None) == 3   # 24-byte rows
+    assert lib.lm_head_sharded(2, 0, 16, 10, None, 16, w, None, 0, None, 0, None) == 0
+    assert lib.lm_head_sharded(2, 0, 16, 10, None, 16, w, None, 0, none2, 0, None) == 0
+    assert lib.lm_head_sharded(2, 0, 12, 10, None, 16, w, None, 0, None, 0, None) == 3  # h % 8
+    cols = (ctypes.c_int64 * 2)(3, 5)
+    assert lib.tp_shard_gather(2, 0, cols, 0, none2, None, None) == 0
+    assert lib.tp_reduce_scatter_rmsnorm(2, 0, 64, 0, none2, None, FAKE, ctypes.c_float(1e-6), 0, None, None,
+                                         None) == 0
+    assert lib.tp_reduce_scatter_rmsnorm(2, 0, 64, 0, none2, None, None, ctypes.c_float(1e-6), 0, None, None,
+                                         None) == 1                                  # the weight is not row data
+
+
 def test_tuning_knobs_through_the_binding(lib):
     from megatron_tensor_layers_gb300 import TPError, tp_set_gemm_cta_pair, tp_set_gemm_split, tp_set_gemm_tile_n
     for mode in (1, -1, 0):

@@ -941,3 +941,47 @@ def test_allreduce_count_of_a_28_layer_forward(golden_dir):
     tp.lm_head_sharded(x, shards, V)
     torch.cuda.synchronize()
     assert tp.tp_collective_count() == g["prefill_forward_allreduces"] + 1
+
+
+# ------------------------------------------------------------ zero tokens
+
+def test_zero_tokens_every_entry_point():
+    """An empty batch (n = 0, empty CUDA tensors, whose data pointers may be null) is a valid
+    call of every entry point: each returns its empty outputs, launches nothing (the
+    collective counter does not move) and leaves no device error."""
+    t, h, f = 2, 256, 1024
+    fs = f // t
+    x = torch.empty((0, h), dtype=torch.bfloat16, device=DEV)
+    wgu = [normal((2 * fs, h), 0.02, 900 + r) for r in range(t)]
+    wd = [normal((h, fs), 0.02, 910 + r) for r in range(t)]
+    torch.cuda.synchronize()
+    tp.tp_reset_collective_count()
+    for mode in ("direct", "ring", "fused"):
+        assert tp.tp_mlp_forward(x, wgu, wd, mode=mode).shape == (0, h)
+        assert tp.tp_mlp_forward_static(x, wgu, wd, mode=mode).shape == (0, h)
+        assert tp.tp_linear_row([torch.empty((0, fs), dtype=torch.bfloat16, device=DEV)] * t, wd,
+                                mode=mode).shape == (0, h)
+    ys = tp.tp_linear_col(x, wgu, act="silu")
+    assert [y.shape for y in ys] == [(0, fs)] * t
+    assert tp.tp_linear_col(x, [w[:fs] for w in wgu], gather_output=True).shape == (0, f)
+    parts = [torch.empty((0,), dtype=torch.float32, device=DEV) for _ in range(t)]
+    for mode in ("direct", "ring"):
+        assert tp.tp_shard_reduce(parts, mode=mode).shape == (0,)
+    xh = torch.empty((0, h), dtype=torch.bfloat16)          # zero bytes need no page-locking
+    yh = torch.empty((0, h), dtype=torch.bfloat16)
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    assert tp.tp_mlp_forward_host(xh, wgu, wd, y_host=yh, x_dev=x, y_dev=torch.empty_like(x), workspace=ws) is yh
+    vocab = 1000
+    table = [normal(((vocab + 1) // 2, h), 1.0, 920 + r)[: min((r + 1) * 500, vocab) - r * 500] for r in range(t)]
+    table = [tb.contiguous() for tb in table]
+    ids = torch.empty((0,), dtype=torch.int32, device=DEV)
+    assert tp.vocab_parallel_embed(ids, table, vocab).shape == (0, h)
+    assert tp.lm_head_sharded(x, table, vocab).shape == (0, vocab)
+    assert [s.shape for s in tp.lm_head_sharded(x, table, vocab, per_shard=True)] == [(0, 500)] * t
+    assert tp.tp_shard_gather([torch.empty((0, c), dtype=torch.bfloat16, device=DEV) for c in (8, 16)]).shape == (0, 24)
+    sp = [torch.empty((0, h), dtype=torch.float32, device=DEV) for _ in range(t)]
+    _, out = tp.tp_reduce_scatter_rmsnorm(sp, normal((h,), 1.0, 930))
+    assert out.shape == (0, h)
+    torch.cuda.synchronize()
+    assert tp.tp_collective_count() == 0
+    assert tp.tp_device_status() == 0
