@@ -1027,15 +1027,21 @@ struct SplitCfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGING_BYTES = ROWS * BN * 4;      // fp32 accumulator rows
+    // The 64-row, 256-wide store configuration keeps its staging in the ring (five stages
+    // instead of four): valid only when every cluster runs one tile, so that no load is in
+    // flight into the ring once the tile's last MMA has completed.  Its launch checks that.
+    static constexpr bool STAGING_IN_RING = ROWS == 64 && BN == 256 && STAGES == 5;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NBARS = 2 * STAGES + 6;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NBARS * 8 + 16;
+    static constexpr int SMEM_BYTES =
+        1024 + STAGES * STAGE_BYTES + (STAGING_IN_RING ? 0 : STAGING_BYTES) + NBARS * 8 + 16;
     static constexpr int OUT_CHUNKS = (EPI == EPI_GLU ? BN / 2 : BN) / 32;   // 32-column output chunks per tile
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(ROWS == 64 || ROWS == 16 || ROWS == 8, "64, 16 or 8 staged rows");
     static_assert(STAGE_BYTES >= BM * BK * 2, "the M = 128 MMA reads 16 KB of A from the stage's start");
+    static_assert(!STAGING_IN_RING || STAGES * STAGE_BYTES >= STAGING_BYTES, "the staging fits the ring");
 };
 
 // Four fp32 accumulator values (float4 column `f4col` of `row`) summed over
@@ -1094,10 +1100,12 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_splitk_kernel(const __gri
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw_addr);
-    const uint32_t staging = base + STAGES * Cfg::STAGE_BYTES;
-    float4* staging_ptr = reinterpret_cast<float4*>(base_ptr + STAGES * Cfg::STAGE_BYTES);
-    const uint32_t bar_base = staging + Cfg::STAGING_BYTES;
-    uint8_t* bar_ptr = base_ptr + STAGES * Cfg::STAGE_BYTES + Cfg::STAGING_BYTES;
+    constexpr int kStagingOff = Cfg::STAGING_IN_RING ? 0 : STAGES * Cfg::STAGE_BYTES;
+    constexpr int kBarOff = STAGES * Cfg::STAGE_BYTES + (Cfg::STAGING_IN_RING ? 0 : Cfg::STAGING_BYTES);
+    const uint32_t staging = base + kStagingOff;
+    float4* staging_ptr = reinterpret_cast<float4*>(base_ptr + kStagingOff);
+    const uint32_t bar_base = base + kBarOff;
+    uint8_t* bar_ptr = base_ptr + kBarOff;
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
     auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
@@ -1746,17 +1754,6 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
     a.a_box_rows = static_cast<int>((d.M + 7) / 8 * 8);
     // whole segments per CTA: spread the weight reads by starting each segment's K loop elsewhere
     a.rotate_k = (d.segs > 1 && d.segs % cs == 0) ? 1 : 0;
-    const int nA = d.segs > 1 ? d.segs : (d.a_per_group ? d.groups : 1);
-    const int nB = d.segs > 1 ? d.segs : d.groups;
-    const int b_box = EPI == EPI_GLU ? BN / 2 : BN;
-    for (int i = 0; i < nA; ++i)
-        if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
-    for (int i = 0; i < nB; ++i) {
-        const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
-        const bool ok = (EPI == EPI_GLU) ? make_map_glu(&a.mapB[i], d.b[i], d.glu_up_row, d.K, d.ldb, b_box)
-                                         : make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box);
-        if (!ok) return TP_ERR_CUDA;
-    }
     auto kern = tp_gemm_splitk_kernel<BN, STAGES, EPI, KSUB, ROWS>;
     static std::atomic<uint64_t> smem_set{0};
     if (!smem_attribute_once(reinterpret_cast<const void*>(kern), Cfg::SMEM_BYTES, smem_set)) return TP_ERR_CUDA;
@@ -1786,6 +1783,19 @@ static tp_status launch_split(GemmArgs& a, const GemmDesc& d, int cs, cudaStream
         if (cached_dev) max_clusters[dev][cs].store(mc, std::memory_order_relaxed);
     }
     const int cap = d.split_clusters > 0 ? std::min(mc, d.split_clusters) : mc;
+    // staging in the ring needs one tile per cluster: the caller falls back to another configuration
+    if (Cfg::STAGING_IN_RING && a.total_tiles > cap) return TP_ERR_UNSUPPORTED;
+    const int nA = d.segs > 1 ? d.segs : (d.a_per_group ? d.groups : 1);
+    const int nB = d.segs > 1 ? d.segs : d.groups;
+    const int b_box = EPI == EPI_GLU ? BN / 2 : BN;
+    for (int i = 0; i < nA; ++i)
+        if (!make_map(&a.mapA[i], d.a[i], d.M, d.K, d.lda, a.a_box_rows)) return TP_ERR_CUDA;
+    for (int i = 0; i < nB; ++i) {
+        const int64_t rows = (d.segs == 1 && d.n_valid[i] > 0 && !d.glu) ? d.n_valid[i] : d.b_rows;
+        const bool ok = (EPI == EPI_GLU) ? make_map_glu(&a.mapB[i], d.b[i], d.glu_up_row, d.K, d.ldb, b_box)
+                                         : make_map(&a.mapB[i], d.b[i], rows, d.K, d.ldb, b_box);
+        if (!ok) return TP_ERR_CUDA;
+    }
     cfg.gridDim = dim3(cs * std::min(a.total_tiles, cap), 1, 1);
     cfg.numAttrs = d.pdl ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return TP_ERR_CUDA;
@@ -1938,7 +1948,13 @@ tp_status launch_gemm(const GemmDesc& d, cudaStream_t stream) {
             if (plan.bn == 256) return launch_split<256, 4, EPI_GLU>(a, d, cs, stream);
             return launch_split<128, 8, EPI_GLU, 2>(a, d, cs, stream);
         }
-        if (plan.bn == 256) return launch_split<256, 4, EPI_STORE>(a, d, cs, stream);
+        if (plan.bn == 256) {
+            // five stages with the staging in the ring when every cluster runs one tile (the fused
+            // down GEMM of 17-64 tokens, 32 tiles at h = 8192: about 1 % faster), else four
+            const tp_status st = launch_split<256, 5, EPI_STORE>(a, d, cs, stream);
+            if (st != TP_ERR_UNSUPPORTED) return st;
+            return launch_split<256, 4, EPI_STORE>(a, d, cs, stream);
+        }
         return launch_split<128, 8, EPI_STORE, 2>(a, d, cs, stream);
     }
     if (d.M <= 8) {    // one to eight tokens: 8-row A tiles, deeper B rings still
