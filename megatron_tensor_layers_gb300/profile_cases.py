@@ -10,7 +10,10 @@ pair2048 (prefill MLP, 2048 tokens: the CTA-pair gate_up and down GEMMs),
 fused1280 (fused down GEMM + reduce of 1280 rows given scratch: its last wave
 split along K), tiny (the tiny TP-MLP fused, t=2, h=1024, f=3072, 8 tokens: the
 one-kernel path, over 15 weight copies so that each call starts cold), qkv
-(the 70B attention QKV column GEMM at t=8, one token, two weight copies).
+(the 70B attention QKV column GEMM at t=8, one token, two weight copies),
+decode64 (70B MLP decode, t=4, 64 tokens, fused: the split-K down GEMM with five
+stages and its staging in the ring), fused200 (70B MLP, t=4, 200 tokens, fused:
+every tile of the down GEMM split along K over two CTA pairs).
 """
 
 import sys
@@ -52,6 +55,14 @@ def run(mode: str, dev: str = "cuda") -> None:
         wds = [synth.normal_bf16((H, fs), 0.02, 20 + r, device=dev) for r in range(t)]
         for m in ("direct", "fused", "direct", "fused"):
             tp.tp_mlp_forward(x, wgu, wds, mode=m, partial_dtype=torch.bfloat16)
+    elif mode in ("decode64", "fused200"):   # 70B MLP, t=4, fused reduce
+        t = 4; fs = F // t
+        n = 64 if mode == "decode64" else 200
+        x = synth.normal_bf16((n, H), 1.0, 0, device=dev)
+        wgu = [synth.normal_bf16((2 * fs, H), 0.02, 10 + r, device=dev) for r in range(t)]
+        wds = [synth.normal_bf16((H, fs), 0.02, 20 + r, device=dev) for r in range(t)]
+        ws = torch.empty(tp.tp_mlp_workspace_size(t, n, H, F, "fused"), dtype=torch.uint8, device=dev)
+        for _ in range(2): tp.tp_mlp_forward(x, wgu, wds, mode="fused", workspace=ws)
     elif mode == "pair2048":                  # prefill n=2048, t=4: gate_up + down (CTA pairs)
         t = 4; fs = F // t
         x = synth.normal_bf16((2048, H), 1.0, 0, device=dev)
