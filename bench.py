@@ -351,8 +351,8 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
-DETAIL_ROWS = ("prefill", "decode", "prefill_t8", "reduce_sweep", "seqpar", "embed", "lm_head", "tiny", "attn",
-               "host")
+DETAIL_ROWS = ("prefill", "decode", "chunked", "prefill_t8", "reduce_sweep", "seqpar", "embed", "lm_head", "tiny",
+               "attn", "host")
 
 
 def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
@@ -367,6 +367,8 @@ def bench_detail(torch, tp, synth, dev, peaks, wgu4, wds4, x, rows=DETAIL_ROWS):
         out.update(_detail_prefill(torch, tp, dev, ten, wgu4, wds4, x, y))
     if "decode" in rows:
         out.update(_detail_decode(torch, tp, dev, hbm, wgu4, wds4, x))
+    if "chunked" in rows:
+        out.update(_detail_chunked(torch, tp, dev, ten, wgu4, wds4, x))
     if "prefill_t8" in rows:
         out.update(_detail_prefill_t8(torch, tp, synth, dev, ten, y))
     if "reduce_sweep" in rows:
@@ -552,6 +554,24 @@ def _detail_decode(torch, tp, dev, hbm, wgu4, wds4, x):
             if gs:
                 rec.update({"graph_us": gs * 1e6, "graph_hbm_frac": wbytes / gs / 1e9 / hbm})
             out[f"decode_t4_n{n}_{mode}"] = rec
+    return out
+
+
+def _detail_chunked(torch, tp, dev, ten, wgu4, wds4, x):
+    """Chunked-prefill sizes of the same MLP (t=4): 200, 256 and 384 tokens, direct (separate
+    reduce) and fused (down GEMM + reduce; at 129-256 tokens every down-GEMM tile split along K
+    over two CTA pairs), timed in alternation.  Weights 1.41 GB (beyond the L2)."""
+    out = {}
+    for n in (200, 256, 384):
+        xs = x[:n].contiguous()
+        yd = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+        ws = {m: torch.empty(tp.tp_mlp_workspace_size(T, n, H, F, m, torch.bfloat16), dtype=torch.uint8, device=dev)
+              for m in ("direct", "fused")}
+        fns = {m: (lambda m=m: tp.tp_mlp_forward(xs, wgu4, wds4, mode=m, workspace=ws[m], y=yd)) for m in ws}
+        med = time_modes_interleaved(torch, fns, rounds=6, iters=5)
+        fl = 6.0 * n * H * F
+        for m, s in med.items():
+            out[f"chunked_t4_n{n}_{m}"] = {"us": s * 1e6, "tflops": fl / s / 1e12, "frac": fl / s / 1e12 / ten}
     return out
 
 
